@@ -1,0 +1,104 @@
+/*
+ * Oracle for the virtual-rank bf16 allreduce.  TEST INFRASTRUCTURE ONLY.
+ *
+ * This file is the plain, slow, single-threaded CPU definition of what the
+ * GPU library computes.  Only the test suite, the smoke check and the CPU
+ * baseline leg of the benchmark may load it; the library itself never does,
+ * and this file shares no code, header or table with the CUDA sources.
+ *
+ * What is computed.  The pages describe allreduce as "every rank's buffer
+ * summed into every rank's output":
+ *   - "optimize allreduce write mode by broadcast output ptr" (ROCm/aiter
+ *     #1910), Motivation: stage 2 writes the reduced data into every rank's
+ *     output through their output pointers;
+ *   - "One shot all reduce Example" (pytorch-labs/helion #245), performance
+ *     table: one-shot allreduce reads every peer's buffer and reduces locally;
+ *   - "Add monolithic fused packet allreduce kernel and
+ *     Model::all_reduce_packet API" (microsoft/ark #254), Changes: scatter,
+ *     reduce, broadcast fused into one kernel.
+ * None of the pages fixes the arithmetic.  The reading used everywhere here:
+ *   acc = float(in_0[i]); acc = acc + float(in_r[i]) for r = 1 .. R-1 in rank
+ *   order (plain fp32 adds, no fused multiply-add, no reassociation);
+ *   out_r[i] = round-to-nearest-even bf16 of acc, the same for every r.
+ * The accumulator is seeded with rank 0's value rather than +0.0 so that
+ * R = 1 is the identity on every bit pattern (including -0.0).
+ *
+ * Build: gcc -O2 -std=c11 -ffp-contract=off -fno-fast-math
+ *        -fexcess-precision=standard -fPIC -shared oracle.c -o liboracle.so
+ */
+#include <stddef.h>
+#include <stdint.h>
+#include <string.h>
+
+/* bf16 -> fp32 is exact: a bf16 value is the upper half of an fp32 word. */
+static float bf16_to_f32(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+/*
+ * fp32 -> bf16, IEEE 754 round to nearest, ties to even.
+ *
+ * For a finite x, the two bf16 values that bracket |x| are `lower`, the
+ * encoding whose magnitude is the largest bf16 magnitude <= |x| (the upper 16
+ * bits of x), and `lower + 1`, the next larger magnitude (which is infinity
+ * when `lower` is the largest finite bf16).  Within one binade, and across
+ * the subnormal/normal boundary, both grids are uniform and the 16 dropped
+ * bits are the distance from `lower` to |x| in units of 2^-16 of a bf16
+ * spacing, so 0x8000 is exactly the midpoint.  Nearer wins; a tie goes to
+ * the candidate with an even (zero) last significand bit.  The sign bit is
+ * carried through unchanged.
+ *
+ * NaN has no nearest value; it becomes a quiet NaN with the sign and the top
+ * payload bits kept.  +-inf maps to +-inf (dropped bits are zero).
+ */
+uint16_t oracle_f32_to_bf16_rne(float x) {
+  uint32_t u;
+  memcpy(&u, &x, sizeof u);
+  const uint32_t exponent = (u >> 23) & 0xFFu;
+  const uint32_t significand = u & 0x7FFFFFu;
+  if (exponent == 0xFFu && significand != 0u) {
+    return (uint16_t)((u >> 16) | 0x0040u);
+  }
+  const uint32_t lower = u >> 16;
+  const uint32_t dropped = u & 0xFFFFu;
+  const uint32_t midpoint = 0x8000u;
+  uint32_t result;
+  if (dropped < midpoint) {
+    result = lower;
+  } else if (dropped > midpoint) {
+    result = lower + 1u;
+  } else {
+    result = (lower & 1u) ? lower + 1u : lower;
+  }
+  return (uint16_t)result;
+}
+
+float oracle_bf16_to_f32(uint16_t b) { return bf16_to_f32(b); }
+
+/* Element-wise conversion of an array; used by the exhaustive rounding pin. */
+void oracle_f32_to_bf16_array(const float* x, uint16_t* y, size_t n) {
+  for (size_t i = 0; i < n; ++i) y[i] = oracle_f32_to_bf16_rne(x[i]);
+}
+
+/*
+ * The allreduce itself.  in[r] and out[r] are R host buffers of `count` bf16
+ * words.  For each element the inputs are read before any output at that
+ * element is written, so out[r] == in[r] (in place) is allowed.  Returns 0,
+ * or -1 on an argument outside R in [1, 64].
+ */
+int oracle_allreduce_bf16(int R, size_t count, const uint16_t* const* in,
+                          uint16_t* const* out) {
+  if (R < 1 || R > 64) return -1;
+  for (size_t i = 0; i < count; ++i) {
+    float acc = bf16_to_f32(in[0][i]);
+    for (int r = 1; r < R; ++r) {
+      acc = acc + bf16_to_f32(in[r][i]);
+    }
+    const uint16_t y = oracle_f32_to_bf16_rne(acc);
+    for (int r = 0; r < R; ++r) out[r][i] = y;
+  }
+  return 0;
+}

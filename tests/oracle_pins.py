@@ -1,0 +1,236 @@
+"""Pins for the oracle: checks against facts fixed by IEEE 754 arithmetic and
+by library routines, never against the oracle itself.
+
+Each ``pin_*`` function takes a loaded oracle library (the real one, or a
+deliberately broken copy compiled by the mutation tests) and returns a list
+of failure descriptions; an empty list means the pin holds.
+
+The pages print no numeric worked example of the reduction (their tables are
+timings), so the closed-form cases below are derived by hand from the
+definition of fp32 addition and of round-to-nearest-even; each derivation is
+written next to its case.
+"""
+from __future__ import annotations
+
+import struct
+from fractions import Fraction
+
+import numpy as np
+import torch
+
+import oracle
+from shot_allreduce_ranks_gb300 import inputs
+
+
+def bf16_bits_of(x: float) -> int:
+    """Bits of a value that is exactly representable in bf16 (checked)."""
+    u = struct.unpack("<I", struct.pack("<f", x))[0]
+    if u & 0xFFFF:
+        raise ValueError("%r is not exactly representable in bf16" % x)
+    if struct.unpack("<f", struct.pack("<I", u))[0] != x and x == x:
+        raise ValueError("%r is not exactly representable in fp32" % x)
+    return u >> 16
+
+
+def value_of_bits(b: int) -> float:
+    return struct.unpack("<f", struct.pack("<I", (b & 0xFFFF) << 16))[0]
+
+
+def run(lib, rank_bits):
+    """Allreduce a list of per-rank uint16 arrays; returns the R outputs."""
+    return oracle.allreduce_bf16([np.asarray(a, np.uint16) for a in rank_bits], lib=lib)
+
+
+def _all_equal(outs, expect):
+    return all(np.array_equal(o, expect) for o in outs)
+
+
+# --------------------------------------------------------------------------
+# R = 1 is the identity on every non-NaN bit pattern, NaN stays NaN.
+
+def pin_identity(lib):
+    fails = []
+    x = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    (y,) = run(lib, [x])
+    is_nan = ((x & 0x7F80) == 0x7F80) & ((x & 0x007F) != 0)
+    if not np.array_equal(y[~is_nan], x[~is_nan]):
+        bad = np.nonzero(y[~is_nan] != x[~is_nan])[0][:4]
+        fails.append("R=1 not identity at bit patterns %s" % [hex(int(v)) for v in x[~is_nan][bad]])
+    ynan = y[is_nan]
+    if not np.all(((ynan & 0x7F80) == 0x7F80) & ((ynan & 0x007F) != 0)):
+        fails.append("R=1 NaN input did not stay NaN")
+    return fails
+
+
+# --------------------------------------------------------------------------
+# Sums that are exact: their value does not depend on rounding or order.
+
+def pin_all_ones(lib):
+    fails = []
+    for R in range(1, 9):
+        outs = run(lib, [np.full(37, bf16_bits_of(1.0), np.uint16)] * R)
+        if not _all_equal(outs, np.full(37, bf16_bits_of(float(R)), np.uint16)):
+            fails.append("all-ones R=%d did not give exactly %d" % (R, R))
+    return fails
+
+
+def _exact_int_check(lib, R, count, seed, fill):
+    xs = inputs.make_inputs(R, count, seed, fill)
+    ints = [x.to(torch.int64).numpy() for x in xs]
+    exact = np.sum(np.stack(ints), axis=0)          # integer arithmetic
+    assert np.abs(exact).max() <= 256               # exact in bf16
+    expect = np.array([bf16_bits_of(float(v)) for v in exact.tolist()], np.uint16)
+    outs = run(lib, [inputs.bits(x) for x in xs])
+    return _all_equal(outs, expect)
+
+
+def pin_small_integers(lib):
+    fails = []
+    for R in range(1, 9):
+        for seed in (0, 1, 2):
+            if not _exact_int_check(lib, R, 1000 + 7 * R + seed, seed, "ints"):
+                fails.append("ints in [-8,8] R=%d seed=%d not summed exactly" % (R, seed))
+    return fails
+
+
+def pin_position_fill(lib):
+    fails = []
+    for R in (2, 3, 8):
+        if not _exact_int_check(lib, R, 4099, 0, "position"):
+            fails.append("position-dependent fill R=%d not summed exactly" % R)
+    return fails
+
+
+# --------------------------------------------------------------------------
+# Hand-derived closed forms (rank order, a single final rounding, ties to
+# even, signed zeros, subnormals, overflow).
+
+P24 = float(1 << 24)
+CLOSED_FORMS = [
+    # (ranks' values, exact expected result, derivation)
+    ([P24, 1.0, 1.0, -P24], 0.0,
+     "rank order: 2^24+1 is a tie between 2^24 and 2^24+2 in fp32, even -> 2^24;"
+     " +1 -> 2^24 again; -2^24 -> 0.  Any other order gives 1 or 2."),
+    ([1.0, 2.0 ** -9, 2.0 ** -9, 2.0 ** -9], 1.0 + 2.0 ** -7,
+     "fp32 sum 1+3*2^-9 is exact; one bf16 rounding (spacing 2^-7 at 1): 3/4 of a"
+     " spacing above 1 -> 1+2^-7.  Rounding after each add would stay at 1."),
+    ([1.0, 2.0 ** -8], 1.0,
+     "1+2^-8 is exactly halfway between 1 and 1+2^-7; tie to even -> 1."),
+    ([1.0 + 2.0 ** -7, 2.0 ** -8], 1.0 + 2.0 ** -6,
+     "1+2^-7+2^-8 is halfway between 1+2^-7 (odd last bit) and 1+2^-6 (even) -> 1+2^-6."),
+    ([-0.0], -0.0, "R=1 keeps the sign of zero."),
+    ([-0.0, -0.0], -0.0, "(-0)+(-0) = -0 under round to nearest."),
+    ([-0.0, 0.0], 0.0, "(-0)+(+0) = +0 under round to nearest."),
+    ([3.0, -3.0, 5.0], 5.0, "exact: 3-3 = +0, +5 = 5."),
+    ([value_of_bits(0x7F7F), value_of_bits(0x7F7F)], float("inf"),
+     "2 x largest finite bf16 (~3.39e38) exceeds the fp32 range -> +inf."),
+    ([value_of_bits(0xFF7F), value_of_bits(0xFF7F)], float("-inf"), "negative overflow -> -inf."),
+    ([value_of_bits(0x0001)] * 8, value_of_bits(0x0008),
+     "8 x smallest subnormal bf16 (2^-133) = 2^-130, exact, no flush to zero."),
+    ([value_of_bits(0x0080), -value_of_bits(0x0001)], value_of_bits(0x007F),
+     "smallest normal minus smallest subnormal = largest subnormal, exact."),
+    ([float("inf"), 1.0], float("inf"), "inf + finite = inf."),
+]
+
+
+def pin_closed_forms(lib):
+    fails = []
+    for vals, expect, why in CLOSED_FORMS:
+        xs = [np.array([bf16_bits_of(v)], np.uint16) for v in vals]
+        outs = run(lib, xs)
+        want = bf16_bits_of(expect)
+        got = [int(o[0]) for o in outs]
+        if any(g != want for g in got):
+            fails.append("closed form %s: got %s want %s (%s)"
+                         % (vals, [hex(g) for g in got], hex(want), why))
+    # inf + (-inf) is invalid: the result must be a NaN.
+    (y,) = run(lib, [np.array([0x7F80], np.uint16), np.array([0xFF80], np.uint16)])[:1]
+    if not (int(y[0]) & 0x7F80 == 0x7F80 and int(y[0]) & 0x7F):
+        fails.append("inf + -inf did not give NaN")
+    return fails
+
+
+# --------------------------------------------------------------------------
+# Rounding against a library routine (torch's fp32 -> bf16 conversion).
+
+def _rounding_subset():
+    hi = np.arange(1 << 16, dtype=np.uint32) << 16
+    lows = [0x0000, 0x0001, 0x3FFF, 0x7FFF, 0x8000, 0x8001, 0xBFFF, 0xFFFE, 0xFFFF]
+    rng = np.random.default_rng(12345)
+    lows += [int(v) for v in rng.integers(0, 1 << 16, 7)]
+    parts = [hi | np.uint32(lo) for lo in lows]
+    parts.append(rng.integers(0, 1 << 32, 1 << 22, dtype=np.uint64).astype(np.uint32))
+    return np.concatenate(parts)
+
+
+def compare_rounding(lib, u32: np.ndarray):
+    """Returns the bit patterns where the oracle and torch disagree."""
+    f = u32.view(np.float32)
+    mine = oracle.f32_to_bf16(f, lib=lib)
+    ref = torch.from_numpy(f.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    nan_in = np.isnan(f)
+    mine_nan = ((mine & 0x7F80) == 0x7F80) & ((mine & 0x7F) != 0)
+    bad = (~nan_in & (mine != ref)) | (nan_in & ~mine_nan)
+    return u32[bad]
+
+
+def pin_rounding(lib):
+    bad = compare_rounding(lib, _rounding_subset())
+    if bad.size:
+        return ["fp32->bf16 differs from torch at %s" % [hex(int(v)) for v in bad[:4]]]
+    return []
+
+
+# --------------------------------------------------------------------------
+# Whole path against library routines on tiny inputs: torch's fp32 additions
+# in rank order followed by torch's bf16 conversion.
+
+def library_rank_order_sum(xs):
+    acc = xs[0].to(torch.float32)
+    for x in xs[1:]:
+        acc = acc + x.to(torch.float32)
+    return inputs.bits(acc.to(torch.bfloat16))
+
+
+def pin_tiny_brute_force(lib):
+    fails = []
+    for R in range(1, 9):
+        for count in list(range(1, 68, 3)) + [67]:
+            xs = inputs.make_inputs(R, count, seed=R * 100 + count, fill="normal")
+            # widen the dynamic range so cancellation and rounding both occur
+            scale = torch.tensor([2.0 ** ((k % 9) - 4) for k in range(count)], dtype=torch.float32)
+            xs = [(x.float() * scale).to(torch.bfloat16) for x in xs]
+            expect = library_rank_order_sum(xs)
+            outs = run(lib, [inputs.bits(x) for x in xs])
+            if not _all_equal(outs, expect):
+                fails.append("brute force R=%d count=%d differs from torch rank-order sum" % (R, count))
+                break
+    return fails
+
+
+def pin_outputs_identical_and_in_place(lib):
+    fails = []
+    xs = [inputs.bits(x).copy() for x in inputs.make_inputs(5, 257, 3, "normal")]
+    outs = run(lib, xs)
+    if not all(np.array_equal(outs[0], o) for o in outs):
+        fails.append("ranks' outputs differ")
+    expect = library_rank_order_sum([inputs.from_bits(x) for x in xs])
+    bufs = [x.copy() for x in xs]
+    oracle.allreduce_bf16(bufs, lib=lib, outputs=bufs)
+    if not all(np.array_equal(b, expect) for b in bufs):
+        fails.append("in-place call differs from the rank-order sum")
+    return fails
+
+
+ALL_PINS = [
+    pin_identity, pin_all_ones, pin_small_integers, pin_position_fill,
+    pin_closed_forms, pin_rounding, pin_tiny_brute_force,
+    pin_outputs_identical_and_in_place,
+]
+
+
+def all_failures(lib):
+    fails = []
+    for pin in ALL_PINS:
+        fails += pin(lib)
+    return fails

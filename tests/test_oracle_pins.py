@@ -1,0 +1,86 @@
+"""The oracle against its pins (CPU only), plus mutation checks showing that
+each plausible mistake in the oracle fails at least one pin."""
+import os
+import shutil
+
+import numpy as np
+import pytest
+
+import oracle
+from tests import oracle_pins as P
+
+
+@pytest.mark.parametrize("pin", P.ALL_PINS, ids=lambda f: f.__name__)
+def test_oracle_pin(oracle_lib, pin):
+    fails = pin(oracle_lib)
+    assert not fails, "\n".join(fails)
+
+
+def test_rounding_exhaustive(oracle_lib):
+    """All 2^32 fp32 patterns against torch's conversion.  Takes ~2 minutes,
+    so it runs only when AR_EXHAUSTIVE=1; the structured subset (every upper
+    half with below/at/above-midpoint lower halves) runs always."""
+    if os.environ.get("AR_EXHAUSTIVE") != "1":
+        pytest.skip("set AR_EXHAUSTIVE=1 for the full 2^32 sweep")
+    step = 1 << 24
+    for start in range(0, 1 << 32, step):
+        u = np.arange(start, start + step, dtype=np.uint64).astype(np.uint32)
+        bad = P.compare_rounding(oracle_lib, u)
+        assert bad.size == 0, [hex(int(v)) for v in bad[:4]]
+
+
+# Each mutant is one plausible slip in oracle.c: (name, original text, replacement).
+MUTANTS = [
+    ("reversed rank order",
+     "float acc = bf16_to_f32(in[0][i]);\n    for (int r = 1; r < R; ++r) {",
+     "float acc = bf16_to_f32(in[R - 1][i]);\n    for (int r = R - 2; r >= 0; --r) {"),
+    ("accumulator seeded with +0",
+     "float acc = bf16_to_f32(in[0][i]);\n    for (int r = 1; r < R; ++r) {",
+     "float acc = 0.0f;\n    for (int r = 0; r < R; ++r) {"),
+    ("dropped last rank", "for (int r = 1; r < R; ++r)", "for (int r = 1; r < R - 1; ++r)"),
+    ("rounding after every add",
+     "acc = acc + bf16_to_f32(in[r][i]);",
+     "acc = bf16_to_f32(oracle_f32_to_bf16_rne(acc + bf16_to_f32(in[r][i])));"),
+    ("subtraction instead of addition",
+     "acc = acc + bf16_to_f32(in[r][i]);", "acc = acc - bf16_to_f32(in[r][i]);"),
+    ("shifted element index",
+     "acc = acc + bf16_to_f32(in[r][i]);", "acc = acc + bf16_to_f32(in[r][(i + 1) % count]);"),
+    ("rank index used for element", "acc = acc + bf16_to_f32(in[r][i]);",
+     "acc = acc + bf16_to_f32(in[r][i % R]);"),
+    ("only rank 0's output written", "for (int r = 0; r < R; ++r) out[r][i] = y;",
+     "out[0][i] = y; for (int r = 1; r < R; ++r) out[r][i] = 0;"),
+    ("truncation instead of rounding",
+     "} else if (dropped > midpoint) {\n    result = lower + 1u;",
+     "} else if (dropped > midpoint) {\n    result = lower;"),
+    ("ties away from zero", "result = (lower & 1u) ? lower + 1u : lower;", "result = lower + 1u;"),
+    ("ties to odd", "result = (lower & 1u) ? lower + 1u : lower;",
+     "result = (lower & 1u) ? lower : lower + 1u;"),
+    ("midpoint off by one", "const uint32_t midpoint = 0x8000u;",
+     "const uint32_t midpoint = 0x7FFFu;"),
+    ("NaN case dropped", "if (exponent == 0xFFu && significand != 0u) {",
+     "if (0) {"),
+    ("bf16 widened with the wrong shift", "uint32_t u = (uint32_t)b << 16;",
+     "uint32_t u = (uint32_t)b << 15;"),
+    ("sign bit lost in rounding", "const uint32_t lower = u >> 16;",
+     "const uint32_t lower = (u >> 16) & 0x7FFFu;"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_fails_a_pin(tmp_path, name, old, new):
+    src = open(oracle._SRC).read()
+    assert src.count(old) >= 1, "mutation target for %r no longer in oracle.c" % name
+    mutated = src.replace(old, new)
+    c = tmp_path / "oracle_mutant.c"
+    c.write_text(mutated)
+    so = str(tmp_path / ("liboracle_mutant_%d.so" % abs(hash(name))))
+    oracle.build(force=True, src=str(c), out=so)
+    lib = oracle.load(so)
+    for pin in P.ALL_PINS:
+        if pin(lib):
+            return
+    pytest.fail("mutant %r passes every pin" % name)
+
+
+def test_gcc_available():
+    assert shutil.which("gcc"), "the oracle is plain C and needs gcc"
