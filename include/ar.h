@@ -1,0 +1,222 @@
+/*
+ * ar.h -- C ABI of the GB300 virtual-rank bf16 allreduce library
+ *         (libar_gb300.so).
+ *
+ * R "virtual ranks" are R separate bf16 buffers in the HBM of ONE GPU.  An
+ * allreduce leaves, in every rank's output buffer, the element-wise sum of
+ * all R input buffers:
+ *
+ *     out_r[i] = bf16_rne( ((float)in_0[i] + (float)in_1[i]) + ... + (float)in_{R-1}[i] )
+ *
+ * for every r in [0, R) and i in [0, count): fp32 additions in rank order
+ * 0..R-1 (seeded with rank 0's value, no fused multiply-add), one final
+ * round-to-nearest-even to bf16.  Every variant below produces this result
+ * bit for bit; they differ only in how the data moves.
+ *
+ * Where each operation comes from:
+ *   - the input/output pointer tables mirror the broadcast table of output
+ *     pointers of "optimize allreduce write mode by broadcast output ptr"
+ *     (ROCm/aiter #1910, Motivation and Technical Details) and the device
+ *     array of peer pointers passed as a kernel argument in "One shot all
+ *     reduce Example" (pytorch-labs/helion #245, review discussion);
+ *   - AR_ONESHOT_PULL is the one-shot allreduce of "One shot all reduce
+ *     Example" (every rank reads all peers and reduces locally);
+ *   - AR_ONESHOT_FANOUT is that one-shot read combined with the write mode of
+ *     the aiter page (the reduced value is written straight into every
+ *     rank's output through the output-pointer table);
+ *   - AR_TWOPHASE is the two-stage allreduce of the aiter page without write
+ *     mode (stage 1 reduces a shard into its owner's output, stage 2 copies
+ *     it into the other ranks' outputs);
+ *   - AR_FUSED_LL8 is the single fused scatter -> reduce -> broadcast kernel
+ *     synchronised by LL packet flags of "Add monolithic fused packet
+ *     allreduce kernel and Model::all_reduce_packet API" (microsoft/ark #254,
+ *     Changes), with the flag rotated on every call (that page's Known
+ *     limitations leave Flag = 1 hardcoded), the grid sized to co-resident
+ *     CTAs (its NumProcs >= NPeers limitation), and the broadcast done in the
+ *     aiter write mode.
+ *
+ * Threading: a handle may be used from one host thread at a time.  Calls on
+ * one handle must be ordered on one stream (one call in flight), because a
+ * handle owns one packet scratch region and one epoch; use one handle per
+ * concurrent stream.  (The one-shot region of "Add HIP-graph capture
+ * coverage for the sharded-relay collectives" (meta-pytorch/torchcomms
+ * #3850, region-lifetime commit) has the same precondition.)
+ *
+ * Streams are passed as `void*` holding a cudaStream_t (NULL = the legacy
+ * default stream), so that this header needs no CUDA header.
+ */
+#ifndef AR_GB300_H
+#define AR_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define AR_MAX_RANKS 8
+
+typedef struct ar_ctx* ar_handle_t;
+
+typedef enum {
+  AR_BF16 = 0 /* the only element type: IEEE bfloat16, 2 bytes */
+} ar_dtype_t;
+
+typedef enum {
+  AR_OK = 0,
+  AR_ERR_INVALID_ARG = 1, /* bad R, count, pointer, variant or handle */
+  AR_ERR_UNSUPPORTED = 2, /* dtype other than AR_BF16, or no sm_103 device */
+  AR_ERR_OOM = 3,         /* device allocation failed in ar_create */
+  AR_ERR_CUDA = 4,        /* a CUDA runtime call failed (launch, copy, sync) */
+  AR_ERR_TIMEOUT = 5      /* a packet wait inside the fused kernel gave up */
+} ar_status_t;
+
+typedef enum {
+  AR_AUTO = 0,           /* per-size selector (measured table) picks one of the below */
+  AR_ONESHOT_PULL = 1,   /* CTA (chunk, r) reads all R inputs, writes out_r only */
+  AR_ONESHOT_FANOUT = 2, /* CTA reads all R inputs once, writes all R outputs */
+  AR_TWOPHASE = 3,       /* launch 1: owner shards reduced; launch 2: shards copied out */
+  AR_FUSED_LL8 = 4       /* one persistent kernel: LL8 packet scatter, poll+reduce, write mode */
+} ar_variant_t;
+
+#define AR_NUM_VARIANTS 5
+
+/* Static description of a handle (filled by ar_query). */
+typedef struct {
+  int R;                    /* virtual ranks */
+  int dtype;                /* ar_dtype_t */
+  size_t max_count;         /* largest count accepted by ar_allreduce */
+  size_t scratch_bytes;     /* LL8 packet scratch owned by the handle */
+  int num_sms;              /* SMs of the device the handle lives on */
+  int fused_max_ctas;       /* co-resident CTA limit used to size the fused grid */
+  int fused_threads;        /* threads per CTA of the fused kernel */
+  int device;               /* CUDA device ordinal */
+} ar_info_t;
+
+/*
+ * ar_create -- make a handle for R virtual ranks of up to `max_count`
+ * elements each, on the current CUDA device.
+ *   R          1 .. AR_MAX_RANKS.
+ *   max_count  >= 1; bounds `count` of later calls and sizes the scratch.
+ *   dtype      must be AR_BF16.
+ *   out        receives the handle (set to NULL on failure).
+ * Allocates, on the current device, the packet scratch
+ * (32 * R * (R-1) * ceil(ceil(max_count/8)/R) bytes, about 4*(R-1)*max_count,
+ * zeroed here so that no flag matches a live epoch) and a small state block
+ * (epoch, done counter, error word).  Synchronous; not for stream capture.
+ * Errors: AR_ERR_INVALID_ARG (R, max_count, out), AR_ERR_UNSUPPORTED (dtype,
+ * or the current device is not compute capability 10.3), AR_ERR_OOM, AR_ERR_CUDA.
+ */
+ar_status_t ar_create(int R, size_t max_count, int dtype, ar_handle_t* out);
+
+/*
+ * ar_allreduce -- out_r[i] = bf16_rne(sum over s in rank order of in_s[i])
+ * for every r < R and i < count.
+ *   h          handle from ar_create.
+ *   d_in_tbl   DEVICE pointer to an array of R device pointers (8 bytes each,
+ *              e.g. a CUDA int64 tensor of data_ptr()s); entry r is rank r's
+ *              input buffer of `count` bf16 elements, contiguous.
+ *   d_out_tbl  DEVICE pointer to an array of R device pointers; entry r is
+ *              rank r's output buffer of `count` bf16 elements.
+ *   count      elements per rank, 0 .. max_count.  0 returns AR_OK, no launch.
+ *   stream     cudaStream_t (as void*) the kernels are launched on.
+ * The caller owns the buffers and both tables; they must stay valid and
+ * unmodified until the call has completed on `stream`.  The kernels read the
+ * tables on the device, so the host never dereferences them.
+ * Aliasing: out_r may be exactly in_r (in place) for every variant, and any
+ * output may alias any input exactly in AR_ONESHOT_FANOUT.  AR_ONESHOT_PULL
+ * detects exact aliasing on the device and then writes every output from
+ * one CTA per chunk.  Partially overlapping buffers are undefined.
+ * Alignment: buffers 16-byte aligned take 16-byte vector loads and stores;
+ * any misaligned pointer switches that call to 2-byte element accesses
+ * (same result, slower), decided on the device.
+ * Allocates nothing, synchronises nothing, so it can be captured into a CUDA
+ * graph; the fused kernel's epoch lives on the device and rotates on every
+ * execution, including graph replays.
+ * Errors: AR_ERR_INVALID_ARG (NULL handle or table, count > max_count),
+ * AR_ERR_CUDA (launch failure).  A packet wait that exceeds the spin limit
+ * is reported later by ar_get_device_status (the outputs of that call are
+ * then undefined).
+ */
+ar_status_t ar_allreduce(ar_handle_t h, const void* const* d_in_tbl,
+                         void* const* d_out_tbl, size_t count, void* stream);
+
+/* ar_destroy -- synchronise the device and free everything the handle owns.
+ * NULL is accepted.  Returns AR_ERR_CUDA if a free failed. */
+ar_status_t ar_destroy(ar_handle_t h);
+
+/* ar_set_variant -- force a variant for later calls on h (AR_AUTO restores
+ * the selector).  AR_ERR_INVALID_ARG for an unknown value. */
+ar_status_t ar_set_variant(ar_handle_t h, int variant);
+
+/* ar_select -- the variant a call of `count` elements would run (the forced
+ * one, or the selector's choice under AR_AUTO).  Host-only, no device work. */
+ar_status_t ar_select(ar_handle_t h, size_t count, int* variant);
+
+/* ar_set_launch -- override the CTA count and threads per CTA of a variant
+ * (0 = automatic).  ctas is the total grid for AR_FUSED_LL8 (rounded down to
+ * a multiple of R, clamped to the co-resident limit and raised to at least
+ * R), and the grid-stride CTA count for the others.  threads must be a
+ * multiple of 32 in [64, 1024] (the fused kernel accepts 128..512). */
+ar_status_t ar_set_launch(ar_handle_t h, int variant, int ctas, int threads);
+
+/* ar_set_spin_limit_ns -- the longest a fused-kernel packet wait may spin
+ * before it gives up and sets the device error word (default 100 ms,
+ * minimum 1000 ns).  Read by each later launch. */
+ar_status_t ar_set_spin_limit_ns(ar_handle_t h, uint64_t ns);
+
+/* ar_get_device_status -- wait (bounded: at most 60 s of polling) for
+ * `stream` to drain, then read and clear the handle's device error word.
+ * AR_OK, AR_ERR_TIMEOUT if some fused call since the last check gave up
+ * waiting for packets, AR_ERR_CUDA if the stream did not drain or a copy
+ * failed. */
+ar_status_t ar_get_device_status(ar_handle_t h, void* stream);
+
+/* ar_query -- fill *info. */
+ar_status_t ar_query(ar_handle_t h, ar_info_t* info);
+
+/* ar_status_string -- static, never NULL. */
+const char* ar_status_string(int status);
+
+/* ar_variant_name -- static name of a variant ("auto", "oneshot_pull", ...),
+ * "?" for an unknown value. */
+const char* ar_variant_name(int variant);
+
+/* ---- host-buffer path (end-to-end use from host memory) ----------------
+ *
+ * ar_reserve_host_staging -- allocate, once, R input and R output device
+ * buffers of max_count elements plus their device pointer tables, used by
+ * ar_allreduce_host.  Synchronous.  AR_ERR_OOM / AR_ERR_CUDA on failure.
+ *
+ * ar_allreduce_host -- h_in[r] / h_out[r] are HOST pointers (host arrays of
+ * R host pointers; page-locked memory lets the copies run asynchronously).
+ * On `stream`: one cudaMemcpyAsync per rank into the staging inputs, the
+ * allreduce (same variant selection as ar_allreduce), one cudaMemcpyAsync
+ * per rank back into h_out[r].  Returns after enqueueing; the caller
+ * synchronises `stream` before reading h_out.  AR_ERR_INVALID_ARG if the
+ * staging was not reserved or count > max_count.
+ */
+ar_status_t ar_reserve_host_staging(ar_handle_t h);
+ar_status_t ar_allreduce_host(ar_handle_t h, const void* const* h_in,
+                              void* const* h_out, size_t count, void* stream);
+
+/* ---- test hooks (faults made on the host side) --------------------------
+ *
+ * ar_debug_skip_producer -- for the NEXT AR_FUSED_LL8 call only, virtual
+ * rank `rank` stores none of its packets, so every owner's wait for that
+ * rank runs out after the spin limit and the error word is set.  -1 clears.
+ * No memory is touched out of bounds and no wait is unbounded.
+ *
+ * ar_debug_set_epoch / ar_debug_get_epoch -- synchronous write / read of
+ * the device epoch (for testing the wrap from 2^32-1 to 1, which skips 0).
+ */
+ar_status_t ar_debug_skip_producer(ar_handle_t h, int rank);
+ar_status_t ar_debug_set_epoch(ar_handle_t h, uint32_t epoch);
+ar_status_t ar_debug_get_epoch(ar_handle_t h, uint32_t* epoch);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* AR_GB300_H */

@@ -1,0 +1,493 @@
+// C ABI of the virtual-rank allreduce: handle lifetime, argument checks, the
+// per-size variant selector and kernel launches.  Declarations and the
+// contract of every entry point are in include/ar.h.
+#include <errno.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+#include <time.h>
+
+#include <algorithm>
+#include <new>
+#include <vector>
+
+#include "ar_internal.cuh"
+
+using ar::CallArgs;
+using ar::DevState;
+using ar::FusedArgs;
+using ar::LaunchCfg;
+
+// ---------------------------------------------------------------------------
+// Selector table.  A row applies to calls with count <= max_count for its R
+// (R = 0 matches any R); the first matching row wins.  ctas / threads of 0
+// mean "use the variant's automatic launch shape".  The built-in rows are
+// the crossovers measured on GB300 (one-shot variants below, fan-out above),
+// placed where the measured curves meet, as the crossover commit of "Add
+// HIP-graph capture coverage for the sharded-relay collectives"
+// (meta-pytorch/torchcomms #3850) prescribes, and with the launch shape
+// chosen per size instead of one hardcoded block size ("One shot all reduce
+// Example", pytorch-labs/helion #245: "performance drop at 1m due to
+// hardcoded block_size").
+struct TuneRow {
+  int R;
+  size_t max_count;
+  int variant;
+  int ctas;
+  int threads;
+};
+
+static const TuneRow kBuiltinTable[] = {
+    {0, (size_t)-1, AR_ONESHOT_FANOUT, 0, 0},
+};
+
+struct ar_ctx {
+  int R = 0;
+  size_t max_count = 0;
+  int device = 0;
+  int num_sms = 0;
+  int variant = AR_AUTO;
+  LaunchCfg override_cfg[AR_NUM_VARIANTS] = {};
+  std::vector<TuneRow> table;
+  bool log = false;
+
+  DevState* state = nullptr;
+  uint64_t* scratch = nullptr;
+  size_t scratch_bytes = 0;
+  size_t slot_groups = 0;
+  uint64_t spin_limit_ns = 100ull * 1000ull * 1000ull;
+  int skip_producer = -1;
+  int fused_threads = 256;
+  int fused_ctas_per_sm = 0;   // occupancy at fused_threads
+  int occ_threads = 0;         // cache of the last occupancy query
+  int occ_value = 0;
+
+  // host-buffer path
+  uint16_t* staging = nullptr;        // 2 * R * max_count elements
+  uint16_t** staging_tables = nullptr;  // device: R input pointers, then R output pointers
+};
+
+namespace {
+
+ar_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? AR_OK : AR_ERR_CUDA; }
+
+size_t ceil_div(size_t a, size_t b) { return (a + b - 1) / b; }
+
+int parse_variant(const char* s) {
+  if (!s || !*s) return -1;
+  for (int v = 0; v < AR_NUM_VARIANTS; ++v)
+    if (strcmp(s, ar_variant_name(v)) == 0) return v;
+  char* end = nullptr;
+  long v = strtol(s, &end, 10);
+  if (end && *end == '\0' && v >= 0 && v < AR_NUM_VARIANTS) return (int)v;
+  return -1;
+}
+
+// Table file: one row per line, "R max_count variant [ctas threads]",
+// '#' starts a comment; variant by name or number.
+bool load_table_file(const char* path, std::vector<TuneRow>* rows) {
+  FILE* fp = fopen(path, "r");
+  if (!fp) return false;
+  char line[512];
+  std::vector<TuneRow> out;
+  while (fgets(line, sizeof line, fp)) {
+    char* hash = strchr(line, '#');
+    if (hash) *hash = '\0';
+    int R = 0, ctas = 0, threads = 0;
+    unsigned long long maxc = 0;
+    char vname[64] = {0};
+    int n = sscanf(line, "%d %llu %63s %d %d", &R, &maxc, vname, &ctas, &threads);
+    if (n <= 0) continue;
+    if (n < 3) {
+      fclose(fp);
+      return false;
+    }
+    int v = parse_variant(vname);
+    if (v <= AR_AUTO) {
+      fclose(fp);
+      return false;
+    }
+    out.push_back({R, (size_t)maxc, v, n >= 4 ? ctas : 0, n >= 5 ? threads : 0});
+  }
+  fclose(fp);
+  *rows = out;
+  return true;
+}
+
+const TuneRow* lookup(const ar_ctx* h, size_t count) {
+  for (const TuneRow& t : h->table)
+    if ((t.R == 0 || t.R == h->R) && count <= t.max_count) return &t;
+  return nullptr;
+}
+
+int choose(const ar_ctx* h, size_t count, const TuneRow** row) {
+  *row = nullptr;
+  if (h->variant != AR_AUTO) return h->variant;
+  const TuneRow* t = lookup(h, count);
+  *row = t;
+  return t ? t->variant : AR_ONESHOT_FANOUT;
+}
+
+// Launch shape of one call.  Threads default to 256; the grid covers the
+// groups with one group per thread, capped at 16 CTAs per SM for the
+// grid-stride variants (a multiple of R for the rank-major ones).
+LaunchCfg shape(const ar_ctx* h, int variant, const TuneRow* row, size_t groups,
+                size_t shard_groups) {
+  LaunchCfg c = {0, 0};
+  if (row && row->variant == variant) c = {row->ctas, row->threads};
+  const LaunchCfg& o = h->override_cfg[variant];
+  if (o.ctas > 0) c.ctas = o.ctas;
+  if (o.threads > 0) c.threads = o.threads;
+  const int R = h->R;
+  const size_t cap = (size_t)h->num_sms * 16;
+  switch (variant) {
+    case AR_ONESHOT_FANOUT: {
+      if (c.threads <= 0) c.threads = 256;
+      if (c.ctas <= 0) c.ctas = (int)std::min(ceil_div(groups, (size_t)c.threads), cap);
+      break;
+    }
+    case AR_ONESHOT_PULL:
+    case AR_TWOPHASE: {
+      if (c.threads <= 0) c.threads = 256;
+      const size_t span = variant == AR_ONESHOT_PULL ? groups : shard_groups;
+      if (c.ctas <= 0) {
+        const size_t chunks = std::max<size_t>(1, std::min(ceil_div(span, (size_t)c.threads),
+                                                           cap / (size_t)R));
+        c.ctas = (int)(chunks * (size_t)R);
+      } else {
+        c.ctas = std::max(R, c.ctas - c.ctas % R);
+      }
+      break;
+    }
+    case AR_FUSED_LL8: {
+      c.threads = h->fused_threads;
+      if (o.threads > 0) c.threads = o.threads;
+      int per_sm = h->fused_ctas_per_sm;
+      if (c.threads != h->fused_threads) {
+        ar_ctx* mh = const_cast<ar_ctx*>(h);
+        if (mh->occ_threads != c.threads) {
+          mh->occ_value = ar::fused_ctas_per_sm(R, c.threads);
+          mh->occ_threads = c.threads;
+        }
+        per_sm = mh->occ_value;
+      }
+      const size_t limit = (size_t)per_sm * (size_t)h->num_sms / (size_t)R;  // CTAs per rank
+      size_t per_rank = std::max<size_t>(1, ceil_div(shard_groups, (size_t)c.threads));
+      if (c.ctas > 0) per_rank = std::max<size_t>(1, (size_t)c.ctas / (size_t)R);
+      per_rank = std::min(per_rank, limit);
+      c.ctas = (int)(per_rank * (size_t)R);
+      break;
+    }
+    default:
+      break;
+  }
+  return c;
+}
+
+ar_status_t check_device(const ar_ctx* h) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return AR_ERR_CUDA;
+  return dev == h->device ? AR_OK : AR_ERR_INVALID_ARG;
+}
+
+ar_status_t launch(ar_ctx* h, int variant, const TuneRow* row, const void* const* d_in,
+                   void* const* d_out, size_t count, cudaStream_t s) {
+  CallArgs a;
+  a.in_tbl = reinterpret_cast<const uint16_t* const*>(d_in);
+  a.out_tbl = reinterpret_cast<uint16_t* const*>(d_out);
+  a.count = count;
+  a.groups = ceil_div(count, (size_t)ar::kVecElems);
+  a.shard_groups = ceil_div(a.groups, (size_t)h->R);
+  LaunchCfg cfg = shape(h, variant, row, a.groups, a.shard_groups);
+  if (h->log)
+    fprintf(stderr, "[ar] R=%d count=%zu variant=%s ctas=%d threads=%d\n", h->R, count,
+            ar_variant_name(variant), cfg.ctas, cfg.threads);
+  if (cfg.ctas <= 0 || cfg.threads <= 0) return AR_ERR_CUDA;
+  cudaError_t e = cudaErrorInvalidValue;
+  switch (variant) {
+    case AR_ONESHOT_PULL:
+      e = ar::launch_oneshot_pull(h->R, a, cfg, s);
+      break;
+    case AR_ONESHOT_FANOUT:
+      e = ar::launch_oneshot_fanout(h->R, a, cfg, s);
+      break;
+    case AR_TWOPHASE:
+      e = ar::launch_twophase(h->R, a, cfg, s);
+      break;
+    case AR_FUSED_LL8: {
+      FusedArgs f;
+      f.scratch = h->scratch;
+      f.slot_groups = h->slot_groups;
+      f.state = h->state;
+      f.spin_limit_ns = h->spin_limit_ns;
+      f.skip_producer = h->skip_producer;
+      h->skip_producer = -1;
+      e = ar::launch_fused_ll8(h->R, a, f, cfg, s);
+      break;
+    }
+    default:
+      return AR_ERR_INVALID_ARG;
+  }
+  return cuda_status(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ar_status_string(int status) {
+  switch (status) {
+    case AR_OK: return "ok";
+    case AR_ERR_INVALID_ARG: return "invalid argument";
+    case AR_ERR_UNSUPPORTED: return "unsupported dtype or device";
+    case AR_ERR_OOM: return "device out of memory";
+    case AR_ERR_CUDA: return "CUDA runtime error";
+    case AR_ERR_TIMEOUT: return "packet wait timed out on the device";
+    default: return "unknown status";
+  }
+}
+
+const char* ar_variant_name(int variant) {
+  switch (variant) {
+    case AR_AUTO: return "auto";
+    case AR_ONESHOT_PULL: return "oneshot_pull";
+    case AR_ONESHOT_FANOUT: return "oneshot_fanout";
+    case AR_TWOPHASE: return "twophase";
+    case AR_FUSED_LL8: return "fused_ll8";
+    default: return "?";
+  }
+}
+
+ar_status_t ar_create(int R, size_t max_count, int dtype, ar_handle_t* out) {
+  if (!out) return AR_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (R < 1 || R > AR_MAX_RANKS || max_count == 0) return AR_ERR_INVALID_ARG;
+  if (max_count > ((size_t)1 << 40)) return AR_ERR_INVALID_ARG;
+  if (dtype != AR_BF16) return AR_ERR_UNSUPPORTED;
+  int dev = 0, major = 0, minor = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return AR_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return AR_ERR_CUDA;
+  if (major != 10 || minor != 3) return AR_ERR_UNSUPPORTED;
+
+  ar_ctx* h = new (std::nothrow) ar_ctx();
+  if (!h) return AR_ERR_OOM;
+  h->R = R;
+  h->max_count = max_count;
+  h->device = dev;
+  h->num_sms = sms;
+  h->table.assign(kBuiltinTable, kBuiltinTable + sizeof kBuiltinTable / sizeof kBuiltinTable[0]);
+  const char* env = getenv("AR_TUNING_FILE");
+  if (env && *env && !load_table_file(env, &h->table)) {
+    fprintf(stderr, "[ar] cannot use AR_TUNING_FILE=%s; keeping the built-in table\n", env);
+  }
+  env = getenv("AR_VARIANT");
+  if (env && *env) {
+    int v = parse_variant(env);
+    if (v >= 0) h->variant = v;
+  }
+  env = getenv("AR_SPIN_LIMIT_NS");
+  if (env && *env) {
+    unsigned long long ns = strtoull(env, nullptr, 10);
+    if (ns >= 1000) h->spin_limit_ns = ns;
+  }
+  env = getenv("AR_LOG");
+  h->log = env && env[0] == '1';
+
+  const size_t groups = ceil_div(max_count, (size_t)ar::kVecElems);
+  h->slot_groups = ceil_div(groups, (size_t)R);
+  h->scratch_bytes = (size_t)R * (size_t)(R - 1) * h->slot_groups * 4 * sizeof(uint64_t);
+  h->fused_ctas_per_sm = ar::fused_ctas_per_sm(R, h->fused_threads);
+
+  ar_status_t st = AR_OK;
+  if (cudaMalloc(&h->state, sizeof(DevState)) != cudaSuccess) st = AR_ERR_OOM;
+  if (st == AR_OK && h->scratch_bytes &&
+      cudaMalloc(&h->scratch, h->scratch_bytes) != cudaSuccess)
+    st = AR_ERR_OOM;
+  if (st == AR_OK) {
+    DevState init;
+    memset(&init, 0, sizeof init);
+    init.epoch = 1;
+    if (cudaMemcpy(h->state, &init, sizeof init, cudaMemcpyHostToDevice) != cudaSuccess)
+      st = AR_ERR_CUDA;
+  }
+  if (st == AR_OK && h->scratch_bytes && cudaMemset(h->scratch, 0, h->scratch_bytes) != cudaSuccess)
+    st = AR_ERR_CUDA;
+  if (st == AR_OK && cudaDeviceSynchronize() != cudaSuccess) st = AR_ERR_CUDA;
+  if (st != AR_OK) {
+    cudaGetLastError();
+    ar_destroy(h);
+    return st;
+  }
+  *out = h;
+  return AR_OK;
+}
+
+ar_status_t ar_destroy(ar_handle_t h) {
+  if (!h) return AR_OK;
+  ar_status_t st = AR_OK;
+  int prev = -1;
+  cudaGetDevice(&prev);
+  if (prev != h->device) cudaSetDevice(h->device);
+  if (cudaDeviceSynchronize() != cudaSuccess) st = AR_ERR_CUDA;
+  if (h->scratch && cudaFree(h->scratch) != cudaSuccess) st = AR_ERR_CUDA;
+  if (h->state && cudaFree(h->state) != cudaSuccess) st = AR_ERR_CUDA;
+  if (h->staging && cudaFree(h->staging) != cudaSuccess) st = AR_ERR_CUDA;
+  if (h->staging_tables && cudaFree(h->staging_tables) != cudaSuccess) st = AR_ERR_CUDA;
+  if (prev >= 0 && prev != h->device) cudaSetDevice(prev);
+  delete h;
+  return st;
+}
+
+ar_status_t ar_set_variant(ar_handle_t h, int variant) {
+  if (!h || variant < 0 || variant >= AR_NUM_VARIANTS) return AR_ERR_INVALID_ARG;
+  h->variant = variant;
+  return AR_OK;
+}
+
+ar_status_t ar_select(ar_handle_t h, size_t count, int* variant) {
+  if (!h || !variant) return AR_ERR_INVALID_ARG;
+  const TuneRow* row = nullptr;
+  *variant = choose(h, count, &row);
+  return AR_OK;
+}
+
+ar_status_t ar_set_launch(ar_handle_t h, int variant, int ctas, int threads) {
+  if (!h || variant <= AR_AUTO || variant >= AR_NUM_VARIANTS) return AR_ERR_INVALID_ARG;
+  if (ctas < 0 || threads < 0) return AR_ERR_INVALID_ARG;
+  if (threads && (threads % 32 || threads < 64 || threads > 1024)) return AR_ERR_INVALID_ARG;
+  if (variant == AR_FUSED_LL8 && threads && (threads < 128 || threads > 512))
+    return AR_ERR_INVALID_ARG;
+  h->override_cfg[variant] = {ctas, threads};
+  return AR_OK;
+}
+
+ar_status_t ar_set_spin_limit_ns(ar_handle_t h, uint64_t ns) {
+  if (!h || ns < 1000) return AR_ERR_INVALID_ARG;
+  h->spin_limit_ns = ns;
+  return AR_OK;
+}
+
+ar_status_t ar_query(ar_handle_t h, ar_info_t* info) {
+  if (!h || !info) return AR_ERR_INVALID_ARG;
+  info->R = h->R;
+  info->dtype = AR_BF16;
+  info->max_count = h->max_count;
+  info->scratch_bytes = h->scratch_bytes;
+  info->num_sms = h->num_sms;
+  info->fused_max_ctas = h->fused_ctas_per_sm * h->num_sms;
+  info->fused_threads = h->fused_threads;
+  info->device = h->device;
+  return AR_OK;
+}
+
+ar_status_t ar_allreduce(ar_handle_t h, const void* const* d_in_tbl, void* const* d_out_tbl,
+                         size_t count, void* stream) {
+  if (!h || !d_in_tbl || !d_out_tbl) return AR_ERR_INVALID_ARG;
+  if (count > h->max_count) return AR_ERR_INVALID_ARG;
+  if (count == 0) return AR_OK;
+  ar_status_t st = check_device(h);
+  if (st != AR_OK) return st;
+  const TuneRow* row = nullptr;
+  const int v = choose(h, count, &row);
+  return launch(h, v, row, d_in_tbl, d_out_tbl, count, static_cast<cudaStream_t>(stream));
+}
+
+ar_status_t ar_get_device_status(ar_handle_t h, void* stream) {
+  if (!h) return AR_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // Bounded poll instead of an unbounded synchronise.
+  const int max_polls = 600000;  // 60 s at 100 us
+  int polls = 0;
+  cudaError_t q;
+  while ((q = cudaStreamQuery(s)) == cudaErrorNotReady) {
+    if (++polls > max_polls) return AR_ERR_CUDA;
+    struct timespec ts = {0, 100000};
+    nanosleep(&ts, nullptr);
+  }
+  if (q != cudaSuccess) return AR_ERR_CUDA;
+  DevState host;
+  if (cudaMemcpy(&host, h->state, sizeof host, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return AR_ERR_CUDA;
+  if (host.error == ar::kDevErrNone) return AR_OK;
+  const uint32_t zero[3] = {0, 0, 0};  // error, error_info, timeouts
+  if (cudaMemcpy(&h->state->error, zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+    return AR_ERR_CUDA;
+  return host.error == ar::kDevErrTimeout ? AR_ERR_TIMEOUT : AR_ERR_CUDA;
+}
+
+ar_status_t ar_reserve_host_staging(ar_handle_t h) {
+  if (!h) return AR_ERR_INVALID_ARG;
+  if (h->staging) return AR_OK;
+  const size_t per_rank = (h->max_count + 127) / 128 * 128;  // keep every buffer 256-byte aligned
+  const size_t elems = 2 * (size_t)h->R * per_rank;
+  if (cudaMalloc(&h->staging, elems * sizeof(uint16_t)) != cudaSuccess) {
+    cudaGetLastError();
+    h->staging = nullptr;
+    return AR_ERR_OOM;
+  }
+  if (cudaMalloc(&h->staging_tables, 2 * (size_t)h->R * sizeof(uint16_t*)) != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(h->staging);
+    h->staging = nullptr;
+    h->staging_tables = nullptr;
+    return AR_ERR_OOM;
+  }
+  std::vector<uint16_t*> ptrs(2 * (size_t)h->R);
+  for (size_t i = 0; i < ptrs.size(); ++i) ptrs[i] = h->staging + i * per_rank;
+  if (cudaMemcpy(h->staging_tables, ptrs.data(), ptrs.size() * sizeof(uint16_t*),
+                 cudaMemcpyHostToDevice) != cudaSuccess)
+    return AR_ERR_CUDA;
+  return AR_OK;
+}
+
+ar_status_t ar_allreduce_host(ar_handle_t h, const void* const* h_in, void* const* h_out,
+                              size_t count, void* stream) {
+  if (!h || !h_in || !h_out || !h->staging) return AR_ERR_INVALID_ARG;
+  if (count > h->max_count) return AR_ERR_INVALID_ARG;
+  if (count == 0) return AR_OK;
+  ar_status_t st = check_device(h);
+  if (st != AR_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t per_rank = (h->max_count + 127) / 128 * 128;
+  const size_t bytes = count * sizeof(uint16_t);
+  for (int r = 0; r < h->R; ++r) {
+    if (!h_in[r] || !h_out[r]) return AR_ERR_INVALID_ARG;
+    if (cudaMemcpyAsync(h->staging + (size_t)r * per_rank, h_in[r], bytes, cudaMemcpyHostToDevice,
+                        s) != cudaSuccess)
+      return AR_ERR_CUDA;
+  }
+  const TuneRow* row = nullptr;
+  const int v = choose(h, count, &row);
+  st = launch(h, v, row, reinterpret_cast<const void* const*>(h->staging_tables),
+              reinterpret_cast<void* const*>(h->staging_tables + h->R), count, s);
+  if (st != AR_OK) return st;
+  for (int r = 0; r < h->R; ++r) {
+    if (cudaMemcpyAsync(h_out[r], h->staging + (size_t)(h->R + r) * per_rank, bytes,
+                        cudaMemcpyDeviceToHost, s) != cudaSuccess)
+      return AR_ERR_CUDA;
+  }
+  return AR_OK;
+}
+
+ar_status_t ar_debug_skip_producer(ar_handle_t h, int rank) {
+  if (!h || rank < -1 || rank >= h->R) return AR_ERR_INVALID_ARG;
+  h->skip_producer = rank;
+  return AR_OK;
+}
+
+ar_status_t ar_debug_set_epoch(ar_handle_t h, uint32_t epoch) {
+  if (!h || epoch == 0) return AR_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return AR_ERR_CUDA;
+  return cuda_status(cudaMemcpy(&h->state->epoch, &epoch, sizeof epoch, cudaMemcpyHostToDevice));
+}
+
+ar_status_t ar_debug_get_epoch(ar_handle_t h, uint32_t* epoch) {
+  if (!h || !epoch) return AR_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return AR_ERR_CUDA;
+  return cuda_status(cudaMemcpy(epoch, &h->state->epoch, sizeof *epoch, cudaMemcpyDeviceToHost));
+}
+
+}  // extern "C"

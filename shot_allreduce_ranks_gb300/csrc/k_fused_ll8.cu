@@ -1,0 +1,265 @@
+// Fused LL8 packet allreduce with write-mode broadcast: one persistent kernel.
+//
+// This is the monolithic fused packet allreduce of "Add monolithic fused
+// packet allreduce kernel and Model::all_reduce_packet API" (microsoft/ark
+// #254, Changes): scatter -> reduce -> broadcast in one kernel, synchronised
+// by low-latency (LL) packet flags instead of cross-block barriers.  The R
+// virtual ranks live on one GPU, so "remote" scratch is a region of this
+// GPU's memory and the CTAs standing for a rank touch only what that rank's
+// GPU would touch: its own input, the packet slots it owns or sends to, and
+// (write mode) every rank's output.
+//
+// Work split.  The 8-element groups are split into R shards of
+// ceil(groups / R); rank o owns shard o.  The grid has G = R * C CTAs, all
+// co-resident (cooperative launch; the page's NumProcs >= NPeers limit,
+// Known limitations); CTA b stands for rank r = b % R with local index
+// c = b / R, and its threads cover groups j = c*T + t, c*T + t + C*T, ... of
+// a shard (T threads per CTA).
+//
+//   scatter (packet stores): rank r reads group j of every other owner o's
+//     shard from its own input and stores it, as four LL8 packets, into
+//     owner o's slot for source r.
+//   reduce (packet polls): owner r loads, for every other source s, the four
+//     packets of group j from its slot for s until all four carry this
+//     call's flag, takes its own input for position r, and sums the R
+//     contributions in rank order 0..R-1 in fp32.
+//   broadcast (write mode): owner r rounds once to bf16 and stores the group
+//     into all R outputs through the output-pointer table, as in "optimize
+//     allreduce write mode by broadcast output ptr" (ROCm/aiter #1910,
+//     Motivation); completion is the kernel boundary, so no packets flow
+//     back.
+//
+// LL8 packet: one 64-bit word, low 32 bits = two bf16 (lower-indexed element
+// in the low half), high 32 bits = flag.  Stores and loads are 64-bit strong
+// (relaxed, gpu scope) accesses, issued two packets per 16-byte vector
+// instruction; the memory model treats each 64-bit element as single-copy
+// atomic, so a packet whose flag matches carries that call's data.
+//
+// Flag rotation.  The ARK page leaves Flag = 1 hardcoded (Known limitations);
+// here the flag is a device-resident epoch in [1, 2^32-1].  Every CTA reads
+// it at start; the last CTA to finish (done counter) advances it, skipping 0,
+// and resets the counter.  Because the epoch never comes from the host, a
+// CUDA-graph replay rotates it too (the by-value epoch hazard G2 of "Add
+// HIP-graph capture coverage for the sharded-relay collectives",
+// meta-pytorch/torchcomms #3850), and it never rewinds while the handle
+// lives (that page's region-lifetime commit).  Scratch is zeroed at handle
+// creation, and a packet left from an earlier call carries an older epoch,
+// so it reads as not yet arrived.
+//
+// Deadlock freedom.  Every CTA finishes all of its packet stores before it
+// polls, and all CTAs are co-resident, so every poll is eventually
+// satisfied.  Every wait is still bounded: after the spin limit the thread
+// records a timeout in the device error word and abandons the call; other
+// waiters see the error word and stop too.
+#include "ar_internal.cuh"
+
+namespace ar {
+namespace {
+
+constexpr int kFusedMaxThreads = 512;
+constexpr uint32_t kMaxSpins = 1u << 24;
+
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_relaxed_u32(uint32_t* p, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Four packets of one group: flag in the high half of every 64-bit word.
+__device__ __forceinline__ void st_packets(uint64_t* p, uint4 x, uint32_t epoch) {
+  const uint64_t hi = (uint64_t)epoch << 32;
+  asm volatile("st.relaxed.gpu.global.v2.b64 [%0], {%1,%2};" ::"l"(p), "l"(hi | x.x),
+               "l"(hi | x.y)
+               : "memory");
+  asm volatile("st.relaxed.gpu.global.v2.b64 [%0], {%1,%2};" ::"l"(p + 2), "l"(hi | x.z),
+               "l"(hi | x.w)
+               : "memory");
+}
+
+struct Packets4 {
+  uint64_t w[4];
+  __device__ __forceinline__ void load(const uint64_t* p) {
+    asm volatile("ld.relaxed.gpu.global.v2.b64 {%0,%1}, [%2];" : "=l"(w[0]), "=l"(w[1]) : "l"(p));
+    asm volatile("ld.relaxed.gpu.global.v2.b64 {%0,%1}, [%2];"
+                 : "=l"(w[2]), "=l"(w[3])
+                 : "l"(p + 2));
+  }
+  __device__ __forceinline__ bool arrived(uint32_t epoch) const {
+    return (uint32_t)(w[0] >> 32) == epoch && (uint32_t)(w[1] >> 32) == epoch &&
+           (uint32_t)(w[2] >> 32) == epoch && (uint32_t)(w[3] >> 32) == epoch;
+  }
+  __device__ __forceinline__ uint4 data() const {
+    return make_uint4((uint32_t)w[0], (uint32_t)w[1], (uint32_t)w[2], (uint32_t)w[3]);
+  }
+};
+
+// Packet slot of (owner o, source s != o): sources are packed, skipping o.
+template <int R>
+__device__ __forceinline__ uint64_t* slot_base(const FusedArgs& f, int o, int s) {
+  const int slot = o * (R - 1) + (s < o ? s : s - 1);
+  return f.scratch + (size_t)slot * f.slot_groups * 4;
+}
+
+// Records the first timeout in the (sticky) error word and marks this
+// call's epoch as abandoned, so the call's other waiters stop early while
+// later calls, which carry newer epochs, are unaffected.
+__device__ __noinline__ void report_timeout(const FusedArgs& f, int owner, uint32_t pending,
+                                            uint32_t epoch) {
+  const int missing = __ffs((int)pending) - 1;
+  if (atomicCAS(&f.state->error, kDevErrNone, kDevErrTimeout) == kDevErrNone)
+    f.state->error_info = ((uint32_t)owner << 16) | (uint32_t)missing;
+  atomicAdd(&f.state->timeouts, 1u);
+  st_relaxed_u32(&f.state->abort_epoch, epoch);
+}
+
+template <int R>
+__global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, FusedArgs f) {
+  __shared__ const uint16_t* s_in[R];
+  __shared__ uint16_t* s_out[R];
+  __shared__ uint32_t s_epoch;
+  const bool vec = load_tables<R>(a, s_in, s_out);
+  if (threadIdx.x == 0) s_epoch = ld_relaxed_u32(&f.state->epoch);
+  __syncthreads();
+  const uint32_t epoch = s_epoch;
+
+  const int r = (int)(blockIdx.x % R);
+  const size_t C = gridDim.x / R;
+  const size_t t0 = (size_t)(blockIdx.x / R) * blockDim.x + threadIdx.x;
+  const size_t tstride = C * blockDim.x;
+  const size_t Vs = a.shard_groups;
+  const uint16_t* my_in = s_in[r];
+
+  // ---- scatter: packets of rank r for every other owner -------------------
+  if (R > 1 && r != f.skip_producer) {
+    for (size_t j = t0; j < Vs; j += tstride) {
+      uint4 x[R > 1 ? R - 1 : 1];
+#pragma unroll
+      for (int k = 1; k < R; ++k) {
+        const int o = (r + k) % R;
+        const size_t g = (size_t)o * Vs + j;
+        if (g < a.groups) x[k - 1] = load_group(my_in, g, group_valid(g, a.count), vec);
+      }
+#pragma unroll
+      for (int k = 1; k < R; ++k) {
+        const int o = (r + k) % R;
+        const size_t g = (size_t)o * Vs + j;
+        if (g < a.groups) st_packets(slot_base<R>(f, o, r) + j * 4, x[k - 1], epoch);
+      }
+    }
+  }
+
+  // ---- reduce + write-mode broadcast of owner r's shard -------------------
+  const size_t g0 = (size_t)r * Vs;
+  const size_t n = g0 < a.groups ? min(Vs, a.groups - g0) : 0;
+  bool aborted = false;
+  for (size_t j = t0; j < n && !aborted; j += tstride) {
+    const size_t g = g0 + j;
+    const int valid = group_valid(g, a.count);
+    const uint4 own = load_group(my_in, g, valid, vec);
+    Packets4 pk[R];
+    uint32_t pending = 0;
+#pragma unroll
+    for (int s = 0; s < R; ++s)
+      if (s != r) pk[s].load(slot_base<R>(f, r, s) + j * 4);
+#pragma unroll
+    for (int s = 0; s < R; ++s)
+      if (s != r && !pk[s].arrived(epoch)) pending |= 1u << s;
+    if (pending) {
+      uint64_t t_first = 0;
+      uint32_t spins = 0;
+      while (pending) {
+        __nanosleep(32);
+#pragma unroll
+        for (int s = 0; s < R; ++s) {
+          if (pending & (1u << s)) {
+            pk[s].load(slot_base<R>(f, r, s) + j * 4);
+            if (pk[s].arrived(epoch)) pending &= ~(1u << s);
+          }
+        }
+        if (pending && (++spins & 15u) == 0) {
+          // Give up after spin_limit_ns of %globaltimer; the iteration cap
+          // (each iteration is at least one L2 round trip) is a backstop
+          // that bounds the wait even if the timer did not advance.
+          const uint64_t now = global_timer_ns();
+          if (spins == 16u) t_first = now;
+          if (spins > kMaxSpins || (spins > 16u && now - t_first > f.spin_limit_ns)) {
+            report_timeout(f, r, pending, epoch);
+            aborted = true;
+            break;
+          }
+          if (ld_relaxed_u32(&f.state->abort_epoch) == epoch) {
+            aborted = true;
+            break;
+          }
+        }
+      }
+      if (aborted) break;
+    }
+    Acc8 acc;
+    acc.set(r == 0 ? own : pk[0].data());
+#pragma unroll
+    for (int s = 1; s < R; ++s) acc.add(s == r ? own : pk[s].data());
+    const uint4 y = acc.round_bf16();
+#pragma unroll
+    for (int q = 0; q < R; ++q) store_group(s_out[q], g, y, valid, vec);
+  }
+
+  // ---- flag rotation: the last CTA to finish advances the epoch ------------
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const uint32_t prev = atomicAdd(&f.state->done, 1u);
+    if (prev == gridDim.x - 1) {
+      __threadfence();
+      st_relaxed_u32(&f.state->done, 0u);
+      uint32_t next = epoch + 1u;
+      if (next == 0u) next = 1u;
+      st_relaxed_u32(&f.state->epoch, next);
+    }
+  }
+}
+
+}  // namespace
+
+int fused_ctas_per_sm(int R, int threads) {
+  int n = 0;
+  cudaError_t e = cudaErrorInvalidValue;
+#define Q(RR) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_fused_ll8<RR>, threads, 0)
+  switch (R) {
+    case 1: Q(1); break;
+    case 2: Q(2); break;
+    case 3: Q(3); break;
+    case 4: Q(4); break;
+    case 5: Q(5); break;
+    case 6: Q(6); break;
+    case 7: Q(7); break;
+    case 8: Q(8); break;
+    default: return 0;
+  }
+#undef Q
+  return e == cudaSuccess ? n : 0;
+}
+
+cudaError_t launch_fused_ll8(int R, const CallArgs& a, const FusedArgs& f, LaunchCfg cfg,
+                             cudaStream_t s) {
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3((unsigned)cfg.ctas);
+  lc.blockDim = dim3((unsigned)cfg.threads);
+  lc.dynamicSmemBytes = 0;
+  lc.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+#define L(RR) return cudaLaunchKernelEx(&lc, k_fused_ll8<RR>, a, f)
+  AR_RANK_SWITCH(R, L)
+#undef L
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace ar

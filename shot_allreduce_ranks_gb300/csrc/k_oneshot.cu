@@ -1,0 +1,101 @@
+// One-shot allreduce kernels: every element's R inputs are read and summed in
+// a single pass, with no intermediate buffer.
+//
+//  * pull   -- the one-shot allreduce of "One shot all reduce Example"
+//              (pytorch-labs/helion #245): the CTA standing for rank r reads
+//              the chunk from all R ranks' buffers and writes only out_r.
+//              Ranks are the fastest grid dimension, so the R CTAs reading
+//              one chunk run together and share its lines in L2.
+//  * fanout -- the same read, combined with the write mode of "optimize
+//              allreduce write mode by broadcast output ptr" (ROCm/aiter
+//              #1910, Motivation): one thread reads the 8-element group of
+//              every rank once, reduces it, and stores the result into all R
+//              outputs through the output-pointer table.  4*R*N bytes move,
+//              the minimum for this operation.
+//
+// Both handle any count (the last group may be partial) and fall back to
+// 2-byte accesses for a call whose pointers are not all 16-byte aligned.
+#include "ar_internal.cuh"
+
+namespace ar {
+namespace {
+
+template <int R>
+__device__ __forceinline__ uint4 reduce_group(const uint16_t* const* s_in, size_t g, int valid,
+                                              bool vec) {
+  uint4 x[R];
+#pragma unroll
+  for (int s = 0; s < R; ++s) x[s] = load_group(s_in[s], g, valid, vec);
+  Acc8 acc;
+  acc.set(x[0]);
+#pragma unroll
+  for (int s = 1; s < R; ++s) acc.add(x[s]);
+  return acc.round_bf16();
+}
+
+template <int R>
+__global__ void __launch_bounds__(1024) k_oneshot_fanout(CallArgs a) {
+  __shared__ const uint16_t* s_in[R];
+  __shared__ uint16_t* s_out[R];
+  const bool vec = load_tables<R>(a, s_in, s_out);
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t g = (size_t)blockIdx.x * blockDim.x + threadIdx.x; g < a.groups; g += stride) {
+    const int valid = group_valid(g, a.count);
+    const uint4 y = reduce_group<R>(s_in, g, valid, vec);
+#pragma unroll
+    for (int r = 0; r < R; ++r) store_group(s_out[r], g, y, valid, vec);
+  }
+}
+
+// gridDim.x is a multiple of R; CTA b stands for rank b % R and chunk b / R.
+// If some output pointer equals some input pointer (in-place use), a CTA
+// writing out_r could overwrite data another rank's CTA has yet to read, so
+// the kernel detects that case on the device and lets the rank-0 CTA of each
+// chunk write every output instead (the fan-out order, alias-safe).
+template <int R>
+__global__ void __launch_bounds__(1024) k_oneshot_pull(CallArgs a) {
+  __shared__ const uint16_t* s_in[R];
+  __shared__ uint16_t* s_out[R];
+  __shared__ int s_alias;
+  const bool vec = load_tables<R>(a, s_in, s_out);
+  if (threadIdx.x == 0) {
+    int alias = 0;
+    for (int r = 0; r < R; ++r)
+      for (int s = 0; s < R; ++s) alias |= (s_out[r] == s_in[s]);
+    s_alias = alias;
+  }
+  __syncthreads();
+  const bool alias = s_alias != 0;
+  const int r = (int)(blockIdx.x % R);
+  if (alias && r != 0) return;
+  const size_t chunks = gridDim.x / R;
+  const size_t stride = chunks * blockDim.x;
+  for (size_t g = (size_t)(blockIdx.x / R) * blockDim.x + threadIdx.x; g < a.groups; g += stride) {
+    const int valid = group_valid(g, a.count);
+    const uint4 y = reduce_group<R>(s_in, g, valid, vec);
+    if (alias) {
+#pragma unroll
+      for (int q = 0; q < R; ++q) store_group(s_out[q], g, y, valid, vec);
+    } else {
+      store_group(s_out[r], g, y, valid, vec);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_oneshot_fanout(int R, const CallArgs& a, LaunchCfg cfg, cudaStream_t s) {
+#define L(RR) k_oneshot_fanout<RR><<<cfg.ctas, cfg.threads, 0, s>>>(a)
+  AR_RANK_SWITCH(R, L)
+#undef L
+  return cudaGetLastError();
+}
+
+cudaError_t launch_oneshot_pull(int R, const CallArgs& a, LaunchCfg cfg, cudaStream_t s) {
+#define L(RR) k_oneshot_pull<RR><<<cfg.ctas, cfg.threads, 0, s>>>(a)
+  AR_RANK_SWITCH(R, L)
+#undef L
+  return cudaGetLastError();
+}
+
+}  // namespace ar

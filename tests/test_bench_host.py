@@ -1,0 +1,98 @@
+"""Host-side logic of bench.py without a GPU: algorithmic bytes, the
+whole-job aggregation over replicas (gloo, world size 2) and the reference
+arm (the oracle on the host cores)."""
+import json
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+
+
+def test_alg_bytes_match_the_roofline_table():
+    # R = 8, 512x8192 bf16 per rank
+    N = 512 * 8192
+    assert bench.alg_bytes("oneshot_fanout", 8, N) == 134_217_728
+    assert bench.alg_bytes("fused_ll8", 8, N) == 369_098_752
+    assert bench.alg_bytes("twophase", 8, N) == 134_217_728 + 2 * N
+    assert bench.alg_bytes("oneshot_pull", 8, N) == 2 * 64 * N + 2 * 8 * N
+    # R = 4 and R = 8 at 64 MiB per rank
+    assert bench.alg_bytes("fused_ll8", 4, 33_554_432) == 1_342_177_280
+    assert bench.alg_bytes("fused_ll8", 8, 33_554_432) == 2_952_790_016
+    assert bench.alg_bytes("twophase", 1, 100) == 400
+    assert bench.launches_per_call("twophase", 8) == 2
+    assert bench.launches_per_call("fused_ll8", 8) == 1
+
+
+def test_whole_job_aggregation():
+    # 2 ranks x 1000 calls in 0.05 s (slowest rank): 25 us per call overall
+    assert bench.whole_job_us_per_call(0.05, 1000, 2) == pytest.approx(25.0)
+    assert bench.whole_job_us_per_call(0.05, 1000, 1) == pytest.approx(50.0)
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), WORLD_SIZE=str(world),
+                      RANK=str(rank), LOCAL_RANK=str(rank))
+    w, r = bench.dist_init("gloo")
+    bench.barrier()
+    t = 0.010 * (rank + 1)               # rank 1 is the slowest
+    t_max = bench.max_over_ranks(t)
+    tot = bench.sum_over_ranks(1000.0)
+    us = bench.whole_job_us_per_call(t_max, 1000, w)
+    q.put((r, w, t_max, tot, us))
+    import torch.distributed as dist
+    dist.destroy_process_group()
+
+
+def test_replica_timing_over_gloo_world_size_2():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for r, w, t_max, tot, us in res:
+        assert w == 2
+        assert t_max == pytest.approx(0.020)     # max over ranks
+        assert tot == pytest.approx(2000.0)
+        assert us == pytest.approx(10.0)         # 2000 calls in 20 ms
+
+
+def test_reference_arm_prints_one_line(capsys, monkeypatch):
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    bench.main(["--impl", "reference", "--steps", "3", "--warmup", "3",
+                "--workload", "r8_4096"])
+    out = capsys.readouterr().out.strip().splitlines()
+    assert len(out) == 1
+    line = json.loads(out[0])
+    assert line["impl"] == "reference" and line["unit"] == "us/call"
+    assert line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
+    assert line["config"]["workload"] == "r8_4096"
+
+
+def test_reference_arm_other_ranks_stay_silent(capsys, monkeypatch):
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    bench.main(["--impl", "reference", "--steps", "3", "--warmup", "3"])
+    assert capsys.readouterr().out == ""
+
+
+def test_warmup_floor():
+    with pytest.raises(SystemExit):
+        bench.parse_args(["--warmup", "2"])

@@ -1,0 +1,123 @@
+"""Fused LL8 kernel: flag rotation, stale-packet rejection, bounded waits
+(made to run out from the host side, no GPU fault), epoch wrap and CUDA-graph
+replay."""
+import pytest
+import torch
+
+from shot_allreduce_ranks_gb300 import inputs
+from shot_allreduce_ranks_gb300._lib import AR_ERR_TIMEOUT, AR_OK
+from tests import gpu_helpers as G
+
+pytestmark = pytest.mark.gpu
+
+R, COUNT = 8, 65_536 * 8 + 11
+
+
+@pytest.fixture(scope="module")
+def ar():
+    h = G.handle(R, COUNT)
+    h.set_variant("fused_ll8")
+    yield h
+    h.set_spin_limit_ns(100_000_000)
+    G.release_handles()
+
+
+def _bufs(xs):
+    bufs = G.to_device(xs)
+    return bufs, [torch.empty_like(b) for b in bufs]
+
+
+def test_epoch_advances_once_per_call(ar):
+    xs = inputs.make_inputs(R, COUNT, 1)
+    bufs, outs = _bufs(xs)
+    e0 = ar.debug_get_epoch()
+    for _ in range(5):
+        ar(bufs, outs)
+    assert ar.debug_get_epoch() == e0 + 5
+    G.check_all_outputs(outs, G.oracle_expect(xs), "after 5 calls")
+
+
+def test_epoch_wraps_to_one_skipping_zero(ar):
+    xs = inputs.make_inputs(R, COUNT, 2)
+    want = G.oracle_expect(xs)
+    bufs, outs = _bufs(xs)
+    ar.debug_set_epoch(0xFFFFFFFE)
+    ar(bufs, outs)
+    assert ar.debug_get_epoch() == 0xFFFFFFFF
+    G.check_all_outputs(outs, want, "epoch 2^32-2")
+    ar(bufs, outs)
+    assert ar.debug_get_epoch() == 1
+    G.check_all_outputs(outs, want, "epoch 2^32-1")
+    ar(bufs, outs)
+    assert ar.debug_get_epoch() == 2
+    G.check_all_outputs(outs, want, "epoch 1 after wrap")
+
+
+@pytest.mark.parametrize("skip", [0, 3, R - 1])
+def test_missing_producer_times_out_and_next_call_recovers(ar, skip):
+    """Rank `skip` stores no packets for one call: its owners' waits run out
+    after the (short) spin limit, the device error word says so, and the
+    next call, with a newer epoch, is correct."""
+    xs = inputs.make_inputs(R, COUNT, 3)
+    want = G.oracle_expect(xs)
+    bufs, outs = _bufs(xs)
+    assert ar.device_status() == AR_OK
+    ar.set_spin_limit_ns(2_000_000)
+    ar.debug_skip_producer(skip)
+    ar(bufs, outs)
+    assert ar.device_status() == AR_ERR_TIMEOUT
+    assert ar.device_status() == AR_OK  # reading clears it
+    ar(bufs, outs)
+    assert ar.device_status() == AR_OK
+    G.check_all_outputs(outs, want, "call after a timeout")
+    ar.set_spin_limit_ns(100_000_000)
+
+
+def test_stale_packets_are_rejected(ar):
+    """Call A fills every packet slot with epoch e.  Call B (epoch e+1) gets
+    no packets from rank 2: with a constant flag (Flag = 1) it would consume
+    A's packets and return A's data silently; with rotation it must time out."""
+    xa = inputs.make_inputs(R, COUNT, 4)
+    bufs, outs = _bufs(xa)
+    ar(bufs, outs)
+    assert ar.device_status() == AR_OK
+    xb = inputs.make_inputs(R, COUNT, 5)
+    for b, x in zip(bufs, xb):
+        b.copy_(x)
+    ar.set_spin_limit_ns(2_000_000)
+    ar.debug_skip_producer(2)
+    ar(bufs, outs)
+    assert ar.device_status() == AR_ERR_TIMEOUT
+    ar.set_spin_limit_ns(100_000_000)
+    ar(bufs, outs)
+    assert ar.device_status() == AR_OK
+    G.check_all_outputs(outs, G.oracle_expect(xb), "after stale-packet timeout")
+
+
+def test_graph_replay_with_changing_inputs(ar):
+    """Capture one fused call into a CUDA graph, then replay it with inputs
+    that change between replays.  The epoch lives on the device, so every
+    replay rotates it (a by-value epoch would be baked into the graph)."""
+    bufs = [torch.empty(COUNT, dtype=torch.bfloat16, device=G.DEV) for _ in range(R)]
+    outs = [torch.empty_like(b) for b in bufs]
+    in_tbl, out_tbl = ar.tables(bufs, outs)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        ar.allreduce_tables(in_tbl, out_tbl, COUNT)  # warm-up outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        ar.allreduce_tables(in_tbl, out_tbl, COUNT)
+    torch.cuda.synchronize()
+    e0 = ar.debug_get_epoch()
+    for rep in range(6):
+        xs = inputs.make_inputs(R, COUNT, 50 + rep)
+        for b, x in zip(bufs, xs):
+            b.copy_(x)
+        g.replay()
+        torch.cuda.synchronize()
+        G.check_all_outputs(outs, G.oracle_expect(xs), "replay %d" % rep)
+    assert ar.debug_get_epoch() == e0 + 6
+    assert ar.device_status() == AR_OK

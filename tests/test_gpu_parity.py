@@ -1,0 +1,254 @@
+"""CUDA path vs oracle, bit for bit (tolerance 0 ULP), through the C ABI.
+
+Every variant must produce exactly the oracle's result: fp32 accumulation in
+rank order 0..R-1 and one round-to-nearest-even to bf16, identical in every
+rank's output.  Where floating point could decide nothing else, NaN payloads
+are the only freedom (any NaN equals any NaN).
+"""
+import numpy as np
+import pytest
+import torch
+
+from shot_allreduce_ranks_gb300 import ArError, inputs
+from shot_allreduce_ranks_gb300._lib import AR_ERR_INVALID_ARG
+from tests import gpu_helpers as G
+from tests import oracle_pins as P
+
+pytestmark = pytest.mark.gpu
+
+RAGGED = [1, 7, 8, 9, 63, 4095, 4097, 3 * 65536 + 5]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cleanup():
+    yield
+    G.release_handles()
+
+
+@pytest.mark.parametrize("variant", G.PARITY_VARIANTS)
+@pytest.mark.parametrize("R", [1, 2, 3, 5, 8])
+def test_ragged_counts(variant, R):
+    ar = G.handle(R, max(RAGGED))
+    for count in RAGGED:
+        xs = inputs.make_inputs(R, count, seed=count % 7, fill="normal")
+        want = G.oracle_expect(xs)
+        outs = G.run_variant(ar, G.to_device(xs), variant)
+        G.check_all_outputs(outs, want, "%s R=%d count=%d" % (variant, R, count))
+
+
+FULL = ["r8_4096", "r8_440x5120", "r8_512x5120", "r8_512x7168", "r8_512x8192",
+        "r8_632x5120", "r8_680x5120"] + [
+    n for n in inputs.WORKLOADS if n.startswith("r8_") and n.endswith(("_ints", "_normal"))
+] + ["r4_64mib", "r8_64mib"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_configs(name):
+    """Every benchmark workload at its full size, default launch shapes (the
+    ones bench.py times), every variant plus the selector, all outputs."""
+    w = inputs.WORKLOADS[name]
+    ar = G.handle(w.R, w.count)
+    seeds = (0, 1, 2) if w.count <= (1 << 20) else (0,)
+    for seed in seeds:
+        xs = inputs.make_inputs(w.R, w.count, seed, w.fill)
+        want = G.oracle_expect(xs)
+        xd = G.to_device(xs)
+        outs = [torch.empty_like(x) for x in xd]
+        for variant in G.PARITY_VARIANTS + ["auto"]:
+            for o in outs:
+                o.fill_(float("nan"))
+            G.run_variant(ar, xd, variant, outs)
+            G.check_all_outputs(outs, want, "%s %s seed=%d" % (name, variant, seed))
+        del xd, outs
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("variant", G.PARITY_VARIANTS)
+def test_exact_integer_sums_without_oracle(variant):
+    """Integers in [-8, 8] sum exactly: pins the GPU independently of the oracle."""
+    R, count = 8, 1 << 20
+    ar = G.handle(R, count)
+    for fill in ("ints", "position"):
+        xs = inputs.make_inputs(R, count, seed=5, fill=fill)
+        exact = torch.stack([x.to(torch.int64) for x in xs]).sum(0)
+        want = inputs.bits(exact.to(torch.bfloat16))
+        outs = G.run_variant(ar, G.to_device(xs), variant)
+        G.check_all_outputs(outs, want, "%s %s" % (variant, fill))
+
+
+@pytest.mark.parametrize("variant", G.PARITY_VARIANTS)
+def test_closed_forms_on_gpu(variant):
+    """The hand-derived closed forms of the oracle pins hold on the GPU too
+    (rank order, single rounding, ties to even, signed zero, subnormals,
+    overflow, infinities, NaN)."""
+    cases = P.CLOSED_FORMS + [([float("inf"), float("-inf")], None, "NaN")]
+    for vals, expect, why in cases:
+        R = len(vals)
+        ar = G.handle(R, 64)
+        # the same case in every element of a 3-group buffer, ragged tail
+        count = 21
+        xs = [inputs.from_bits(np.full(count, P.bf16_bits_of(v), np.uint16)) for v in vals]
+        outs = G.run_variant(ar, G.to_device(xs), variant)
+        for o in outs:
+            got = G.device_bits(o)
+            if expect is None:
+                assert G.is_nan_bits(got).all(), (variant, vals)
+            else:
+                want = np.full(count, P.bf16_bits_of(expect), np.uint16)
+                G.assert_bitexact(got, want, "%s %s (%s)" % (variant, vals, why))
+
+
+@pytest.mark.parametrize("variant", G.PARITY_VARIANTS)
+def test_special_values_mixed(variant):
+    """Random bit patterns (all classes: subnormal, huge, inf, NaN) vs oracle."""
+    R, count = 8, 40_000
+    rng = np.random.default_rng(7)
+    xs = [inputs.from_bits(rng.integers(0, 1 << 16, count, dtype=np.uint64).astype(np.uint16))
+          for _ in range(R)]
+    want = G.oracle_expect(xs)
+    outs = G.run_variant(G.handle(R, count), G.to_device(xs), variant)
+    G.check_all_outputs(outs, want, variant)
+
+
+@pytest.mark.parametrize("variant", G.PARITY_VARIANTS)
+@pytest.mark.parametrize("which", ["inputs", "outputs", "both"])
+def test_misaligned_pointers(variant, which):
+    """Pointers offset by one element (2 bytes): the call takes the element
+    path and still matches."""
+    R, count = 8, 4099
+    ar = G.handle(R, count + 8)
+    xs = inputs.make_inputs(R, count, seed=11, fill="normal")
+    want = G.oracle_expect(xs)
+    base_in = [torch.empty(count + 8, dtype=torch.bfloat16, device=G.DEV) for _ in range(R)]
+    base_out = [torch.empty(count + 8, dtype=torch.bfloat16, device=G.DEV) for _ in range(R)]
+    off_in = 1 if which in ("inputs", "both") else 0
+    off_out = 1 if which in ("outputs", "both") else 0
+    xin = [b[off_in:off_in + count] for b in base_in]
+    xout = [b[off_out:off_out + count] for b in base_out]
+    for d, x in zip(xin, xs):
+        d.copy_(x)
+    G.run_variant(ar, xin, variant, xout)
+    G.check_all_outputs(xout, want, "%s misaligned %s" % (variant, which))
+
+
+@pytest.mark.parametrize("variant", G.PARITY_VARIANTS)
+def test_in_place(variant):
+    R, count = 8, (1 << 20) + 3
+    ar = G.handle(R, count)
+    xs = inputs.make_inputs(R, count, seed=3, fill="normal")
+    want = G.oracle_expect(xs)
+    bufs = G.to_device(xs)
+    G.run_variant(ar, bufs, variant, bufs)
+    G.check_all_outputs(bufs, want, "%s in place" % variant)
+
+
+@pytest.mark.parametrize("variant", G.PARITY_VARIANTS)
+def test_guard_canaries(variant):
+    """Nothing is written outside [0, count) of any output."""
+    R, count, pad = 8, 1000 * 8 + 5, 64
+    ar = G.handle(R, count)
+    xs = inputs.make_inputs(R, count, seed=2, fill="normal")
+    want = G.oracle_expect(xs)
+    bases = [torch.full((count + 2 * pad,), 12345.0, dtype=torch.bfloat16, device=G.DEV)
+             for _ in range(R)]
+    outs = [b[pad:pad + count] for b in bases]
+    G.run_variant(ar, G.to_device(xs), variant, outs)
+    G.check_all_outputs(outs, want, variant)
+    canary = inputs.bits(torch.tensor([12345.0], dtype=torch.bfloat16))[0]
+    for b in bases:
+        bits = G.device_bits(b)
+        assert (bits[:pad] == canary).all() and (bits[pad + count:] == canary).all()
+
+
+def test_back_to_back_calls_with_changing_inputs():
+    """Twenty fused calls in a row on one stream, inputs changing every call,
+    no synchronisation between them: a stale flag or stale packet would show
+    up as wrong data in some call."""
+    R, count = 8, 300_000 + 3
+    ar = G.handle(R, count)
+    ar.set_variant("fused_ll8")
+    bufs = [torch.empty(count, dtype=torch.bfloat16, device=G.DEV) for _ in range(R)]
+    outs = [torch.empty_like(b) for b in bufs]
+    in_tbl, out_tbl = ar.tables(bufs, outs)
+    snaps, wants = [], []
+    for call in range(20):
+        xs = inputs.make_inputs(R, count, seed=100 + call, fill="normal")
+        wants.append(G.oracle_expect(xs))
+        for b, x in zip(bufs, xs):
+            b.copy_(x, non_blocking=False)
+        ar.allreduce_tables(in_tbl, out_tbl, count)
+        snaps.append([o.clone() for o in outs])
+    torch.cuda.synchronize()
+    for call, (snap, want) in enumerate(zip(snaps, wants)):
+        G.check_all_outputs(snap, want, "call %d" % call)
+
+
+def test_fused_launch_shapes():
+    """The fused kernel is correct for every CTA count it can be given,
+    down to one CTA per rank, and for 128/256/512 threads."""
+    R, count = 8, 200_003
+    ar = G.handle(R, count)
+    xs = inputs.make_inputs(R, count, seed=9, fill="normal")
+    want = G.oracle_expect(xs)
+    xd = G.to_device(xs)
+    for threads in (128, 256, 512):
+        for ctas in (R, 3 * R, 64, 152 * 2, 0):
+            ar.set_launch("fused_ll8", ctas, threads)
+            outs = G.run_variant(ar, xd, "fused_ll8")
+            G.check_all_outputs(outs, want, "fused ctas=%d threads=%d" % (ctas, threads))
+    ar.set_launch("fused_ll8", 0, 0)
+
+
+@pytest.mark.parametrize("variant", ["oneshot_pull", "oneshot_fanout", "twophase"])
+def test_grid_stride_shapes(variant):
+    R, count = 8, 100_001
+    ar = G.handle(R, count)
+    xs = inputs.make_inputs(R, count, seed=4, fill="normal")
+    want = G.oracle_expect(xs)
+    xd = G.to_device(xs)
+    for ctas, threads in ((1, 64), (R, 128), (40, 1024), (0, 512)):
+        ar.set_launch(variant, ctas, threads)
+        outs = G.run_variant(ar, xd, variant)
+        G.check_all_outputs(outs, want, "%s ctas=%d threads=%d" % (variant, ctas, threads))
+    ar.set_launch(variant, 0, 0)
+
+
+def test_count_zero_and_bounds():
+    R = 4
+    ar = G.handle(R, 1000)
+    xs = G.to_device(inputs.make_inputs(R, 1000, 0))
+    outs = [torch.full_like(x, 7.0) for x in xs]
+    ar(xs, outs, count=0)
+    torch.cuda.synchronize()
+    assert all((o == 7.0).all() for o in outs)
+    in_tbl, out_tbl = ar.tables(xs, outs)
+    with pytest.raises(ArError) as e:
+        ar.allreduce_tables(in_tbl, out_tbl, 1001)
+    assert e.value.status == AR_ERR_INVALID_ARG
+
+
+def test_selector_picks_a_real_variant_and_matches():
+    R = 8
+    ar = G.handle(R, 1 << 22)
+    ar.set_variant("auto")
+    for count in (4096, 65536, 1 << 20, 1 << 22):
+        assert ar.select(count) in G.PARITY_VARIANTS
+        xs = inputs.make_inputs(R, count, seed=1)
+        outs = G.run_variant(ar, G.to_device(xs), "auto")
+        G.check_all_outputs(outs, G.oracle_expect(xs), "auto count=%d" % count)
+
+
+def test_host_buffer_path():
+    R, count = 8, 123_457
+    ar = G.handle(R, count)
+    ar.reserve_host_staging()
+    xs = inputs.make_inputs(R, count, seed=6)
+    want = G.oracle_expect(xs)
+    hin = [x.pin_memory() for x in xs]
+    hout = [torch.empty(count, dtype=torch.bfloat16).pin_memory() for _ in range(R)]
+    for variant in G.PARITY_VARIANTS:
+        ar.set_variant(variant)
+        ar.allreduce_host(hin, hout)
+        torch.cuda.synchronize()
+        for r in range(R):
+            G.assert_bitexact(inputs.bits(hout[r]), want, "host path %s rank %d" % (variant, r))
