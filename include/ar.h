@@ -215,6 +215,47 @@ ar_status_t ar_debug_skip_producer(ar_handle_t h, int rank);
 ar_status_t ar_debug_set_epoch(ar_handle_t h, uint32_t epoch);
 ar_status_t ar_debug_get_epoch(ar_handle_t h, uint32_t* epoch);
 
+/* ---- allocation-free entry point ----------------------------------------
+ *
+ * The pages have no counterpart to this call; it exists for callers of this
+ * library that cannot allocate device memory themselves, so cannot use
+ * ar_create: for example a plugin running inside a host framework whose
+ * allocator has already reserved the device memory budget and forbids side
+ * allocations, or a process that must not allocate once it has started
+ * serving.
+ *
+ * ar_allreduce_fused_noalloc -- the AR_FUSED_LL8 allreduce without a handle.
+ * Same arguments and result as ar_allreduce (R = rank count, 1..AR_MAX_RANKS;
+ * device pointer tables; count elements per rank; stream), but the packet
+ * scratch and the epoch/counter/error block live in fixed arrays inside the
+ * library's device image (AR_NOALLOC_SCRATCH_BYTES of scratch plus 64 bytes),
+ * which every GPU that loads the library holds until the process exits.  It
+ * calls no cudaMalloc, cudaFree or other allocating routine.
+ *   - The first call on each device sets that device up, synchronously:
+ *     it looks up the arrays' device addresses, zeroes the scratch and
+ *     starts the epoch at 1.  Make that first call before any stream capture.
+ *   - count must be <= AR_NOALLOC_MAX_COUNT(R) (about 1.19 M elements for
+ *     R = 8, 8.4 M for R = 2, no limit for R = 1); a larger count returns
+ *     AR_ERR_INVALID_ARG and launches nothing.  count = 0 returns AR_OK.
+ *   - Every call on a device shares the one array and the one epoch, which
+ *     keep the last call's contents; the kernel needs nothing cleared between
+ *     calls (stale packets carry older epochs, the done counter is left at 0
+ *     by the call before).  Calls that overlap on the GPU (other streams, or
+ *     other threads) race on the array and give wrong results: order them.
+ *   - A packet wait that gives up (100 ms) is recorded in the device-side
+ *     error word, which no entry point reads back for this call; that call's
+ *     outputs are then undefined.
+ * Errors: AR_ERR_INVALID_ARG (R, NULL table, count too large),
+ * AR_ERR_UNSUPPORTED (device ordinal >= 64), AR_ERR_CUDA (set-up or launch).
+ */
+#define AR_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+#define AR_NOALLOC_MAX_COUNT(R)                                                   \
+  ((R) <= 1 ? (size_t)-1                                                          \
+            : (AR_NOALLOC_SCRATCH_BYTES / ((size_t)32 * (size_t)(R) * (size_t)((R)-1))) * \
+                  (size_t)8 * (size_t)(R))
+ar_status_t ar_allreduce_fused_noalloc(int R, const void* const* d_in_tbl,
+                                       void* const* d_out_tbl, size_t count, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

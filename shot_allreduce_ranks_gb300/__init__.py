@@ -12,7 +12,7 @@ import ctypes
 from ._lib import (AR_AUTO, AR_FUSED_LL8, AR_ONESHOT_FANOUT, AR_ONESHOT_PULL,  # noqa: F401
                    AR_TWOPHASE, AR_MAX_RANKS, VARIANTS, ArError, ArInfo, check, load)
 
-__all__ = ["AllReduce", "ArError", "VARIANTS", "load"]
+__all__ = ["AllReduce", "ArError", "VARIANTS", "allreduce_fused_noalloc", "load"]
 
 
 def _variant_id(v) -> int:
@@ -170,3 +170,19 @@ class AllReduce:
         e = ctypes.c_uint32()
         check(self._lib.ar_debug_get_epoch(self._h, ctypes.byref(e)), "ar_debug_get_epoch")
         return e.value
+
+
+def allreduce_fused_noalloc(R: int, in_tbl, out_tbl, count: int, stream=None) -> None:
+    """Fused LL8 allreduce for callers that cannot allocate device memory.
+
+    No handle: the packet scratch is a fixed array inside the library's
+    device image, set up on the first call per device (make that call before
+    any stream capture).  ``in_tbl`` / ``out_tbl`` are device int64 tensors
+    (or addresses) of R buffer pointers; ``count`` must not exceed
+    ``_lib.noalloc_max_count(R)``.  Calls that overlap on the GPU race.
+    """
+    lib = load()
+    ip = in_tbl if isinstance(in_tbl, int) else in_tbl.data_ptr()
+    op = out_tbl if isinstance(out_tbl, int) else out_tbl.data_ptr()
+    check(lib.ar_allreduce_fused_noalloc(int(R), ip, op, int(count), _stream_handle(stream)),
+          "ar_allreduce_fused_noalloc")

@@ -63,7 +63,18 @@ PROTOTYPES = {
     "ar_debug_skip_producer": (_ST, [_H, _I]),
     "ar_debug_set_epoch": (_ST, [_H, ctypes.c_uint32]),
     "ar_debug_get_epoch": (_ST, [_H, ctypes.POINTER(ctypes.c_uint32)]),
+    "ar_allreduce_fused_noalloc": (_ST, [_I, _VP, _VP, _SZ, _VP]),
 }
+
+AR_NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def noalloc_max_count(R: int) -> int:
+    """Largest count ar_allreduce_fused_noalloc accepts for R ranks."""
+    if R <= 1:
+        return (1 << 64) - 1
+    return (AR_NOALLOC_SCRATCH_BYTES // (32 * R * (R - 1))) * 8 * R
+
 
 _lock = threading.Lock()
 _lib = None

@@ -51,6 +51,11 @@
 // satisfied.  Every wait is still bounded: after the spin limit the thread
 // records a timeout in the device error word and abandons the call; other
 // waiters see the error word and stop too.
+#include <string.h>
+
+#include <algorithm>
+#include <mutex>
+
 #include "ar_internal.cuh"
 
 namespace ar {
@@ -263,3 +268,98 @@ cudaError_t launch_fused_ll8(int R, const CallArgs& a, const FusedArgs& f, Launc
 }
 
 }  // namespace ar
+
+// ---------------------------------------------------------------------------
+// Allocation-free entry point: the same fused kernel, with its packet
+// scratch and its epoch/counter/error block in fixed device arrays that the
+// library image carries, instead of memory a handle allocates.  Every GPU
+// that loads this library holds these arrays (AR_NOALLOC_SCRATCH_BYTES plus
+// 64 bytes) until the process exits.
+
+namespace {
+
+constexpr size_t kNoAllocWords = AR_NOALLOC_SCRATCH_BYTES / sizeof(uint64_t);
+static __device__ __align__(256) uint64_t g_noalloc_scratch[kNoAllocWords];
+static __device__ __align__(256) ar::DevState g_noalloc_state;
+
+constexpr int kNoAllocMaxDevices = 64;
+constexpr int kNoAllocThreads = 256;
+
+struct NoAllocDevice {
+  bool ready;
+  uint64_t* scratch;     // device address of g_noalloc_scratch on this device
+  ar::DevState* state;   // device address of g_noalloc_state on this device
+  int sms;
+  int ctas_per_sm[AR_MAX_RANKS + 1];
+};
+
+NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
+std::mutex g_noalloc_mu;
+
+// Once per device, with that device current: look up the arrays' device
+// addresses (in host code their names are host-side stand-ins, not device
+// addresses), zero the scratch so no stale word can carry a live flag, and
+// start the epoch at 1.  Synchronous; allocates nothing.
+ar_status_t noalloc_setup(int dev, int R, NoAllocDevice* out) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  NoAllocDevice& d = g_noalloc_dev[dev];
+  if (!d.ready) {
+    void* scratch = nullptr;
+    void* state = nullptr;
+    if (cudaGetSymbolAddress(&scratch, g_noalloc_scratch) != cudaSuccess) return AR_ERR_CUDA;
+    if (cudaGetSymbolAddress(&state, g_noalloc_state) != cudaSuccess) return AR_ERR_CUDA;
+    ar::DevState init;
+    memset(&init, 0, sizeof init);
+    init.epoch = 1;
+    int sms = 0;
+    if (cudaMemset(scratch, 0, AR_NOALLOC_SCRATCH_BYTES) != cudaSuccess ||
+        cudaMemcpy(state, &init, sizeof init, cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return AR_ERR_CUDA;
+    d.scratch = static_cast<uint64_t*>(scratch);
+    d.state = static_cast<ar::DevState*>(state);
+    d.sms = sms;
+    d.ready = true;
+  }
+  if (d.ctas_per_sm[R] == 0) d.ctas_per_sm[R] = ar::fused_ctas_per_sm(R, kNoAllocThreads);
+  *out = d;
+  return AR_OK;
+}
+
+}  // namespace
+
+extern "C" ar_status_t ar_allreduce_fused_noalloc(int R, const void* const* d_in_tbl,
+                                                  void* const* d_out_tbl, size_t count,
+                                                  void* stream) {
+  if (R < 1 || R > AR_MAX_RANKS || !d_in_tbl || !d_out_tbl) return AR_ERR_INVALID_ARG;
+  if (count == 0) return AR_OK;
+  if (count > AR_NOALLOC_MAX_COUNT(R)) return AR_ERR_INVALID_ARG;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return AR_ERR_CUDA;
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return AR_ERR_UNSUPPORTED;
+  NoAllocDevice d;
+  ar_status_t st = noalloc_setup(dev, R, &d);
+  if (st != AR_OK) return st;
+  if (d.ctas_per_sm[R] <= 0) return AR_ERR_CUDA;
+
+  ar::CallArgs a;
+  a.in_tbl = reinterpret_cast<const uint16_t* const*>(d_in_tbl);
+  a.out_tbl = reinterpret_cast<uint16_t* const*>(d_out_tbl);
+  a.count = count;
+  a.groups = (count + ar::kVecElems - 1) / ar::kVecElems;
+  a.shard_groups = (a.groups + (size_t)R - 1) / (size_t)R;
+  ar::FusedArgs f;
+  f.scratch = d.scratch;
+  f.slot_groups = a.shard_groups;  // R*(R-1)*slot_groups*32 <= scratch bytes by the check above
+  f.state = d.state;
+  f.spin_limit_ns = 100ull * 1000ull * 1000ull;
+  f.skip_producer = -1;
+  const size_t limit = (size_t)d.ctas_per_sm[R] * (size_t)d.sms / (size_t)R;
+  size_t per_rank = (a.shard_groups + kNoAllocThreads - 1) / kNoAllocThreads;
+  per_rank = std::max<size_t>(1, std::min(per_rank, limit));
+  ar::LaunchCfg cfg = {(int)(per_rank * (size_t)R), kNoAllocThreads};
+  return ar::launch_fused_ll8(R, a, f, cfg, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? AR_OK
+             : AR_ERR_CUDA;
+}
