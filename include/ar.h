@@ -158,7 +158,8 @@ ar_status_t ar_select(ar_handle_t h, size_t count, int* variant);
  * (0 = automatic).  ctas is the total grid for AR_FUSED_LL8 (rounded down to
  * a multiple of R, clamped to the co-resident limit and raised to at least
  * R), and the grid-stride CTA count for the others.  threads must be a
- * multiple of 32 in [64, 1024] (the fused kernel accepts 128..512). */
+ * multiple of 32 in [64, 1024] (the fused and fan-out kernels accept
+ * 128..512). */
 ar_status_t ar_set_launch(ar_handle_t h, int variant, int ctas, int threads);
 
 /* ar_set_spin_limit_ns -- the longest a fused-kernel packet wait may spin

@@ -59,8 +59,9 @@ struct ar_ctx {
   int skip_producer = -1;
   int fused_threads = 256;
   int fused_ctas_per_sm = 0;   // occupancy at fused_threads
-  int occ_threads = 0;         // cache of the last occupancy query
-  int occ_value = 0;
+  // Occupancy cache (CTAs per SM) indexed by threads / 32; 0 = not queried.
+  int occ_fused[33] = {};
+  int occ_fanout[33] = {};
 
   // host-buffer path
   uint16_t* staging = nullptr;        // 2 * R * max_count elements
@@ -128,11 +129,23 @@ int choose(const ar_ctx* h, size_t count, const TuneRow** row) {
   return t ? t->variant : AR_ONESHOT_FANOUT;
 }
 
-// Launch shape of one call.  Threads default to 256; the grid covers the
-// groups with one group per thread, capped at 16 CTAs per SM for the
-// grid-stride variants (a multiple of R for the rank-major ones).
-LaunchCfg shape(const ar_ctx* h, int variant, const TuneRow* row, size_t groups,
-                size_t shard_groups) {
+int occupancy(ar_ctx* h, int variant, int threads) {
+  int* cache = variant == AR_FUSED_LL8 ? h->occ_fused : h->occ_fanout;
+  const int k = threads / 32;
+  if (k < 0 || k > 32) return 0;
+  if (cache[k] == 0) {
+    const int n = variant == AR_FUSED_LL8 ? ar::fused_ctas_per_sm(h->R, threads)
+                                          : ar::fanout_ctas_per_sm(h->R, threads);
+    cache[k] = n > 0 ? n : -1;
+  }
+  return cache[k] > 0 ? cache[k] : 0;
+}
+
+// Launch shape of one call.  Threads default to 256.  Fan-out: a persistent
+// grid of co-resident CTAs (two groups per thread per iteration); pull and
+// two-phase: one group per thread, capped at 16 CTAs per SM, a multiple of
+// R; fused: R x min(groups per shard / threads, co-resident CTAs / R).
+LaunchCfg shape(ar_ctx* h, int variant, const TuneRow* row, size_t groups, size_t shard_groups) {
   LaunchCfg c = {0, 0};
   if (row && row->variant == variant) c = {row->ctas, row->threads};
   const LaunchCfg& o = h->override_cfg[variant];
@@ -143,7 +156,11 @@ LaunchCfg shape(const ar_ctx* h, int variant, const TuneRow* row, size_t groups,
   switch (variant) {
     case AR_ONESHOT_FANOUT: {
       if (c.threads <= 0) c.threads = 256;
-      if (c.ctas <= 0) c.ctas = (int)std::min(ceil_div(groups, (size_t)c.threads), cap);
+      if (c.ctas <= 0) {
+        const size_t resident = (size_t)occupancy(h, variant, c.threads) * (size_t)h->num_sms;
+        c.ctas = (int)std::max<size_t>(
+            1, std::min(ceil_div(groups, 2 * (size_t)c.threads), std::max<size_t>(resident, 1)));
+      }
       break;
     }
     case AR_ONESHOT_PULL:
@@ -160,17 +177,8 @@ LaunchCfg shape(const ar_ctx* h, int variant, const TuneRow* row, size_t groups,
       break;
     }
     case AR_FUSED_LL8: {
-      c.threads = h->fused_threads;
-      if (o.threads > 0) c.threads = o.threads;
-      int per_sm = h->fused_ctas_per_sm;
-      if (c.threads != h->fused_threads) {
-        ar_ctx* mh = const_cast<ar_ctx*>(h);
-        if (mh->occ_threads != c.threads) {
-          mh->occ_value = ar::fused_ctas_per_sm(R, c.threads);
-          mh->occ_threads = c.threads;
-        }
-        per_sm = mh->occ_value;
-      }
+      if (c.threads <= 0) c.threads = h->fused_threads;
+      const int per_sm = occupancy(h, variant, c.threads);
       const size_t limit = (size_t)per_sm * (size_t)h->num_sms / (size_t)R;  // CTAs per rank
       size_t per_rank = std::max<size_t>(1, ceil_div(shard_groups, (size_t)c.threads));
       if (c.ctas > 0) per_rank = std::max<size_t>(1, (size_t)c.ctas / (size_t)R);
@@ -299,7 +307,7 @@ ar_status_t ar_create(int R, size_t max_count, int dtype, ar_handle_t* out) {
   const size_t groups = ceil_div(max_count, (size_t)ar::kVecElems);
   h->slot_groups = ceil_div(groups, (size_t)R);
   h->scratch_bytes = (size_t)R * (size_t)(R - 1) * h->slot_groups * 4 * sizeof(uint64_t);
-  h->fused_ctas_per_sm = ar::fused_ctas_per_sm(R, h->fused_threads);
+  h->fused_ctas_per_sm = occupancy(h, AR_FUSED_LL8, h->fused_threads);
 
   ar_status_t st = AR_OK;
   if (cudaMalloc(&h->state, sizeof(DevState)) != cudaSuccess) st = AR_ERR_OOM;
@@ -358,7 +366,8 @@ ar_status_t ar_set_launch(ar_handle_t h, int variant, int ctas, int threads) {
   if (!h || variant <= AR_AUTO || variant >= AR_NUM_VARIANTS) return AR_ERR_INVALID_ARG;
   if (ctas < 0 || threads < 0) return AR_ERR_INVALID_ARG;
   if (threads && (threads % 32 || threads < 64 || threads > 1024)) return AR_ERR_INVALID_ARG;
-  if (variant == AR_FUSED_LL8 && threads && (threads < 128 || threads > 512))
+  if ((variant == AR_FUSED_LL8 || variant == AR_ONESHOT_FANOUT) && threads &&
+      (threads < 128 || threads > 512))
     return AR_ERR_INVALID_ARG;
   h->override_cfg[variant] = {ctas, threads};
   return AR_OK;

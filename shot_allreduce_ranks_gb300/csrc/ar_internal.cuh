@@ -48,18 +48,42 @@ struct FusedArgs {
 // ---------------------------------------------------------------------------
 // Small device helpers.
 
-__device__ __forceinline__ uint4 ld_v4_stream(const uint16_t* p) {
+// 16-byte global accesses that bypass L1 allocation.  With kHint the access
+// carries an L2 cache policy (createpolicy) chosen by the caller.
+template <bool kHint = false>
+__device__ __forceinline__ uint4 ld_v4_stream(const uint16_t* p, uint64_t pol = 0) {
   uint4 v;
-  asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
+  if (kHint) {
+    asm volatile("ld.global.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(pol));
+  } else {
+    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+  }
   return v;
 }
 
-__device__ __forceinline__ void st_v4_stream(uint16_t* p, uint4 v) {
-  asm volatile("st.global.L1::no_allocate.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x),
-               "r"(v.y), "r"(v.z), "r"(v.w)
-               : "memory");
+template <bool kHint = false>
+__device__ __forceinline__ void st_v4_stream(uint16_t* p, uint4 v, uint64_t pol = 0) {
+  if (kHint) {
+    asm volatile("st.global.L1::no_allocate.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;" ::"l"(p),
+                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol)
+                 : "memory");
+  } else {
+    asm volatile("st.global.L1::no_allocate.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x),
+                 "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+  }
+}
+
+// L2 policy under which a line is among the first to be evicted (data that
+// streams through once).
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
 }
 
 __device__ __forceinline__ uint16_t ld_u16(const uint16_t* p) {
@@ -75,22 +99,40 @@ __device__ __forceinline__ void st_u16(uint16_t* p, uint16_t v) {
 // Load group g (8 elements) of a buffer.  `valid` < 8 only for the last,
 // partial group; `vec` is false when some pointer of the call is not
 // 16-byte aligned.  Missing elements read as +0 (never stored back).
-__device__ __forceinline__ uint4 load_group(const uint16_t* base, size_t g, int valid, bool vec) {
+template <bool kHint = false>
+__device__ __forceinline__ uint4 load_group(const uint16_t* base, size_t g, int valid, bool vec,
+                                            uint64_t pol = 0) {
   const uint16_t* p = base + g * kVecElems;
-  if (vec && valid == kVecElems) return ld_v4_stream(p);
-  uint32_t w[4] = {0u, 0u, 0u, 0u};
-  for (int e = 0; e < valid; ++e) w[e >> 1] |= (uint32_t)ld_u16(p + e) << (16 * (e & 1));
-  return make_uint4(w[0], w[1], w[2], w[3]);
+  if (vec && valid == kVecElems) return ld_v4_stream<kHint>(p, pol);
+  uint32_t w0 = 0u, w1 = 0u, w2 = 0u, w3 = 0u;
+#pragma unroll
+  for (int e = 0; e < kVecElems; ++e) {
+    if (e < valid) {
+      const uint32_t h = (uint32_t)ld_u16(p + e) << (16 * (e & 1));
+      if (e < 2) w0 |= h;
+      else if (e < 4) w1 |= h;
+      else if (e < 6) w2 |= h;
+      else w3 |= h;
+    }
+  }
+  return make_uint4(w0, w1, w2, w3);
 }
 
-__device__ __forceinline__ void store_group(uint16_t* base, size_t g, uint4 v, int valid, bool vec) {
+template <bool kHint = false>
+__device__ __forceinline__ void store_group(uint16_t* base, size_t g, uint4 v, int valid, bool vec,
+                                            uint64_t pol = 0) {
   uint16_t* p = base + g * kVecElems;
   if (vec && valid == kVecElems) {
-    st_v4_stream(p, v);
+    st_v4_stream<kHint>(p, v, pol);
     return;
   }
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  for (int e = 0; e < valid; ++e) st_u16(p + e, (uint16_t)(w[e >> 1] >> (16 * (e & 1))));
+#pragma unroll
+  for (int e = 0; e < kVecElems; ++e) {
+    if (e < valid) {
+      const uint32_t w = e < 2 ? v.x : e < 4 ? v.y : e < 6 ? v.z : v.w;
+      st_u16(p + e, (uint16_t)(w >> (16 * (e & 1))));
+    }
+  }
 }
 
 // bf16 -> fp32 is exact: the bf16 bits are the upper half of the fp32 word.
@@ -180,8 +222,10 @@ cudaError_t launch_twophase(int R, const CallArgs& a, LaunchCfg cfg, cudaStream_
 cudaError_t launch_fused_ll8(int R, const CallArgs& a, const FusedArgs& f, LaunchCfg cfg,
                              cudaStream_t s);
 
-// Occupancy of the fused kernel (CTAs per SM) for R ranks and `threads`.
+// Occupancy (CTAs per SM) of the fused and fan-out kernels for R ranks and
+// `threads` threads per CTA.
 int fused_ctas_per_sm(int R, int threads);
+int fanout_ctas_per_sm(int R, int threads);
 
 }  // namespace ar
 

@@ -74,24 +74,23 @@ __device__ __forceinline__ void st_relaxed_u32(uint32_t* p, uint32_t v) {
   asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-// Four packets of one group: flag in the high half of every 64-bit word.
+// Four packets of one group in one 32-byte access, flag in the high half of
+// every 64-bit word.  Stores ask L2 to keep the line (it is read back soon by
+// the owner); loads mark it evict-first once read.  As a vector access, the
+// memory model treats it as four 64-bit accesses, each single-copy atomic.
 __device__ __forceinline__ void st_packets(uint64_t* p, uint4 x, uint32_t epoch) {
   const uint64_t hi = (uint64_t)epoch << 32;
-  asm volatile("st.relaxed.gpu.global.v2.b64 [%0], {%1,%2};" ::"l"(p), "l"(hi | x.x),
-               "l"(hi | x.y)
-               : "memory");
-  asm volatile("st.relaxed.gpu.global.v2.b64 [%0], {%1,%2};" ::"l"(p + 2), "l"(hi | x.z),
-               "l"(hi | x.w)
+  asm volatile("st.relaxed.gpu.global.L2::evict_last.v4.b64 [%0], {%1,%2,%3,%4};" ::"l"(p),
+               "l"(hi | x.x), "l"(hi | x.y), "l"(hi | x.z), "l"(hi | x.w)
                : "memory");
 }
 
 struct Packets4 {
   uint64_t w[4];
   __device__ __forceinline__ void load(const uint64_t* p) {
-    asm volatile("ld.relaxed.gpu.global.v2.b64 {%0,%1}, [%2];" : "=l"(w[0]), "=l"(w[1]) : "l"(p));
-    asm volatile("ld.relaxed.gpu.global.v2.b64 {%0,%1}, [%2];"
-                 : "=l"(w[2]), "=l"(w[3])
-                 : "l"(p + 2));
+    asm volatile("ld.relaxed.gpu.global.L2::evict_first.v4.b64 {%0,%1,%2,%3}, [%4];"
+                 : "=l"(w[0]), "=l"(w[1]), "=l"(w[2]), "=l"(w[3])
+                 : "l"(p));
   }
   __device__ __forceinline__ bool arrived(uint32_t epoch) const {
     return (uint32_t)(w[0] >> 32) == epoch && (uint32_t)(w[1] >> 32) == epoch &&
@@ -138,21 +137,34 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, Fuse
   const size_t Vs = a.shard_groups;
   const uint16_t* my_in = s_in[r];
 
+  // Inputs stream through once: evict-first, so they do not push packets
+  // out of L2 before their owners read them.
+  const uint64_t pol_in = l2_policy_evict_first();
+
   // ---- scatter: packets of rank r for every other owner -------------------
+  // Two groups (j, j + tstride) per iteration: all 2(R-1) loads are issued
+  // before the first packet store.
   if (R > 1 && r != f.skip_producer) {
-    for (size_t j = t0; j < Vs; j += tstride) {
-      uint4 x[R > 1 ? R - 1 : 1];
+    for (size_t j = t0; j < Vs; j += 2 * tstride) {
+      const size_t j2 = j + tstride;
+      uint4 x[R > 1 ? R - 1 : 1], y[R > 1 ? R - 1 : 1];
 #pragma unroll
       for (int k = 1; k < R; ++k) {
         const int o = (r + k) % R;
         const size_t g = (size_t)o * Vs + j;
-        if (g < a.groups) x[k - 1] = load_group(my_in, g, group_valid(g, a.count), vec);
+        if (g < a.groups) x[k - 1] = load_group<true>(my_in, g, group_valid(g, a.count), vec, pol_in);
+        const size_t g2 = (size_t)o * Vs + j2;
+        if (j2 < Vs && g2 < a.groups)
+          y[k - 1] = load_group<true>(my_in, g2, group_valid(g2, a.count), vec, pol_in);
       }
 #pragma unroll
       for (int k = 1; k < R; ++k) {
         const int o = (r + k) % R;
         const size_t g = (size_t)o * Vs + j;
-        if (g < a.groups) st_packets(slot_base<R>(f, o, r) + j * 4, x[k - 1], epoch);
+        uint64_t* slot = slot_base<R>(f, o, r);
+        if (g < a.groups) st_packets(slot + j * 4, x[k - 1], epoch);
+        const size_t g2 = (size_t)o * Vs + j2;
+        if (j2 < Vs && g2 < a.groups) st_packets(slot + j2 * 4, y[k - 1], epoch);
       }
     }
   }
@@ -164,7 +176,7 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, Fuse
   for (size_t j = t0; j < n && !aborted; j += tstride) {
     const size_t g = g0 + j;
     const int valid = group_valid(g, a.count);
-    const uint4 own = load_group(my_in, g, valid, vec);
+    const uint4 own = load_group<true>(my_in, g, valid, vec, pol_in);
     Packets4 pk[R];
     uint32_t pending = 0;
 #pragma unroll

@@ -33,13 +33,40 @@ __device__ __forceinline__ uint4 reduce_group(const uint16_t* const* s_in, size_
   return acc.round_bf16();
 }
 
+// Grid-stride over groups, two groups (g, g + stride) per iteration so that
+// 2R independent 16-byte loads are in flight per thread before any store.
 template <int R>
-__global__ void __launch_bounds__(1024) k_oneshot_fanout(CallArgs a) {
+__global__ void __launch_bounds__(512) k_oneshot_fanout(CallArgs a) {
   __shared__ const uint16_t* s_in[R];
   __shared__ uint16_t* s_out[R];
   const bool vec = load_tables<R>(a, s_in, s_out);
   const size_t stride = (size_t)gridDim.x * blockDim.x;
-  for (size_t g = (size_t)blockIdx.x * blockDim.x + threadIdx.x; g < a.groups; g += stride) {
+  size_t g = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  for (; g + stride < a.groups; g += 2 * stride) {
+    const size_t g2 = g + stride;
+    const int valid2 = group_valid(g2, a.count);
+    uint4 x[R], y[R];
+#pragma unroll
+    for (int s = 0; s < R; ++s) {
+      x[s] = load_group(s_in[s], g, kVecElems, vec);
+      y[s] = load_group(s_in[s], g2, valid2, vec);
+    }
+    Acc8 ax, ay;
+    ax.set(x[0]);
+    ay.set(y[0]);
+#pragma unroll
+    for (int s = 1; s < R; ++s) {
+      ax.add(x[s]);
+      ay.add(y[s]);
+    }
+    const uint4 rx = ax.round_bf16(), ry = ay.round_bf16();
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      store_group(s_out[r], g, rx, kVecElems, vec);
+      store_group(s_out[r], g2, ry, valid2, vec);
+    }
+  }
+  if (g < a.groups) {
     const int valid = group_valid(g, a.count);
     const uint4 y = reduce_group<R>(s_in, g, valid, vec);
 #pragma unroll
@@ -89,6 +116,25 @@ cudaError_t launch_oneshot_fanout(int R, const CallArgs& a, LaunchCfg cfg, cudaS
   AR_RANK_SWITCH(R, L)
 #undef L
   return cudaGetLastError();
+}
+
+int fanout_ctas_per_sm(int R, int threads) {
+  int n = 0;
+  cudaError_t e = cudaErrorInvalidValue;
+#define Q(RR) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_oneshot_fanout<RR>, threads, 0)
+  switch (R) {
+    case 1: Q(1); break;
+    case 2: Q(2); break;
+    case 3: Q(3); break;
+    case 4: Q(4); break;
+    case 5: Q(5); break;
+    case 6: Q(6); break;
+    case 7: Q(7); break;
+    case 8: Q(8); break;
+    default: return 0;
+  }
+#undef Q
+  return e == cudaSuccess ? n : 0;
 }
 
 cudaError_t launch_oneshot_pull(int R, const CallArgs& a, LaunchCfg cfg, cudaStream_t s) {
