@@ -56,7 +56,7 @@ def alg_bytes(variant: str, R: int, N: int) -> int:
     stage-1 stores are already outputs).  fused LL8: 4RN plus each of the
     R-1 foreign shards per rank as 4-byte-per-element packets, written once
     and read once (8(R-1)N)."""
-    if variant == "oneshot_fanout":
+    if variant in ("oneshot_fanout", "oneshot_fanout_bulk"):
         return 4 * R * N
     if variant == "oneshot_pull":
         return 2 * R * R * N + 2 * R * N
@@ -64,10 +64,15 @@ def alg_bytes(variant: str, R: int, N: int) -> int:
         return 4 * R * N + (2 * N if R > 1 else 0)
     if variant == "fused_ll8":
         return 4 * R * N + 8 * (R - 1) * N
+    if variant in ("fused_ll8_staged", "packet_3op"):
+        # plus the reduced shards sent back as packets and read by every rank
+        return 4 * R * N + 16 * (R - 1) * N
     raise ValueError(variant)
 
 
 def launches_per_call(variant: str, R: int) -> int:
+    if variant == "packet_3op":
+        return 3
     return 2 if (variant == "twophase" and R > 1) else 1
 
 
@@ -255,18 +260,58 @@ def make_sets(R, N, fill, nsets, device, seed0=0):
     return sets
 
 
-def time_variant(ar, sets, N, variant, steps, warmup, stream, sampler=None):
-    """Per-step CUDA events over exactly `steps` calls; returns (total_s,
-    per-step durations in s, wall t0, wall t1)."""
+def time_variant(ar, sets, N, variant, steps, warmup, stream, mode="graph", per_graph=50):
+    """Time exactly `steps` calls with CUDA events on `stream`.
+
+    mode "graph": the calls are captured into CUDA graphs of `per_graph`
+    calls (plus one graph for the remainder) and replayed, the regime of the
+    aiter write-mode tables ("CudaGraph: on"); per-call time = region / steps.
+    mode "stream": plain back-to-back launches with an event between calls.
+    Returns (total_s, per-call durations in s, wall t0, wall t1)."""
     import torch
     ar.set_variant(variant)
     tables = [ar.tables(xin, xout) for _, xin, xout in sets]
-    with torch.cuda.stream(stream):
-        for i in range(warmup):
+
+    def issue(n, first=0):
+        for i in range(first, first + n):
             it, ot = tables[i % len(tables)]
             ar.allreduce_tables(it, ot, N, stream)
-    events = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+
+    with torch.cuda.stream(stream):
+        issue(warmup)
     torch.cuda.synchronize()
+    if mode == "graph":
+        g_n = max(1, min(per_graph, steps))
+        graphs = []
+        for n in ([g_n] if steps >= g_n else []) + ([steps % g_n] if steps % g_n else []):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                issue(n)
+            graphs.append((g, n))
+        full, rest = steps // g_n, steps % g_n
+        with torch.cuda.stream(stream):
+            for g, _ in graphs:
+                g.replay()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        w0 = time.time()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(full):
+                graphs[0][0].replay()
+            if rest:
+                graphs[-1][0].replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        w1 = time.time()
+        barrier()
+        total = e0.elapsed_time(e1) * 1e-3
+        del graphs
+        return total, [total / steps] * steps, w0, w1
+    events = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
     barrier()
     torch.cuda.synchronize()
     w0 = time.time()
@@ -345,7 +390,8 @@ def run_ours(args):
     sampler = ClockSampler(gpu_id_for(local)) if not args.no_clocks else None
     if sampler:
         sampler.wait_ready()
-    total, per, w0, w1 = time_variant(ar, sets, N, args.variant, args.steps, args.warmup, stream)
+    total, per, w0, w1 = time_variant(ar, sets, N, args.variant, args.steps, args.warmup, stream,
+                                      args.timing)
     clocks = sampler.summary(w0, w1) if sampler else None
     if sampler:
         sampler.stop()
@@ -357,8 +403,7 @@ def run_ours(args):
     peak, peak_kind = measured_peaks()
     ab = alg_bytes(args.variant, R, N)
     achieved = ab / launch_avg_s / 1e9 if launch_avg_s > 0 else None
-    kernel = {"fused_ll8": "fused_ll8", "oneshot_fanout": "oneshot_fanout",
-              "oneshot_pull": "oneshot_pull", "twophase": "twophase"}[args.variant]
+    kernel = args.variant
     traffic = profiled_traffic(kernel, args.workload)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,
@@ -368,14 +413,21 @@ def run_ours(args):
 
     extra = {}
     if not args.no_extra:
-        for v in ("oneshot_fanout", "oneshot_pull", "twophase", "fused_ll8"):
+        for v in ("oneshot_fanout", "oneshot_fanout_bulk", "oneshot_pull", "twophase",
+                  "fused_ll8", "fused_ll8_staged", "packet_3op"):
             if v == args.variant:
                 continue
-            t, pv, _, _ = time_variant(ar, sets, N, v, min(args.steps, 2000), 20, stream)
+            t, pv, _, _ = time_variant(ar, sets, N, v, min(args.steps, 2000), 20, stream,
+                                       args.timing)
             us = t * 1e6 / min(args.steps, 2000)
             extra[v] = {"us_per_call": round(us, 3),
                         "alg_GBps": round(alg_bytes(v, R, N) / statistics.fmean(pv) / 1e9, 1)}
         extra[args.variant] = {"us_per_call": round(local_us, 3), "alg_GBps": round(achieved, 1)}
+        other = "stream" if args.timing == "graph" else "graph"
+        t, pv, _, _ = time_variant(ar, sets, N, args.variant, min(args.steps, 2000), 20, stream,
+                                   other)
+        extra["%s_%s_timing" % (args.variant, other)] = {
+            "us_per_call": round(t * 1e6 / min(args.steps, 2000), 3)}
         ar.set_variant("auto")
         extra["auto_selects"] = ar.select(N)
 
@@ -409,7 +461,8 @@ def run_ours(args):
         tsets = make_sets(wt.R, wt.count, wt.fill, 2, dev)
         art = AllReduce(wt.R, wt.count, device=dev)
         for v in ("fused_ll8", "oneshot_fanout"):
-            t, pv, _, _ = time_variant(art, tsets, wt.count, v, min(args.steps, 2000), 20, stream)
+            t, pv, _, _ = time_variant(art, tsets, wt.count, v, min(args.steps, 2000), 20, stream,
+                                       args.timing)
             ab_t = alg_bytes(v, wt.R, wt.count)
             g = ab_t / statistics.fmean(pv) / 1e9
             extra["r8_512x8192_" + v] = {
@@ -426,6 +479,7 @@ def run_ours(args):
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": args.workload, "R": R, "count": N,
                    "shape": list(w.shape), "fill": w.fill, "variant": args.variant,
+                   "timing": args.timing,
                    "parallelism": "replicas" if world > 1 else "single",
                    "l2": "inputs rotate over %d buffer sets (%.0f MB touched between reuses)"
                          % (nsets, (nsets - 1) * per_set / 1e6)},
@@ -500,7 +554,10 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="r8_440x5120")
     p.add_argument("--variant", default="fused_ll8",
-                   choices=["oneshot_pull", "oneshot_fanout", "twophase", "fused_ll8"])
+                   choices=["oneshot_pull", "oneshot_fanout", "twophase", "fused_ll8",
+                            "oneshot_fanout_bulk", "fused_ll8_staged", "packet_3op"])
+    p.add_argument("--timing", choices=["graph", "stream"], default="graph",
+                   help="graph: calls replayed from CUDA graphs; stream: plain launches")
     p.add_argument("--e2e-steps", type=int, default=200)
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-extra", action="store_true")

@@ -27,6 +27,16 @@
  *   - AR_TWOPHASE is the two-stage allreduce of the aiter page without write
  *     mode (stage 1 reduces a shard into its owner's output, stage 2 copies
  *     it into the other ranks' outputs);
+ *   - AR_ONESHOT_FANOUT_BULK is the same fan-out with every input tile
+ *     brought into shared memory, and every result tile sent to the R
+ *     outputs, by the bulk-copy (TMA) engine;
+ *   - AR_FUSED_LL8_STAGED is that fused kernel without write mode: each
+ *     owner sends its reduced shard back as LL8 packets to every rank's
+ *     result slot and every rank copies them into its output (the packet
+ *     broadcast of the ARK page); AR_PACKET_3OP runs the same three phases
+ *     as three launches (that page's send_packet -> recv_reduce_send_packet
+ *     -> recv_packet decomposition).  Both exist to measure what write mode
+ *     and fusion save;
  *   - AR_FUSED_LL8 is the single fused scatter -> reduce -> broadcast kernel
  *     synchronised by LL packet flags of "Add monolithic fused packet
  *     allreduce kernel and Model::all_reduce_packet API" (microsoft/ark #254,
@@ -77,17 +87,20 @@ typedef enum {
   AR_ONESHOT_PULL = 1,   /* CTA (chunk, r) reads all R inputs, writes out_r only */
   AR_ONESHOT_FANOUT = 2, /* CTA reads all R inputs once, writes all R outputs */
   AR_TWOPHASE = 3,       /* launch 1: owner shards reduced; launch 2: shards copied out */
-  AR_FUSED_LL8 = 4       /* one persistent kernel: LL8 packet scatter, poll+reduce, write mode */
+  AR_FUSED_LL8 = 4,      /* one persistent kernel: LL8 packet scatter, poll+reduce, write mode */
+  AR_ONESHOT_FANOUT_BULK = 5, /* fan-out with tiles moved by bulk (TMA) copies through shared memory */
+  AR_FUSED_LL8_STAGED = 6,    /* fused LL8 without write mode: result packets back to every rank */
+  AR_PACKET_3OP = 7           /* the same three packet phases as three separate launches */
 } ar_variant_t;
 
-#define AR_NUM_VARIANTS 5
+#define AR_NUM_VARIANTS 8
 
 /* Static description of a handle (filled by ar_query). */
 typedef struct {
   int R;                    /* virtual ranks */
   int dtype;                /* ar_dtype_t */
   size_t max_count;         /* largest count accepted by ar_allreduce */
-  size_t scratch_bytes;     /* LL8 packet scratch owned by the handle */
+  size_t scratch_bytes;     /* LL8 packet scratch owned by the handle (both regions) */
   int num_sms;              /* SMs of the device the handle lives on */
   int fused_max_ctas;       /* co-resident CTA limit used to size the fused grid */
   int fused_threads;        /* threads per CTA of the fused kernel */
@@ -101,10 +114,12 @@ typedef struct {
  *   max_count  >= 1; bounds `count` of later calls and sizes the scratch.
  *   dtype      must be AR_BF16.
  *   out        receives the handle (set to NULL on failure).
- * Allocates, on the current device, the packet scratch
- * (32 * R * (R-1) * ceil(ceil(max_count/8)/R) bytes, about 4*(R-1)*max_count,
- * zeroed here so that no flag matches a live epoch) and a small state block
- * (epoch, done counter, error word).  Synchronous; not for stream capture.
+ * Allocates, on the current device, two packet scratch regions (scatter
+ * packets and the staged variants' result packets), each
+ * 32 * R * (R-1) * ceil(ceil(max_count/8)/R) bytes (about
+ * 4*(R-1)*max_count), zeroed here so that no flag matches a live epoch, and
+ * a small state block (epoch, done counter, error word).  Synchronous; not
+ * for stream capture.
  * Errors: AR_ERR_INVALID_ARG (R, max_count, out), AR_ERR_UNSUPPORTED (dtype,
  * or the current device is not compute capability 10.3), AR_ERR_OOM, AR_ERR_CUDA.
  */
@@ -141,6 +156,30 @@ ar_status_t ar_create(int R, size_t max_count, int dtype, ar_handle_t* out);
  */
 ar_status_t ar_allreduce(ar_handle_t h, const void* const* d_in_tbl,
                          void* const* d_out_tbl, size_t count, void* stream);
+
+/*
+ * ar_reduce_scatter -- rank r keeps block r of the sum:
+ *   out_r[j] = bf16_rne(sum over s in rank order of in_s[r*recvcount + j]),
+ * j < recvcount.  Same numerics as ar_allreduce.  Each input holds
+ * R*recvcount elements, each output recvcount elements; R*recvcount <=
+ * max_count.  It is the "srcStride = recvCount, ownOffset = slot *
+ * recvCount" case of the one-shot push-reduce kernel of "Add HIP-graph
+ * capture coverage for the sharded-relay collectives" (meta-pytorch/
+ * torchcomms #3850), whose allreduce case is the stride-0 one.
+ * ar_all_gather -- every output is the concatenation of all inputs in rank
+ * order: out_r[s*sendcount + j] = in_s[j]; inputs hold sendcount elements,
+ * outputs R*sendcount; R*sendcount <= max_count.
+ * Both: device pointer tables as in ar_allreduce; outputs must not overlap
+ * inputs; 16-byte vectors when every pointer is 16-byte aligned and the
+ * block length is a multiple of 8, else 2-byte accesses; one launch, no
+ * allocation, no synchronisation.  Errors: AR_ERR_INVALID_ARG (NULL handle
+ * or table, block too large), AR_ERR_CUDA (launch).  A block of 0 returns
+ * AR_OK without a launch.
+ */
+ar_status_t ar_reduce_scatter(ar_handle_t h, const void* const* d_in_tbl,
+                              void* const* d_out_tbl, size_t recvcount, void* stream);
+ar_status_t ar_all_gather(ar_handle_t h, const void* const* d_in_tbl,
+                          void* const* d_out_tbl, size_t sendcount, void* stream);
 
 /* ar_destroy -- synchronise the device and free everything the handle owns.
  * NULL is accepted.  Returns AR_ERR_CUDA if a free failed. */

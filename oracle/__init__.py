@@ -64,6 +64,10 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_allreduce_bf16.argtypes = [
         ctypes.c_int, ctypes.c_size_t, ctypes.POINTER(u16p), ctypes.POINTER(u16p)]
     lib.oracle_allreduce_bf16.restype = ctypes.c_int
+    for name in ("oracle_reduce_scatter_bf16", "oracle_all_gather_bf16"):
+        fn = getattr(lib, name)
+        fn.argtypes = [ctypes.c_int, ctypes.c_size_t, ctypes.POINTER(u16p), ctypes.POINTER(u16p)]
+        fn.restype = ctypes.c_int
     return lib
 
 
@@ -106,5 +110,41 @@ def allreduce_bf16(inputs, lib: ctypes.CDLL | None = None, outputs=None):
     out_tbl = (u16p * R)(*[o.ctypes.data_as(u16p) for o in outs])
     rc = lib.oracle_allreduce_bf16(R, count, in_tbl, out_tbl)
     if rc != 0:
+        raise ValueError("oracle rejected R=%d" % R)
+    return outs
+
+
+def _tables(bufs):
+    u16p = ctypes.POINTER(ctypes.c_uint16)
+    return (u16p * len(bufs))(*[b.ctypes.data_as(u16p) for b in bufs])
+
+
+def reduce_scatter_bf16(inputs, lib: ctypes.CDLL | None = None):
+    """Reduce-scatter of R inputs of R*recvcount elements; returns R outputs
+    of recvcount elements (output r = rank-order sum of block r)."""
+    lib = lib or load()
+    ins = [_u16(a) for a in inputs]
+    R = len(ins)
+    total = ins[0].size
+    if total % R or any(a.size != total for a in ins):
+        raise ValueError("inputs must all hold R * recvcount elements")
+    rc = total // R
+    outs = [np.empty(rc, np.uint16) for _ in range(R)]
+    if lib.oracle_reduce_scatter_bf16(R, rc, _tables(ins), _tables(outs)) != 0:
+        raise ValueError("oracle rejected R=%d" % R)
+    return outs
+
+
+def all_gather_bf16(inputs, lib: ctypes.CDLL | None = None):
+    """All-gather of R inputs of sendcount elements; returns R outputs of
+    R*sendcount elements (the inputs concatenated in rank order)."""
+    lib = lib or load()
+    ins = [_u16(a) for a in inputs]
+    R = len(ins)
+    sc = ins[0].size
+    if any(a.size != sc for a in ins):
+        raise ValueError("inputs must hold the same element count")
+    outs = [np.empty(R * sc, np.uint16) for _ in range(R)]
+    if lib.oracle_all_gather_bf16(R, sc, _tables(ins), _tables(outs)) != 0:
         raise ValueError("oracle rejected R=%d" % R)
     return outs

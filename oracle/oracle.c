@@ -102,3 +102,41 @@ int oracle_allreduce_bf16(int R, size_t count, const uint16_t* const* in,
   }
   return 0;
 }
+
+/*
+ * Reduce-scatter: the same summation, but rank r keeps only block r.  Rank
+ * s's input holds R blocks of `recvcount` elements; rank r's output holds
+ *   out[r][j] = bf16_rne(sum over s in rank order of in[s][r*recvcount + j]).
+ * This is the "srcStride = recvCount, ownOffset = slot * recvCount" case of
+ * the one-shot push-reduce kernel in "Add HIP-graph capture coverage for the
+ * sharded-relay collectives" (meta-pytorch/torchcomms #3850, the commit that
+ * generalises the one-shot kernel to allreduce), whose allreduce case is the
+ * stride-0 one above.  Outputs must not overlap inputs.
+ */
+int oracle_reduce_scatter_bf16(int R, size_t recvcount, const uint16_t* const* in,
+                               uint16_t* const* out) {
+  if (R < 1 || R > 64) return -1;
+  for (int r = 0; r < R; ++r) {
+    const size_t base = (size_t)r * recvcount;
+    for (size_t j = 0; j < recvcount; ++j) {
+      float acc = bf16_to_f32(in[0][base + j]);
+      for (int s = 1; s < R; ++s) acc = acc + bf16_to_f32(in[s][base + j]);
+      out[r][j] = oracle_f32_to_bf16_rne(acc);
+    }
+  }
+  return 0;
+}
+
+/*
+ * All-gather: every rank's output is the concatenation, in rank order, of
+ * all ranks' inputs of `sendcount` elements: out[r][s*sendcount + j] =
+ * in[s][j].  No arithmetic.  Outputs must not overlap inputs.
+ */
+int oracle_all_gather_bf16(int R, size_t sendcount, const uint16_t* const* in,
+                           uint16_t* const* out) {
+  if (R < 1 || R > 64) return -1;
+  for (int r = 0; r < R; ++r)
+    for (int s = 0; s < R; ++s)
+      for (size_t j = 0; j < sendcount; ++j) out[r][(size_t)s * sendcount + j] = in[s][j];
+  return 0;
+}

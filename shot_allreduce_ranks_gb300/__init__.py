@@ -120,6 +120,37 @@ class AllReduce:
         self.allreduce_tables(in_tbl, out_tbl, count, stream)
         return outputs
 
+    def reduce_scatter(self, inputs, outputs=None, recvcount=None, stream=None):
+        """outputs[r] <- block r of the rank-order sum; inputs hold R*recvcount."""
+        import torch
+        if recvcount is None:
+            recvcount = inputs[0].numel() // self.R
+        if outputs is None:
+            outputs = [torch.empty(recvcount, dtype=torch.bfloat16, device=self.device)
+                       for _ in range(self.R)]
+        self._check_buffers(inputs, self.R * recvcount)
+        self._check_buffers(outputs, recvcount)
+        in_tbl, out_tbl = self.tables(inputs, outputs)
+        check(self._lib.ar_reduce_scatter(self._h, in_tbl.data_ptr(), out_tbl.data_ptr(),
+                                          int(recvcount), _stream_handle(stream)),
+              "ar_reduce_scatter")
+        return outputs
+
+    def all_gather(self, inputs, outputs=None, sendcount=None, stream=None):
+        """outputs[r] <- concatenation of all inputs in rank order."""
+        import torch
+        if sendcount is None:
+            sendcount = inputs[0].numel()
+        if outputs is None:
+            outputs = [torch.empty(self.R * sendcount, dtype=torch.bfloat16, device=self.device)
+                       for _ in range(self.R)]
+        self._check_buffers(inputs, sendcount)
+        self._check_buffers(outputs, self.R * sendcount)
+        in_tbl, out_tbl = self.tables(inputs, outputs)
+        check(self._lib.ar_all_gather(self._h, in_tbl.data_ptr(), out_tbl.data_ptr(),
+                                      int(sendcount), _stream_handle(stream)), "ar_all_gather")
+        return outputs
+
     def allreduce_host(self, host_inputs, host_outputs, count=None, stream=None) -> None:
         """End-to-end call on HOST tensors (pinned for asynchronous copies)."""
         if count is None:

@@ -17,12 +17,16 @@ HEADER = os.path.join(os.path.dirname(PKG), "include", "ar.h")
 AR_OK, AR_ERR_INVALID_ARG, AR_ERR_UNSUPPORTED, AR_ERR_OOM, AR_ERR_CUDA, AR_ERR_TIMEOUT = range(6)
 AR_BF16 = 0
 AR_AUTO, AR_ONESHOT_PULL, AR_ONESHOT_FANOUT, AR_TWOPHASE, AR_FUSED_LL8 = range(5)
+AR_ONESHOT_FANOUT_BULK, AR_FUSED_LL8_STAGED, AR_PACKET_3OP = 5, 6, 7
 VARIANTS = {
     "auto": AR_AUTO,
     "oneshot_pull": AR_ONESHOT_PULL,
     "oneshot_fanout": AR_ONESHOT_FANOUT,
     "twophase": AR_TWOPHASE,
     "fused_ll8": AR_FUSED_LL8,
+    "oneshot_fanout_bulk": AR_ONESHOT_FANOUT_BULK,
+    "fused_ll8_staged": AR_FUSED_LL8_STAGED,
+    "packet_3op": AR_PACKET_3OP,
 }
 AR_MAX_RANKS = 8
 
@@ -64,6 +68,8 @@ PROTOTYPES = {
     "ar_debug_set_epoch": (_ST, [_H, ctypes.c_uint32]),
     "ar_debug_get_epoch": (_ST, [_H, ctypes.POINTER(ctypes.c_uint32)]),
     "ar_allreduce_fused_noalloc": (_ST, [_I, _VP, _VP, _SZ, _VP]),
+    "ar_reduce_scatter": (_ST, [_H, _VP, _VP, _SZ, _VP]),
+    "ar_all_gather": (_ST, [_H, _VP, _VP, _SZ, _VP]),
 }
 
 AR_NOALLOC_SCRATCH_BYTES = 32 << 20

@@ -52,8 +52,9 @@ struct ar_ctx {
   bool log = false;
 
   DevState* state = nullptr;
-  uint64_t* scratch = nullptr;
-  size_t scratch_bytes = 0;
+  uint64_t* scratch = nullptr;   // scatter packets
+  uint64_t* rscratch = nullptr;  // result packets (staged variants)
+  size_t scratch_bytes = 0;      // bytes of each region
   size_t slot_groups = 0;
   uint64_t spin_limit_ns = 100ull * 1000ull * 1000ull;
   int skip_producer = -1;
@@ -61,7 +62,9 @@ struct ar_ctx {
   int fused_ctas_per_sm = 0;   // occupancy at fused_threads
   // Occupancy cache (CTAs per SM) indexed by threads / 32; 0 = not queried.
   int occ_fused[33] = {};
+  int occ_staged[33] = {};
   int occ_fanout[33] = {};
+  int bulk_ctas_per_sm = 0;    // bulk fan-out (fixed 256 threads)
 
   // host-buffer path
   uint16_t* staging = nullptr;        // 2 * R * max_count elements
@@ -130,12 +133,15 @@ int choose(const ar_ctx* h, size_t count, const TuneRow** row) {
 }
 
 int occupancy(ar_ctx* h, int variant, int threads) {
-  int* cache = variant == AR_FUSED_LL8 ? h->occ_fused : h->occ_fanout;
+  int* cache = variant == AR_FUSED_LL8          ? h->occ_fused
+               : variant == AR_FUSED_LL8_STAGED ? h->occ_staged
+                                                : h->occ_fanout;
   const int k = threads / 32;
   if (k < 0 || k > 32) return 0;
   if (cache[k] == 0) {
-    const int n = variant == AR_FUSED_LL8 ? ar::fused_ctas_per_sm(h->R, threads)
-                                          : ar::fanout_ctas_per_sm(h->R, threads);
+    const int n = variant == AR_FUSED_LL8          ? ar::fused_ctas_per_sm(h->R, threads)
+                  : variant == AR_FUSED_LL8_STAGED ? ar::fused_staged_ctas_per_sm(h->R, threads)
+                                                   : ar::fanout_ctas_per_sm(h->R, threads);
     cache[k] = n > 0 ? n : -1;
   }
   return cache[k] > 0 ? cache[k] : 0;
@@ -176,7 +182,24 @@ LaunchCfg shape(ar_ctx* h, int variant, const TuneRow* row, size_t groups, size_
       }
       break;
     }
-    case AR_FUSED_LL8: {
+    case AR_ONESHOT_FANOUT_BULK: {
+      c.threads = ar::kBulkThreads;
+      const size_t tiles = ceil_div(groups, (size_t)ar::kBulkThreads);
+      const size_t resident = (size_t)h->bulk_ctas_per_sm * (size_t)h->num_sms;
+      if (c.ctas <= 0) c.ctas = (int)std::max<size_t>(1, std::min(tiles, resident));
+      break;
+    }
+    case AR_PACKET_3OP: {
+      // Three ordinary launches: no co-residency needed, one group per thread.
+      if (c.threads <= 0) c.threads = h->fused_threads;
+      size_t per_rank = std::max<size_t>(1, ceil_div(shard_groups, (size_t)c.threads));
+      if (c.ctas > 0) per_rank = std::max<size_t>(1, (size_t)c.ctas / (size_t)R);
+      per_rank = std::min(per_rank, std::max<size_t>(1, cap / (size_t)R));
+      c.ctas = (int)(per_rank * (size_t)R);
+      break;
+    }
+    case AR_FUSED_LL8:
+    case AR_FUSED_LL8_STAGED: {
       if (c.threads <= 0) c.threads = h->fused_threads;
       const int per_sm = occupancy(h, variant, c.threads);
       const size_t limit = (size_t)per_sm * (size_t)h->num_sms / (size_t)R;  // CTAs per rank
@@ -206,6 +229,8 @@ ar_status_t launch(ar_ctx* h, int variant, const TuneRow* row, const void* const
   a.count = count;
   a.groups = ceil_div(count, (size_t)ar::kVecElems);
   a.shard_groups = ceil_div(a.groups, (size_t)h->R);
+  a.state = h->state;
+  a.spin_limit_ns = h->spin_limit_ns;
   LaunchCfg cfg = shape(h, variant, row, a.groups, a.shard_groups);
   if (h->log)
     fprintf(stderr, "[ar] R=%d count=%zu variant=%s ctas=%d threads=%d\n", h->R, count,
@@ -222,15 +247,23 @@ ar_status_t launch(ar_ctx* h, int variant, const TuneRow* row, const void* const
     case AR_TWOPHASE:
       e = ar::launch_twophase(h->R, a, cfg, s);
       break;
-    case AR_FUSED_LL8: {
+    case AR_ONESHOT_FANOUT_BULK:
+      e = ar::launch_oneshot_fanout_bulk(h->R, a, cfg.ctas, s);
+      break;
+    case AR_FUSED_LL8:
+    case AR_FUSED_LL8_STAGED:
+    case AR_PACKET_3OP: {
       FusedArgs f;
       f.scratch = h->scratch;
+      f.rscratch = h->rscratch;
       f.slot_groups = h->slot_groups;
       f.state = h->state;
       f.spin_limit_ns = h->spin_limit_ns;
       f.skip_producer = h->skip_producer;
       h->skip_producer = -1;
-      e = ar::launch_fused_ll8(h->R, a, f, cfg, s);
+      e = variant == AR_FUSED_LL8          ? ar::launch_fused_ll8(h->R, a, f, cfg, s)
+          : variant == AR_FUSED_LL8_STAGED ? ar::launch_fused_ll8_staged(h->R, a, f, cfg, s)
+                                           : ar::launch_packet_3op(h->R, a, f, cfg, s);
       break;
     }
     default:
@@ -262,6 +295,9 @@ const char* ar_variant_name(int variant) {
     case AR_ONESHOT_FANOUT: return "oneshot_fanout";
     case AR_TWOPHASE: return "twophase";
     case AR_FUSED_LL8: return "fused_ll8";
+    case AR_ONESHOT_FANOUT_BULK: return "oneshot_fanout_bulk";
+    case AR_FUSED_LL8_STAGED: return "fused_ll8_staged";
+    case AR_PACKET_3OP: return "packet_3op";
     default: return "?";
   }
 }
@@ -308,11 +344,14 @@ ar_status_t ar_create(int R, size_t max_count, int dtype, ar_handle_t* out) {
   h->slot_groups = ceil_div(groups, (size_t)R);
   h->scratch_bytes = (size_t)R * (size_t)(R - 1) * h->slot_groups * 4 * sizeof(uint64_t);
   h->fused_ctas_per_sm = occupancy(h, AR_FUSED_LL8, h->fused_threads);
+  if (ar::bulk_prepare(R) == cudaSuccess) h->bulk_ctas_per_sm = ar::bulk_ctas_per_sm(R);
+  cudaGetLastError();
 
   ar_status_t st = AR_OK;
   if (cudaMalloc(&h->state, sizeof(DevState)) != cudaSuccess) st = AR_ERR_OOM;
   if (st == AR_OK && h->scratch_bytes &&
-      cudaMalloc(&h->scratch, h->scratch_bytes) != cudaSuccess)
+      (cudaMalloc(&h->scratch, h->scratch_bytes) != cudaSuccess ||
+       cudaMalloc(&h->rscratch, h->scratch_bytes) != cudaSuccess))
     st = AR_ERR_OOM;
   if (st == AR_OK) {
     DevState init;
@@ -321,7 +360,9 @@ ar_status_t ar_create(int R, size_t max_count, int dtype, ar_handle_t* out) {
     if (cudaMemcpy(h->state, &init, sizeof init, cudaMemcpyHostToDevice) != cudaSuccess)
       st = AR_ERR_CUDA;
   }
-  if (st == AR_OK && h->scratch_bytes && cudaMemset(h->scratch, 0, h->scratch_bytes) != cudaSuccess)
+  if (st == AR_OK && h->scratch_bytes &&
+      (cudaMemset(h->scratch, 0, h->scratch_bytes) != cudaSuccess ||
+       cudaMemset(h->rscratch, 0, h->scratch_bytes) != cudaSuccess))
     st = AR_ERR_CUDA;
   if (st == AR_OK && cudaDeviceSynchronize() != cudaSuccess) st = AR_ERR_CUDA;
   if (st != AR_OK) {
@@ -341,6 +382,7 @@ ar_status_t ar_destroy(ar_handle_t h) {
   if (prev != h->device) cudaSetDevice(h->device);
   if (cudaDeviceSynchronize() != cudaSuccess) st = AR_ERR_CUDA;
   if (h->scratch && cudaFree(h->scratch) != cudaSuccess) st = AR_ERR_CUDA;
+  if (h->rscratch && cudaFree(h->rscratch) != cudaSuccess) st = AR_ERR_CUDA;
   if (h->state && cudaFree(h->state) != cudaSuccess) st = AR_ERR_CUDA;
   if (h->staging && cudaFree(h->staging) != cudaSuccess) st = AR_ERR_CUDA;
   if (h->staging_tables && cudaFree(h->staging_tables) != cudaSuccess) st = AR_ERR_CUDA;
@@ -384,7 +426,7 @@ ar_status_t ar_query(ar_handle_t h, ar_info_t* info) {
   info->R = h->R;
   info->dtype = AR_BF16;
   info->max_count = h->max_count;
-  info->scratch_bytes = h->scratch_bytes;
+  info->scratch_bytes = 2 * h->scratch_bytes;
   info->num_sms = h->num_sms;
   info->fused_max_ctas = h->fused_ctas_per_sm * h->num_sms;
   info->fused_threads = h->fused_threads;
@@ -402,6 +444,44 @@ ar_status_t ar_allreduce(ar_handle_t h, const void* const* d_in_tbl, void* const
   const TuneRow* row = nullptr;
   const int v = choose(h, count, &row);
   return launch(h, v, row, d_in_tbl, d_out_tbl, count, static_cast<cudaStream_t>(stream));
+}
+
+// Reduce-scatter (rs = true) or all-gather of blocks of `block` elements.
+static ar_status_t launch_block_collective(ar_handle_t h, bool rs, const void* const* d_in,
+                                           void* const* d_out, size_t block, void* stream) {
+  if (!h || !d_in || !d_out) return AR_ERR_INVALID_ARG;
+  if (block == 0) return AR_OK;
+  if (block > h->max_count / (size_t)h->R) return AR_ERR_INVALID_ARG;
+  ar_status_t st = check_device(h);
+  if (st != AR_OK) return st;
+  CallArgs a;
+  a.in_tbl = reinterpret_cast<const uint16_t* const*>(d_in);
+  a.out_tbl = reinterpret_cast<uint16_t* const*>(d_out);
+  a.count = block;
+  a.groups = ceil_div(block, (size_t)ar::kVecElems);
+  a.shard_groups = a.groups;
+  a.state = h->state;
+  a.spin_limit_ns = h->spin_limit_ns;
+  LaunchCfg cfg;
+  cfg.threads = 256;
+  const size_t cap = std::max<size_t>(1, (size_t)h->num_sms * 16 / (size_t)h->R);
+  cfg.ctas = (int)std::max<size_t>(1, std::min(ceil_div(a.groups, (size_t)cfg.threads), cap));
+  if (h->log)
+    fprintf(stderr, "[ar] R=%d %s block=%zu ctas=%dx%d threads=%d\n", h->R,
+            rs ? "reduce_scatter" : "all_gather", block, cfg.ctas, h->R, cfg.threads);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return cuda_status(rs ? ar::launch_reduce_scatter(h->R, a, cfg, s)
+                        : ar::launch_all_gather(h->R, a, cfg, s));
+}
+
+ar_status_t ar_reduce_scatter(ar_handle_t h, const void* const* d_in_tbl, void* const* d_out_tbl,
+                              size_t recvcount, void* stream) {
+  return launch_block_collective(h, true, d_in_tbl, d_out_tbl, recvcount, stream);
+}
+
+ar_status_t ar_all_gather(ar_handle_t h, const void* const* d_in_tbl, void* const* d_out_tbl,
+                          size_t sendcount, void* stream) {
+  return launch_block_collective(h, false, d_in_tbl, d_out_tbl, sendcount, stream);
 }
 
 ar_status_t ar_get_device_status(ar_handle_t h, void* stream) {

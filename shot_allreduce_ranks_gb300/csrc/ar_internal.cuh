@@ -25,7 +25,9 @@ struct DevState {
   uint32_t pad[10];
 };
 
-enum DevError : uint32_t { kDevErrNone = 0, kDevErrTimeout = 1 };
+// Device error codes.  kDevErrTimeout: an LL8 packet wait gave up.
+// kDevErrCopyTimeout: a wait for a bulk (TMA) copy into shared memory gave up.
+enum DevError : uint32_t { kDevErrNone = 0, kDevErrTimeout = 1, kDevErrCopyTimeout = 2 };
 
 // Everything a kernel needs about one call, passed by value.
 struct CallArgs {
@@ -34,11 +36,14 @@ struct CallArgs {
   size_t count;                   // elements per rank
   size_t groups;                  // ceil(count / 8)
   size_t shard_groups;            // ceil(groups / R): groups owned by each rank
+  DevState* state;                // the handle's state block (error word)
+  uint64_t spin_limit_ns;         // bound of every device-side wait
 };
 
 // Extra arguments of the fused packet kernel.
 struct FusedArgs {
   uint64_t* scratch;      // packets, layout [owner][source slot][group][4]
+  uint64_t* rscratch;     // result packets of the staged variants, [dest][owner slot][group][4]
   size_t slot_groups;     // groups per (owner, source) slot = shard_groups at max_count
   DevState* state;
   uint64_t spin_limit_ns;
@@ -221,11 +226,28 @@ cudaError_t launch_oneshot_fanout(int R, const CallArgs& a, LaunchCfg cfg, cudaS
 cudaError_t launch_twophase(int R, const CallArgs& a, LaunchCfg cfg, cudaStream_t s);
 cudaError_t launch_fused_ll8(int R, const CallArgs& a, const FusedArgs& f, LaunchCfg cfg,
                              cudaStream_t s);
+cudaError_t launch_fused_ll8_staged(int R, const CallArgs& a, const FusedArgs& f, LaunchCfg cfg,
+                                    cudaStream_t s);
+cudaError_t launch_packet_3op(int R, const CallArgs& a, const FusedArgs& f, LaunchCfg cfg,
+                              cudaStream_t s);
+int fused_staged_ctas_per_sm(int R, int threads);
+// Reduce-scatter / all-gather (k_rs_ag.cu): a.count is the block length;
+// the grid is (cfg.ctas, R).
+cudaError_t launch_reduce_scatter(int R, const CallArgs& a, LaunchCfg cfg, cudaStream_t s);
+cudaError_t launch_all_gather(int R, const CallArgs& a, LaunchCfg cfg, cudaStream_t s);
 
 // Occupancy (CTAs per SM) of the fused and fan-out kernels for R ranks and
 // `threads` threads per CTA.
 int fused_ctas_per_sm(int R, int threads);
 int fanout_ctas_per_sm(int R, int threads);
+
+// Bulk-copy fan-out (k_oneshot_bulk.cu): fixed 256 threads per CTA, dynamic
+// shared memory per CTA, CTAs per SM, and a one-time attribute set-up.
+constexpr int kBulkThreads = 256;
+size_t bulk_smem_bytes(int R);
+int bulk_ctas_per_sm(int R);
+cudaError_t bulk_prepare(int R);
+cudaError_t launch_oneshot_fanout_bulk(int R, const CallArgs& a, int ctas, cudaStream_t s);
 
 }  // namespace ar
 

@@ -101,11 +101,13 @@ struct Packets4 {
   }
 };
 
-// Packet slot of (owner o, source s != o): sources are packed, skipping o.
+// Packet slot (a, b != a) of a region laid out [a][b packed, skipping a]
+// [group][4]: for scatter packets a = owner, b = source; for result packets
+// (the staged variants) a = destination rank, b = owner.
 template <int R>
-__device__ __forceinline__ uint64_t* slot_base(const FusedArgs& f, int o, int s) {
-  const int slot = o * (R - 1) + (s < o ? s : s - 1);
-  return f.scratch + (size_t)slot * f.slot_groups * 4;
+__device__ __forceinline__ uint64_t* slot_ptr(uint64_t* region, size_t slot_groups, int a, int b) {
+  const int slot = a * (R - 1) + (b < a ? b : b - 1);
+  return region + (size_t)slot * slot_groups * 4;
 }
 
 // Records the first timeout in the (sticky) error word and marks this
@@ -120,112 +122,184 @@ __device__ __noinline__ void report_timeout(const FusedArgs& f, int owner, uint3
   st_relaxed_u32(&f.state->abort_epoch, epoch);
 }
 
+// Per-thread view of one launch of a packet kernel.
+struct Lane {
+  int r;              // virtual rank this CTA stands for (blockIdx.x % R)
+  size_t t0, tstride; // first group and group stride of this thread within a shard
+  size_t Vs;          // groups per shard
+  uint32_t epoch;
+  bool vec;
+  uint64_t pol_in;    // evict-first policy for input reads
+};
+
 template <int R>
-__global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, FusedArgs f) {
-  __shared__ const uint16_t* s_in[R];
-  __shared__ uint16_t* s_out[R];
+__device__ __forceinline__ Lane make_lane(const CallArgs& a, uint32_t epoch, bool vec) {
+  Lane l;
+  l.r = (int)(blockIdx.x % R);
+  l.t0 = (size_t)(blockIdx.x / R) * blockDim.x + threadIdx.x;
+  l.tstride = (size_t)(gridDim.x / R) * blockDim.x;
+  l.Vs = a.shard_groups;
+  l.epoch = epoch;
+  l.vec = vec;
+  l.pol_in = l2_policy_evict_first();
+  return l;
+}
+
+// Prologue of every packet kernel: pointer tables into shared memory, the
+// call's epoch read once by thread 0 and shared with the CTA.
+template <int R>
+__device__ __forceinline__ Lane packet_prologue(const CallArgs& a, const FusedArgs& f,
+                                                const uint16_t** s_in, uint16_t** s_out) {
   __shared__ uint32_t s_epoch;
   const bool vec = load_tables<R>(a, s_in, s_out);
   if (threadIdx.x == 0) s_epoch = ld_relaxed_u32(&f.state->epoch);
   __syncthreads();
-  const uint32_t epoch = s_epoch;
+  return make_lane<R>(a, s_epoch, vec);
+}
 
-  const int r = (int)(blockIdx.x % R);
-  const size_t C = gridDim.x / R;
-  const size_t t0 = (size_t)(blockIdx.x / R) * blockDim.x + threadIdx.x;
-  const size_t tstride = C * blockDim.x;
-  const size_t Vs = a.shard_groups;
-  const uint16_t* my_in = s_in[r];
-
-  // Inputs stream through once: evict-first, so they do not push packets
-  // out of L2 before their owners read them.
-  const uint64_t pol_in = l2_policy_evict_first();
-
-  // ---- scatter: packets of rank r for every other owner -------------------
-  // Two groups (j, j + tstride) per iteration: all 2(R-1) loads are issued
-  // before the first packet store.
-  if (R > 1 && r != f.skip_producer) {
-    for (size_t j = t0; j < Vs; j += 2 * tstride) {
-      const size_t j2 = j + tstride;
-      uint4 x[R > 1 ? R - 1 : 1], y[R > 1 ? R - 1 : 1];
+// Waits until every packet set s in `pending` (already loaded once into
+// pk[s]) carries the epoch, re-polling slot_ptr(region, a_idx, s) + j * 4.
+// Bounded: after spin_limit_ns of %globaltimer (or an iteration cap, a
+// backstop in case the timer did not advance; every iteration is at least
+// one L2 round trip) it records a timeout and returns false; it also
+// returns false as soon as another waiter of this call has given up.
+template <int R>
+__device__ __forceinline__ bool wait_packets(const FusedArgs& f, uint64_t* region, int a_idx,
+                                             size_t j, Packets4 (&pk)[R], uint32_t pending,
+                                             uint32_t epoch) {
 #pragma unroll
-      for (int k = 1; k < R; ++k) {
-        const int o = (r + k) % R;
-        const size_t g = (size_t)o * Vs + j;
-        if (g < a.groups) x[k - 1] = load_group<true>(my_in, g, group_valid(g, a.count), vec, pol_in);
-        const size_t g2 = (size_t)o * Vs + j2;
-        if (j2 < Vs && g2 < a.groups)
-          y[k - 1] = load_group<true>(my_in, g2, group_valid(g2, a.count), vec, pol_in);
-      }
+  for (int s = 0; s < R; ++s)
+    if ((pending & (1u << s)) && pk[s].arrived(epoch)) pending &= ~(1u << s);
+  if (!pending) return true;
+  uint64_t t_first = 0;
+  uint32_t spins = 0;
+  while (pending) {
+    __nanosleep(32);
 #pragma unroll
-      for (int k = 1; k < R; ++k) {
-        const int o = (r + k) % R;
-        const size_t g = (size_t)o * Vs + j;
-        uint64_t* slot = slot_base<R>(f, o, r);
-        if (g < a.groups) st_packets(slot + j * 4, x[k - 1], epoch);
-        const size_t g2 = (size_t)o * Vs + j2;
-        if (j2 < Vs && g2 < a.groups) st_packets(slot + j2 * 4, y[k - 1], epoch);
+    for (int s = 0; s < R; ++s) {
+      if (pending & (1u << s)) {
+        pk[s].load(slot_ptr<R>(region, f.slot_groups, a_idx, s) + j * 4);
+        if (pk[s].arrived(epoch)) pending &= ~(1u << s);
       }
     }
+    if (pending && (++spins & 15u) == 0) {
+      const uint64_t now = global_timer_ns();
+      if (spins == 16u) t_first = now;
+      if (spins > kMaxSpins || (spins > 16u && now - t_first > f.spin_limit_ns)) {
+        report_timeout(f, a_idx, pending, epoch);
+        return false;
+      }
+      if (ld_relaxed_u32(&f.state->abort_epoch) == epoch) return false;
+    }
   }
+  return true;
+}
 
-  // ---- reduce + write-mode broadcast of owner r's shard -------------------
-  const size_t g0 = (size_t)r * Vs;
-  const size_t n = g0 < a.groups ? min(Vs, a.groups - g0) : 0;
-  bool aborted = false;
-  for (size_t j = t0; j < n && !aborted; j += tstride) {
+// ---- scatter: rank r's slices of every other owner's shard, as packets ----
+// Two groups (j, j + tstride) per iteration: all 2(R-1) loads are issued
+// before the first packet store.
+template <int R>
+__device__ __forceinline__ void phase_scatter(const CallArgs& a, const FusedArgs& f, const Lane& l,
+                                              const uint16_t* my_in) {
+  if (R == 1 || l.r == f.skip_producer) return;
+  for (size_t j = l.t0; j < l.Vs; j += 2 * l.tstride) {
+    const size_t j2 = j + l.tstride;
+    uint4 x[R > 1 ? R - 1 : 1], y[R > 1 ? R - 1 : 1];
+#pragma unroll
+    for (int k = 1; k < R; ++k) {
+      const int o = (l.r + k) % R;
+      const size_t g = (size_t)o * l.Vs + j;
+      if (g < a.groups)
+        x[k - 1] = load_group<true>(my_in, g, group_valid(g, a.count), l.vec, l.pol_in);
+      const size_t g2 = (size_t)o * l.Vs + j2;
+      if (j2 < l.Vs && g2 < a.groups)
+        y[k - 1] = load_group<true>(my_in, g2, group_valid(g2, a.count), l.vec, l.pol_in);
+    }
+#pragma unroll
+    for (int k = 1; k < R; ++k) {
+      const int o = (l.r + k) % R;
+      uint64_t* slot = slot_ptr<R>(f.scratch, f.slot_groups, o, l.r);
+      const size_t g = (size_t)o * l.Vs + j;
+      if (g < a.groups) st_packets(slot + j * 4, x[k - 1], l.epoch);
+      const size_t g2 = (size_t)o * l.Vs + j2;
+      if (j2 < l.Vs && g2 < a.groups) st_packets(slot + j2 * 4, y[k - 1], l.epoch);
+    }
+  }
+}
+
+// ---- reduce owner r's shard ------------------------------------------------
+// Polls the R-1 sources' packets of each group, sums the R contributions in
+// rank order (own input at position r), rounds once.  kWriteMode: store the
+// group into all R outputs.  Otherwise: store it into out_r only and send it
+// as result packets to every other rank's result slot for owner r.
+// Returns false if the call was abandoned after a timeout.
+template <int R, bool kWriteMode>
+__device__ __forceinline__ bool phase_reduce(const CallArgs& a, const FusedArgs& f, const Lane& l,
+                                             const uint16_t* my_in, uint16_t* const* s_out) {
+  const size_t g0 = (size_t)l.r * l.Vs;
+  const size_t n = g0 < a.groups ? min(l.Vs, a.groups - g0) : 0;
+  for (size_t j = l.t0; j < n; j += l.tstride) {
     const size_t g = g0 + j;
     const int valid = group_valid(g, a.count);
-    const uint4 own = load_group<true>(my_in, g, valid, vec, pol_in);
+    const uint4 own = load_group<true>(my_in, g, valid, l.vec, l.pol_in);
     Packets4 pk[R];
     uint32_t pending = 0;
 #pragma unroll
     for (int s = 0; s < R; ++s)
-      if (s != r) pk[s].load(slot_base<R>(f, r, s) + j * 4);
-#pragma unroll
-    for (int s = 0; s < R; ++s)
-      if (s != r && !pk[s].arrived(epoch)) pending |= 1u << s;
-    if (pending) {
-      uint64_t t_first = 0;
-      uint32_t spins = 0;
-      while (pending) {
-        __nanosleep(32);
-#pragma unroll
-        for (int s = 0; s < R; ++s) {
-          if (pending & (1u << s)) {
-            pk[s].load(slot_base<R>(f, r, s) + j * 4);
-            if (pk[s].arrived(epoch)) pending &= ~(1u << s);
-          }
-        }
-        if (pending && (++spins & 15u) == 0) {
-          // Give up after spin_limit_ns of %globaltimer; the iteration cap
-          // (each iteration is at least one L2 round trip) is a backstop
-          // that bounds the wait even if the timer did not advance.
-          const uint64_t now = global_timer_ns();
-          if (spins == 16u) t_first = now;
-          if (spins > kMaxSpins || (spins > 16u && now - t_first > f.spin_limit_ns)) {
-            report_timeout(f, r, pending, epoch);
-            aborted = true;
-            break;
-          }
-          if (ld_relaxed_u32(&f.state->abort_epoch) == epoch) {
-            aborted = true;
-            break;
-          }
-        }
+      if (s != l.r) {
+        pk[s].load(slot_ptr<R>(f.scratch, f.slot_groups, l.r, s) + j * 4);
+        pending |= 1u << s;
       }
-      if (aborted) break;
-    }
+    if (!wait_packets<R>(f, f.scratch, l.r, j, pk, pending, l.epoch)) return false;
     Acc8 acc;
-    acc.set(r == 0 ? own : pk[0].data());
+    acc.set(l.r == 0 ? own : pk[0].data());
 #pragma unroll
-    for (int s = 1; s < R; ++s) acc.add(s == r ? own : pk[s].data());
+    for (int s = 1; s < R; ++s) acc.add(s == l.r ? own : pk[s].data());
     const uint4 y = acc.round_bf16();
+    if (kWriteMode) {
 #pragma unroll
-    for (int q = 0; q < R; ++q) store_group(s_out[q], g, y, valid, vec);
+      for (int q = 0; q < R; ++q) store_group(s_out[q], g, y, valid, l.vec);
+    } else {
+      store_group(s_out[l.r], g, y, valid, l.vec);
+#pragma unroll
+      for (int q = 0; q < R; ++q)
+        if (q != l.r) st_packets(slot_ptr<R>(f.rscratch, f.slot_groups, q, l.r) + j * 4, y, l.epoch);
+    }
   }
+  return true;
+}
 
-  // ---- flag rotation: the last CTA to finish advances the epoch ------------
+// ---- receive: rank r copies every other owner's reduced shard out of its
+// result slots into out_r (the staged variants' last step) -------------------
+template <int R>
+__device__ __forceinline__ bool phase_recv(const CallArgs& a, const FusedArgs& f, const Lane& l,
+                                           uint16_t* const* s_out) {
+  if (R == 1) return true;
+  uint16_t* my_out = s_out[l.r];
+  for (size_t j = l.t0; j < l.Vs; j += l.tstride) {
+    Packets4 pk[R];
+    uint32_t pending = 0;
+#pragma unroll
+    for (int o = 0; o < R; ++o)
+      if (o != l.r && (size_t)o * l.Vs + j < a.groups) {
+        pk[o].load(slot_ptr<R>(f.rscratch, f.slot_groups, l.r, o) + j * 4);
+        pending |= 1u << o;
+      }
+    const uint32_t present = pending;
+    if (!wait_packets<R>(f, f.rscratch, l.r, j, pk, pending, l.epoch)) return false;
+#pragma unroll
+    for (int o = 0; o < R; ++o)
+      if (present & (1u << o)) {
+        const size_t g = (size_t)o * l.Vs + j;
+        store_group(my_out, g, pk[o].data(), group_valid(g, a.count), l.vec);
+      }
+  }
+  return true;
+}
+
+// ---- flag rotation: the last CTA of the call's last kernel advances the
+// epoch (skipping 0) and resets the done counter ------------------------------
+__device__ __forceinline__ void epoch_advance(const FusedArgs& f, uint32_t epoch) {
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
@@ -240,12 +314,114 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, Fuse
   }
 }
 
+// Write mode: scatter -> reduce -> broadcast straight into all R outputs.
+template <int R>
+__global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, FusedArgs f) {
+  __shared__ const uint16_t* s_in[R];
+  __shared__ uint16_t* s_out[R];
+  const Lane l = packet_prologue<R>(a, f, s_in, s_out);
+  phase_scatter<R>(a, f, l, s_in[l.r]);
+  phase_reduce<R, true>(a, f, l, s_in[l.r], s_out);
+  epoch_advance(f, l.epoch);
+}
+
+// Without write mode (the packet broadcast of the ARK page): scatter ->
+// reduce -> result packets to every rank -> every rank copies them out.
+template <int R>
+__global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8_staged(CallArgs a, FusedArgs f) {
+  __shared__ const uint16_t* s_in[R];
+  __shared__ uint16_t* s_out[R];
+  const Lane l = packet_prologue<R>(a, f, s_in, s_out);
+  phase_scatter<R>(a, f, l, s_in[l.r]);
+  if (phase_reduce<R, false>(a, f, l, s_in[l.r], s_out)) phase_recv<R>(a, f, l, s_out);
+  epoch_advance(f, l.epoch);
+}
+
+// The three-launch decomposition the ARK page replaced (send_packet ->
+// recv_reduce_send_packet -> recv_packet): the same phases, one kernel each,
+// ordered by kernel boundaries instead of by co-residency.
+template <int R>
+__global__ void __launch_bounds__(kFusedMaxThreads) k_packet_send(CallArgs a, FusedArgs f) {
+  __shared__ const uint16_t* s_in[R];
+  __shared__ uint16_t* s_out[R];
+  const Lane l = packet_prologue<R>(a, f, s_in, s_out);
+  phase_scatter<R>(a, f, l, s_in[l.r]);
+}
+
+template <int R>
+__global__ void __launch_bounds__(kFusedMaxThreads) k_packet_reduce_send(CallArgs a, FusedArgs f) {
+  __shared__ const uint16_t* s_in[R];
+  __shared__ uint16_t* s_out[R];
+  const Lane l = packet_prologue<R>(a, f, s_in, s_out);
+  phase_reduce<R, false>(a, f, l, s_in[l.r], s_out);
+}
+
+template <int R>
+__global__ void __launch_bounds__(kFusedMaxThreads) k_packet_recv(CallArgs a, FusedArgs f) {
+  __shared__ const uint16_t* s_in[R];
+  __shared__ uint16_t* s_out[R];
+  const Lane l = packet_prologue<R>(a, f, s_in, s_out);
+  phase_recv<R>(a, f, l, s_out);
+  epoch_advance(f, l.epoch);
+}
+
 }  // namespace
 
 int fused_ctas_per_sm(int R, int threads) {
   int n = 0;
   cudaError_t e = cudaErrorInvalidValue;
 #define Q(RR) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_fused_ll8<RR>, threads, 0)
+  switch (R) {
+    case 1: Q(1); break;
+    case 2: Q(2); break;
+    case 3: Q(3); break;
+    case 4: Q(4); break;
+    case 5: Q(5); break;
+    case 6: Q(6); break;
+    case 7: Q(7); break;
+    case 8: Q(8); break;
+    default: return 0;
+  }
+#undef Q
+  return e == cudaSuccess ? n : 0;
+}
+
+cudaError_t launch_fused_ll8_staged(int R, const CallArgs& a, const FusedArgs& f, LaunchCfg cfg,
+                                    cudaStream_t s) {
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3((unsigned)cfg.ctas);
+  lc.blockDim = dim3((unsigned)cfg.threads);
+  lc.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+#define L(RR) return cudaLaunchKernelEx(&lc, k_fused_ll8_staged<RR>, a, f)
+  AR_RANK_SWITCH(R, L)
+#undef L
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_packet_3op(int R, const CallArgs& a, const FusedArgs& f, LaunchCfg cfg,
+                              cudaStream_t s) {
+  cudaError_t e = cudaSuccess;
+#define L(RR)                                                                  \
+  k_packet_send<RR><<<cfg.ctas, cfg.threads, 0, s>>>(a, f);                    \
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;                       \
+  k_packet_reduce_send<RR><<<cfg.ctas, cfg.threads, 0, s>>>(a, f);             \
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;                       \
+  k_packet_recv<RR><<<cfg.ctas, cfg.threads, 0, s>>>(a, f);                    \
+  return cudaGetLastError()
+  AR_RANK_SWITCH(R, L)
+#undef L
+  return cudaErrorInvalidValue;
+}
+
+int fused_staged_ctas_per_sm(int R, int threads) {
+  int n = 0;
+  cudaError_t e = cudaErrorInvalidValue;
+#define Q(RR) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_fused_ll8_staged<RR>, threads, 0)
   switch (R) {
     case 1: Q(1); break;
     case 2: Q(2); break;
@@ -361,8 +537,11 @@ extern "C" ar_status_t ar_allreduce_fused_noalloc(int R, const void* const* d_in
   a.count = count;
   a.groups = (count + ar::kVecElems - 1) / ar::kVecElems;
   a.shard_groups = (a.groups + (size_t)R - 1) / (size_t)R;
+  a.state = d.state;
+  a.spin_limit_ns = 100ull * 1000ull * 1000ull;
   ar::FusedArgs f;
   f.scratch = d.scratch;
+  f.rscratch = nullptr;
   f.slot_groups = a.shard_groups;  // R*(R-1)*slot_groups*32 <= scratch bytes by the check above
   f.state = d.state;
   f.spin_limit_ns = 100ull * 1000ull * 1000ull;

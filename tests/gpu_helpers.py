@@ -9,7 +9,8 @@ import oracle
 from shot_allreduce_ranks_gb300 import AllReduce, build, inputs
 
 DEV = "cuda"
-PARITY_VARIANTS = ["oneshot_pull", "oneshot_fanout", "twophase", "fused_ll8"]
+PARITY_VARIANTS = ["oneshot_pull", "oneshot_fanout", "twophase", "fused_ll8",
+                   "oneshot_fanout_bulk", "fused_ll8_staged", "packet_3op"]
 
 _handles = {}
 

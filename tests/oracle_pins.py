@@ -222,10 +222,63 @@ def pin_outputs_identical_and_in_place(lib):
     return fails
 
 
+# --------------------------------------------------------------------------
+# Reduce-scatter and all-gather (the other two collectives the one-shot
+# kernel of the torchcomms relay page serves).
+
+def pin_reduce_scatter_exact(lib):
+    fails = []
+    for R, rc in ((1, 13), (2, 7), (4, 1003), (8, 129)):
+        for fill in ("ints", "position"):
+            xs = inputs.make_inputs(R, R * rc, seed=R + rc, fill=fill)
+            ints = np.stack([x.to(torch.int64).numpy() for x in xs])
+            outs = oracle.reduce_scatter_bf16([inputs.bits(x) for x in xs], lib=lib)
+            for r in range(R):
+                exact = ints[:, r * rc:(r + 1) * rc].sum(axis=0)
+                want = np.array([bf16_bits_of(float(v)) for v in exact.tolist()], np.uint16)
+                if not np.array_equal(outs[r], want):
+                    fails.append("reduce-scatter %s R=%d rc=%d block %d not exact" % (fill, R, rc, r))
+    return fails
+
+
+def pin_reduce_scatter_order(lib):
+    """The rank-order closed form placed in one block of a 4-rank call."""
+    fails = []
+    R, rc = 4, 5
+    vals = [P24, 1.0, 1.0, -P24]
+    for blk in range(R):
+        xs = []
+        for s in range(R):
+            a = np.zeros(R * rc, np.uint16)
+            a[blk * rc:(blk + 1) * rc] = bf16_bits_of(vals[s])
+            xs.append(a)
+        outs = oracle.reduce_scatter_bf16(xs, lib=lib)
+        for r in range(R):
+            want = 0 if r != blk else bf16_bits_of(0.0)
+            if not (outs[r] == want).all():
+                fails.append("reduce-scatter order case, block %d, rank %d" % (blk, r))
+    return fails
+
+
+def pin_all_gather_exact(lib):
+    fails = []
+    for R, sc in ((1, 9), (3, 17), (8, 257)):
+        xs = inputs.make_inputs(R, sc, seed=0, fill="position")
+        outs = oracle.all_gather_bf16([inputs.bits(x) for x in xs], lib=lib)
+        for r in range(R):
+            for s in range(R):
+                # the position fill written out again from its formula
+                want = [bf16_bits_of(float(((7 * j + 13 * s) % 17) - 8)) for j in range(sc)]
+                if outs[r][s * sc:(s + 1) * sc].tolist() != want:
+                    fails.append("all-gather R=%d rank %d block %d" % (R, r, s))
+    return fails
+
+
 ALL_PINS = [
     pin_identity, pin_all_ones, pin_small_integers, pin_position_fill,
     pin_closed_forms, pin_rounding, pin_tiny_brute_force,
-    pin_outputs_identical_and_in_place,
+    pin_outputs_identical_and_in_place, pin_reduce_scatter_exact, pin_reduce_scatter_order,
+    pin_all_gather_exact,
 ]
 
 

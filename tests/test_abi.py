@@ -52,6 +52,9 @@ def test_create_rejects_bad_arguments_before_touching_the_device(lib):
 def test_null_handle_calls(lib):
     assert lib.ar_allreduce(None, 1, 1, 8, None) == _lib.AR_ERR_INVALID_ARG
     assert lib.ar_allreduce_host(None, 1, 1, 8, None) == _lib.AR_ERR_INVALID_ARG
+    assert lib.ar_reduce_scatter(None, 1, 1, 8, None) == _lib.AR_ERR_INVALID_ARG
+    assert lib.ar_all_gather(None, 1, 1, 8, None) == _lib.AR_ERR_INVALID_ARG
+    assert lib.ar_allreduce_fused_noalloc(0, 1, 1, 8, None) == _lib.AR_ERR_INVALID_ARG
     assert lib.ar_destroy(None) == _lib.AR_OK
     assert lib.ar_set_variant(None, 0) == _lib.AR_ERR_INVALID_ARG
     v = ctypes.c_int()

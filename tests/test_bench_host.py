@@ -24,6 +24,8 @@ def test_alg_bytes_match_the_roofline_table():
     assert bench.alg_bytes("twophase", 1, 100) == 400
     assert bench.launches_per_call("twophase", 8) == 2
     assert bench.launches_per_call("fused_ll8", 8) == 1
+    assert bench.launches_per_call("packet_3op", 8) == 3
+    assert bench.alg_bytes("fused_ll8_staged", 8, N) == 4 * 8 * N + 16 * 7 * N
 
 
 def test_whole_job_aggregation():

@@ -53,11 +53,29 @@ def test_epoch_wraps_to_one_skipping_zero(ar):
     G.check_all_outputs(outs, want, "epoch 1 after wrap")
 
 
+PACKET_VARIANTS = ["fused_ll8", "fused_ll8_staged", "packet_3op"]
+
+
+@pytest.mark.parametrize("variant", PACKET_VARIANTS)
+def test_epoch_advances_once_per_call_every_packet_variant(ar, variant):
+    xs = inputs.make_inputs(R, COUNT, 11)
+    bufs, outs = _bufs(xs)
+    ar.set_variant(variant)
+    e0 = ar.debug_get_epoch()
+    for _ in range(3):
+        ar(bufs, outs)
+    assert ar.debug_get_epoch() == e0 + 3
+    G.check_all_outputs(outs, G.oracle_expect(xs), variant)
+    ar.set_variant("fused_ll8")
+
+
+@pytest.mark.parametrize("variant", PACKET_VARIANTS)
 @pytest.mark.parametrize("skip", [0, 3, R - 1])
-def test_missing_producer_times_out_and_next_call_recovers(ar, skip):
+def test_missing_producer_times_out_and_next_call_recovers(ar, variant, skip):
     """Rank `skip` stores no packets for one call: its owners' waits run out
     after the (short) spin limit, the device error word says so, and the
     next call, with a newer epoch, is correct."""
+    ar.set_variant(variant)
     xs = inputs.make_inputs(R, COUNT, 3)
     want = G.oracle_expect(xs)
     bufs, outs = _bufs(xs)
@@ -71,6 +89,7 @@ def test_missing_producer_times_out_and_next_call_recovers(ar, skip):
     assert ar.device_status() == AR_OK
     G.check_all_outputs(outs, want, "call after a timeout")
     ar.set_spin_limit_ns(100_000_000)
+    ar.set_variant("fused_ll8")
 
 
 def test_stale_packets_are_rejected(ar):

@@ -63,6 +63,15 @@ MUTANTS = [
      "uint32_t u = (uint32_t)b << 15;"),
     ("sign bit lost in rounding", "const uint32_t lower = u >> 16;",
      "const uint32_t lower = (u >> 16) & 0x7FFFu;"),
+    ("reduce-scatter reads block 0 for every rank", "const size_t base = (size_t)r * recvcount;",
+     "const size_t base = 0;"),
+    ("reduce-scatter in reversed rank order",
+     "float acc = bf16_to_f32(in[0][base + j]);\n      for (int s = 1; s < R; ++s) acc = acc + bf16_to_f32(in[s][base + j]);",
+     "float acc = bf16_to_f32(in[R - 1][base + j]);\n      for (int s = R - 2; s >= 0; --s) acc = acc + bf16_to_f32(in[s][base + j]);"),
+    ("all-gather copies the own rank", "out[r][(size_t)s * sendcount + j] = in[s][j];",
+     "out[r][(size_t)s * sendcount + j] = in[r][j];"),
+    ("all-gather blocks in the wrong order", "out[r][(size_t)s * sendcount + j] = in[s][j];",
+     "out[r][(size_t)(R - 1 - s) * sendcount + j] = in[s][j];"),
 ]
 
 
