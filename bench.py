@@ -139,14 +139,23 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_digest() -> str:
+KERNEL_SOURCES = {
+    "fused_ll8": "k_fused_ll8.cu", "fused_ll8_staged": "k_fused_ll8.cu",
+    "packet_3op": "k_fused_ll8.cu", "oneshot_fanout": "k_oneshot.cu",
+    "oneshot_pull": "k_oneshot.cu", "oneshot_fanout_bulk": "k_oneshot_bulk.cu",
+    "twophase": "k_twophase.cu",
+}
+
+
+def kernel_source_digest(kernel: str) -> str:
+    """Digest of the sources a kernel is compiled from (its file and the
+    shared device header)."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "shot_allreduce_ranks_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    for name in ("ar_internal.cuh", KERNEL_SOURCES[kernel]):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
@@ -161,7 +170,7 @@ def profiled_traffic(kernel: str, workload: str):
                 if ":" in line and not line.startswith("#"):
                     k, v = line.split(":", 1)
                     fields[k.strip()] = v.strip()
-        if fields.get("source_digest") != kernel_source_digest():
+        if fields.get("source_digest") != kernel_source_digest(kernel):
             return None
         return int(float(fields["dram_bytes_per_launch"]))
     except Exception:
