@@ -37,6 +37,11 @@
  *     as three launches (that page's send_packet -> recv_reduce_send_packet
  *     -> recv_packet decomposition).  Both exist to measure what write mode
  *     and fusion save;
+ *   - AR_FUSED_LL8_RING is AR_FUSED_LL8 with its packets in a ring of a few
+ *     rounds per (owner, source, CTA) instead of a region sized for the
+ *     whole message: producers take credits from the owners' progress words
+ *     before reusing a slot, and the flag advances once per round, so the
+ *     packet footprint stays small enough to live in L2;
  *   - AR_FUSED_LL8 is the single fused scatter -> reduce -> broadcast kernel
  *     synchronised by LL packet flags of "Add monolithic fused packet
  *     allreduce kernel and Model::all_reduce_packet API" (microsoft/ark #254,
@@ -90,10 +95,11 @@ typedef enum {
   AR_FUSED_LL8 = 4,      /* one persistent kernel: LL8 packet scatter, poll+reduce, write mode */
   AR_ONESHOT_FANOUT_BULK = 5, /* fan-out with tiles moved by bulk (TMA) copies through shared memory */
   AR_FUSED_LL8_STAGED = 6,    /* fused LL8 without write mode: result packets back to every rank */
-  AR_PACKET_3OP = 7           /* the same three packet phases as three separate launches */
+  AR_PACKET_3OP = 7,          /* the same three packet phases as three separate launches */
+  AR_FUSED_LL8_RING = 8       /* AR_FUSED_LL8 with packets in a small per-CTA ring (credits) */
 } ar_variant_t;
 
-#define AR_NUM_VARIANTS 8
+#define AR_NUM_VARIANTS 9
 
 /* Static description of a handle (filled by ar_query). */
 typedef struct {
@@ -116,8 +122,10 @@ typedef struct {
  *   out        receives the handle (set to NULL on failure).
  * Allocates, on the current device, two packet scratch regions (scatter
  * packets and the staged variants' result packets), each
- * 32 * R * (R-1) * ceil(ceil(max_count/8)/R) bytes (about
- * 4*(R-1)*max_count), zeroed here so that no flag matches a live epoch, and
+ * 32 * R * (R-1) * S bytes with S = ceil(ceil(max_count/8)/R) rounded up
+ * to a multiple of 4 (about 4*(R-1)*max_count); the ring variant's packet ring (32 * R * (R-1) * 4 *
+ * the co-resident threads per rank, independent of max_count) and its
+ * progress words; all zeroed here so that no flag matches a live epoch; and
  * a small state block (epoch, done counter, error word).  Synchronous; not
  * for stream capture.
  * Errors: AR_ERR_INVALID_ARG (R, max_count, out), AR_ERR_UNSUPPORTED (dtype,
@@ -230,12 +238,19 @@ const char* ar_variant_name(int variant);
  * ar_allreduce_host.  Synchronous.  AR_ERR_OOM / AR_ERR_CUDA on failure.
  *
  * ar_allreduce_host -- h_in[r] / h_out[r] are HOST pointers (host arrays of
- * R host pointers; page-locked memory lets the copies run asynchronously).
- * On `stream`: one cudaMemcpyAsync per rank into the staging inputs, the
- * allreduce (same variant selection as ar_allreduce), one cudaMemcpyAsync
- * per rank back into h_out[r].  Returns after enqueueing; the caller
- * synchronises `stream` before reading h_out.  AR_ERR_INVALID_ARG if the
- * staging was not reserved or count > max_count.
+ * R host pointers).  When every buffer is page-locked (or device memory),
+ * the kernel reads and writes the buffers where they are -- page-locked
+ * host memory is device-addressable through unified addressing, over
+ * NVLink-C2C on Grace-Blackwell -- so each input byte crosses to the device
+ * once and each output byte back once, both directions concurrently; with
+ * AR_AUTO this path runs AR_ONESHOT_FANOUT (one read and one write per
+ * byte), otherwise the forced variant (AR_ONESHOT_FANOUT_BULK always
+ * takes the staging path).  Otherwise (pageable memory) on
+ * `stream`: one cudaMemcpyAsync per rank into the staging inputs, the
+ * allreduce (same selection as ar_allreduce), one cudaMemcpyAsync per rank
+ * back into h_out[r].  Returns after enqueueing; the caller synchronises
+ * `stream` before reading h_out.  AR_ERR_INVALID_ARG if the staging was not
+ * reserved or count > max_count.
  */
 ar_status_t ar_reserve_host_staging(ar_handle_t h);
 ar_status_t ar_allreduce_host(ar_handle_t h, const void* const* h_in,
@@ -250,6 +265,10 @@ ar_status_t ar_allreduce_host(ar_handle_t h, const void* const* h_in,
  *
  * ar_debug_set_epoch / ar_debug_get_epoch -- synchronous write / read of
  * the device epoch (for testing the wrap from 2^32-1 to 1, which skips 0).
+ * Setting it also zeroes every packet region and the ring progress words,
+ * so that no packet or credit left from before the jump can match the new
+ * epoch's flags (in normal use the epoch only moves forward one step per
+ * call or per ring round, and a stale match needs a full 2^32 wrap).
  */
 ar_status_t ar_debug_skip_producer(ar_handle_t h, int rank);
 ar_status_t ar_debug_set_epoch(ar_handle_t h, uint32_t epoch);

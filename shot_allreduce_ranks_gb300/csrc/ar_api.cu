@@ -60,6 +60,12 @@ struct ar_ctx {
   uint64_t* scratch = nullptr;   // scatter packets
   uint64_t* rscratch = nullptr;  // result packets (staged variants)
   size_t scratch_bytes = 0;      // bytes of each region
+  uint64_t* ring = nullptr;      // ring variant's packets
+  size_t ring_bytes = 0;
+  size_t ring_threads = 0;       // threads per rank the ring can hold (C * T)
+  uint32_t* progress = nullptr;  // ring variant's progress words [R][kMaxRingCtas]
+  int ring_depth = 2;
+  uint32_t fused_opts = 0;       // kFusedOpt* bits for the write-mode fused kernels
   size_t slot_groups = 0;
   uint64_t spin_limit_ns = 100ull * 1000ull * 1000ull;
   int skip_producer = -1;
@@ -68,12 +74,14 @@ struct ar_ctx {
   // Occupancy cache (CTAs per SM) indexed by threads / 32; 0 = not queried.
   int occ_fused[33] = {};
   int occ_staged[33] = {};
+  int occ_ring[33] = {};
   int occ_fanout[33] = {};
   int bulk_ctas_per_sm = 0;    // bulk fan-out (fixed 256 threads)
 
   // host-buffer path
   uint16_t* staging = nullptr;        // 2 * R * max_count elements
   uint16_t** staging_tables = nullptr;  // device: R input pointers, then R output pointers
+  uint16_t** direct_tables = nullptr;   // device: the caller's buffers, when device-accessible
 };
 
 namespace {
@@ -140,12 +148,14 @@ int choose(const ar_ctx* h, size_t count, const TuneRow** row) {
 int occupancy(ar_ctx* h, int variant, int threads) {
   int* cache = variant == AR_FUSED_LL8          ? h->occ_fused
                : variant == AR_FUSED_LL8_STAGED ? h->occ_staged
+               : variant == AR_FUSED_LL8_RING   ? h->occ_ring
                                                 : h->occ_fanout;
   const int k = threads / 32;
   if (k < 0 || k > 32) return 0;
   if (cache[k] == 0) {
     const int n = variant == AR_FUSED_LL8          ? ar::fused_ctas_per_sm(h->R, threads)
                   : variant == AR_FUSED_LL8_STAGED ? ar::fused_staged_ctas_per_sm(h->R, threads)
+                  : variant == AR_FUSED_LL8_RING   ? ar::fused_ring_ctas_per_sm(h->R, threads)
                                                    : ar::fanout_ctas_per_sm(h->R, threads);
     cache[k] = n > 0 ? n : -1;
   }
@@ -203,6 +213,19 @@ LaunchCfg shape(ar_ctx* h, int variant, const TuneRow* row, size_t groups, size_
       c.ctas = (int)(per_rank * (size_t)R);
       break;
     }
+    case AR_FUSED_LL8_RING: {
+      // Co-resident, at most kMaxRingCtas per rank, and C * T within the ring.
+      if (c.threads <= 0) c.threads = h->fused_threads;
+      const int per_sm = occupancy(h, variant, c.threads);
+      size_t limit = (size_t)per_sm * (size_t)h->num_sms / (size_t)R;
+      limit = std::min(limit, (size_t)ar::kMaxRingCtas);
+      limit = std::min(limit, h->ring_threads / (size_t)c.threads);
+      size_t per_rank = std::max<size_t>(1, ceil_div(shard_groups, (size_t)c.threads));
+      if (c.ctas > 0) per_rank = std::max<size_t>(1, (size_t)c.ctas / (size_t)R);
+      per_rank = std::min(per_rank, limit);
+      c.ctas = (int)(per_rank * (size_t)R);
+      break;
+    }
     case AR_FUSED_LL8:
     case AR_FUSED_LL8_STAGED: {
       if (c.threads <= 0) c.threads = h->fused_threads;
@@ -255,6 +278,21 @@ ar_status_t launch(ar_ctx* h, int variant, const TuneRow* row, const void* const
     case AR_ONESHOT_FANOUT_BULK:
       e = ar::launch_oneshot_fanout_bulk(h->R, a, cfg.ctas, s);
       break;
+    case AR_FUSED_LL8_RING: {
+      FusedArgs f;
+      f.scratch = h->ring;
+      f.rscratch = nullptr;
+      f.slot_groups = 0;
+      f.state = h->state;
+      f.spin_limit_ns = h->spin_limit_ns;
+      f.skip_producer = h->skip_producer;
+      f.ring_depth = h->ring_depth;
+      f.progress = h->progress;
+      f.opts = h->fused_opts;
+      h->skip_producer = -1;
+      e = ar::launch_fused_ll8_ring(h->R, a, f, cfg, s);
+      break;
+    }
     case AR_FUSED_LL8:
     case AR_FUSED_LL8_STAGED:
     case AR_PACKET_3OP: {
@@ -265,6 +303,9 @@ ar_status_t launch(ar_ctx* h, int variant, const TuneRow* row, const void* const
       f.state = h->state;
       f.spin_limit_ns = h->spin_limit_ns;
       f.skip_producer = h->skip_producer;
+      f.ring_depth = h->ring_depth;
+      f.progress = h->progress;
+      f.opts = h->fused_opts;
       h->skip_producer = -1;
       e = variant == AR_FUSED_LL8          ? ar::launch_fused_ll8(h->R, a, f, cfg, s)
           : variant == AR_FUSED_LL8_STAGED ? ar::launch_fused_ll8_staged(h->R, a, f, cfg, s)
@@ -303,6 +344,7 @@ const char* ar_variant_name(int variant) {
     case AR_ONESHOT_FANOUT_BULK: return "oneshot_fanout_bulk";
     case AR_FUSED_LL8_STAGED: return "fused_ll8_staged";
     case AR_PACKET_3OP: return "packet_3op";
+    case AR_FUSED_LL8_RING: return "fused_ll8_ring";
     default: return "?";
   }
 }
@@ -346,9 +388,23 @@ ar_status_t ar_create(int R, size_t max_count, int dtype, ar_handle_t* out) {
   h->log = env && env[0] == '1';
 
   const size_t groups = ceil_div(max_count, (size_t)ar::kVecElems);
-  h->slot_groups = ceil_div(groups, (size_t)R);
+  // Rounded up to 4 groups so that every slot starts on a 128-byte line.
+  h->slot_groups = (ceil_div(groups, (size_t)R) + 3) / 4 * 4;
   h->scratch_bytes = (size_t)R * (size_t)(R - 1) * h->slot_groups * 4 * sizeof(uint64_t);
   h->fused_ctas_per_sm = occupancy(h, AR_FUSED_LL8, h->fused_threads);
+  env = getenv("AR_FUSED_OPTS");
+  if (env && *env) h->fused_opts = (uint32_t)strtoul(env, nullptr, 0) & 3u;
+  env = getenv("AR_RING_DEPTH");
+  if (env && *env) {
+    const long d = strtol(env, nullptr, 10);
+    if (d >= 2 && d <= ar::kMaxRingDepth) h->ring_depth = (int)d;
+  }
+  for (int t = 128; t <= 512; t *= 2) {
+    const size_t per_rank = std::min<size_t>(
+        (size_t)occupancy(h, AR_FUSED_LL8_RING, t) * (size_t)sms / (size_t)R, ar::kMaxRingCtas);
+    h->ring_threads = std::max(h->ring_threads, per_rank * (size_t)t);
+  }
+  h->ring_bytes = (size_t)R * (size_t)(R - 1) * ar::kMaxRingDepth * h->ring_threads * 32;
   if (ar::bulk_prepare(R) == cudaSuccess) h->bulk_ctas_per_sm = ar::bulk_ctas_per_sm(R);
   cudaGetLastError();
 
@@ -365,9 +421,16 @@ ar_status_t ar_create(int R, size_t max_count, int dtype, ar_handle_t* out) {
     if (cudaMemcpy(h->state, &init, sizeof init, cudaMemcpyHostToDevice) != cudaSuccess)
       st = AR_ERR_CUDA;
   }
+  const size_t progress_bytes = (size_t)R * ar::kMaxRingCtas * sizeof(uint32_t);
+  if (st == AR_OK && cudaMalloc(&h->progress, progress_bytes) != cudaSuccess) st = AR_ERR_OOM;
+  if (st == AR_OK && h->ring_bytes && cudaMalloc(&h->ring, h->ring_bytes) != cudaSuccess)
+    st = AR_ERR_OOM;
   if (st == AR_OK && h->scratch_bytes &&
       (cudaMemset(h->scratch, 0, h->scratch_bytes) != cudaSuccess ||
        cudaMemset(h->rscratch, 0, h->scratch_bytes) != cudaSuccess))
+    st = AR_ERR_CUDA;
+  if (st == AR_OK && (cudaMemset(h->progress, 0, progress_bytes) != cudaSuccess ||
+                      (h->ring_bytes && cudaMemset(h->ring, 0, h->ring_bytes) != cudaSuccess)))
     st = AR_ERR_CUDA;
   if (st == AR_OK && cudaDeviceSynchronize() != cudaSuccess) st = AR_ERR_CUDA;
   if (st != AR_OK) {
@@ -388,9 +451,12 @@ ar_status_t ar_destroy(ar_handle_t h) {
   if (cudaDeviceSynchronize() != cudaSuccess) st = AR_ERR_CUDA;
   if (h->scratch && cudaFree(h->scratch) != cudaSuccess) st = AR_ERR_CUDA;
   if (h->rscratch && cudaFree(h->rscratch) != cudaSuccess) st = AR_ERR_CUDA;
+  if (h->ring && cudaFree(h->ring) != cudaSuccess) st = AR_ERR_CUDA;
+  if (h->progress && cudaFree(h->progress) != cudaSuccess) st = AR_ERR_CUDA;
   if (h->state && cudaFree(h->state) != cudaSuccess) st = AR_ERR_CUDA;
   if (h->staging && cudaFree(h->staging) != cudaSuccess) st = AR_ERR_CUDA;
   if (h->staging_tables && cudaFree(h->staging_tables) != cudaSuccess) st = AR_ERR_CUDA;
+  if (h->direct_tables && cudaFree(h->direct_tables) != cudaSuccess) st = AR_ERR_CUDA;
   if (prev >= 0 && prev != h->device) cudaSetDevice(prev);
   delete h;
   return st;
@@ -431,7 +497,7 @@ ar_status_t ar_query(ar_handle_t h, ar_info_t* info) {
   info->R = h->R;
   info->dtype = AR_BF16;
   info->max_count = h->max_count;
-  info->scratch_bytes = 2 * h->scratch_bytes;
+  info->scratch_bytes = 2 * h->scratch_bytes + h->ring_bytes;
   info->num_sms = h->num_sms;
   info->fused_max_ctas = h->fused_ctas_per_sm * h->num_sms;
   info->fused_threads = h->fused_threads;
@@ -522,11 +588,14 @@ ar_status_t ar_reserve_host_staging(ar_handle_t h) {
     h->staging = nullptr;
     return AR_ERR_OOM;
   }
-  if (cudaMalloc(&h->staging_tables, 2 * (size_t)h->R * sizeof(uint16_t*)) != cudaSuccess) {
+  if (cudaMalloc(&h->staging_tables, 2 * (size_t)h->R * sizeof(uint16_t*)) != cudaSuccess ||
+      cudaMalloc(&h->direct_tables, 2 * (size_t)h->R * sizeof(uint16_t*)) != cudaSuccess) {
     cudaGetLastError();
     cudaFree(h->staging);
+    if (h->staging_tables) cudaFree(h->staging_tables);
     h->staging = nullptr;
     h->staging_tables = nullptr;
+    h->direct_tables = nullptr;
     return AR_ERR_OOM;
   }
   std::vector<uint16_t*> ptrs(2 * (size_t)h->R);
@@ -545,10 +614,47 @@ ar_status_t ar_allreduce_host(ar_handle_t h, const void* const* h_in, void* cons
   ar_status_t st = check_device(h);
   if (st != AR_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  for (int r = 0; r < h->R; ++r)
+    if (!h_in[r] || !h_out[r]) return AR_ERR_INVALID_ARG;
+
+  // Direct path: page-locked host buffers (and device buffers) are
+  // addressable by the kernels through unified addressing -- over
+  // NVLink-C2C on Grace-Blackwell -- so the kernel itself reads every input
+  // byte from the host once and writes every output byte to the host once,
+  // both directions at the same time.  The pointer table goes to the device
+  // in stream order (copied out of this stack array before the call returns).
+  void* direct[2 * AR_MAX_RANKS];
+  // The bulk-copy variant keeps to device memory (staging path).
+  bool ok_direct = h->variant != AR_ONESHOT_FANOUT_BULK;
+  for (int i = 0; i < 2 * h->R && ok_direct; ++i) {
+    const void* p = i < h->R ? h_in[i] : h_out[i - h->R];
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+      cudaGetLastError();
+      ok_direct = false;
+    } else if ((at.type == cudaMemoryTypeHost || at.type == cudaMemoryTypeDevice ||
+                at.type == cudaMemoryTypeManaged) &&
+               at.devicePointer != nullptr) {
+      direct[i] = at.devicePointer;
+    } else {
+      ok_direct = false;
+    }
+  }
+  if (ok_direct) {
+    if (cudaMemcpyAsync(h->direct_tables, direct, 2 * (size_t)h->R * sizeof(void*),
+                        cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return AR_ERR_CUDA;
+    // The fan-out reads and writes each byte exactly once: the selector's
+    // choice for host memory unless a variant is forced.
+    const int v = h->variant != AR_AUTO ? h->variant : AR_ONESHOT_FANOUT;
+    return launch(h, v, nullptr, reinterpret_cast<const void* const*>(h->direct_tables),
+                  reinterpret_cast<void* const*>(h->direct_tables + h->R), count, s);
+  }
+
+  // Staging path (pageable host memory): one copy per rank each way.
   const size_t per_rank = (h->max_count + 127) / 128 * 128;
   const size_t bytes = count * sizeof(uint16_t);
   for (int r = 0; r < h->R; ++r) {
-    if (!h_in[r] || !h_out[r]) return AR_ERR_INVALID_ARG;
     if (cudaMemcpyAsync(h->staging + (size_t)r * per_rank, h_in[r], bytes, cudaMemcpyHostToDevice,
                         s) != cudaSuccess)
       return AR_ERR_CUDA;
@@ -575,6 +681,15 @@ ar_status_t ar_debug_skip_producer(ar_handle_t h, int rank) {
 ar_status_t ar_debug_set_epoch(ar_handle_t h, uint32_t epoch) {
   if (!h || epoch == 0) return AR_ERR_INVALID_ARG;
   if (cudaDeviceSynchronize() != cudaSuccess) return AR_ERR_CUDA;
+  // A jump of the epoch invalidates the "older flag = not arrived" ordering
+  // for everything written before it: clear every packet and credit.
+  if ((h->scratch_bytes && (cudaMemset(h->scratch, 0, h->scratch_bytes) != cudaSuccess ||
+                            cudaMemset(h->rscratch, 0, h->scratch_bytes) != cudaSuccess)) ||
+      (h->ring_bytes && cudaMemset(h->ring, 0, h->ring_bytes) != cudaSuccess) ||
+      cudaMemset(h->progress, 0, (size_t)h->R * ar::kMaxRingCtas * sizeof(uint32_t)) !=
+          cudaSuccess ||
+      cudaDeviceSynchronize() != cudaSuccess)
+    return AR_ERR_CUDA;
   return cuda_status(cudaMemcpy(&h->state->epoch, &epoch, sizeof epoch, cudaMemcpyHostToDevice));
 }
 

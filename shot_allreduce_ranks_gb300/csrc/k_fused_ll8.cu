@@ -158,18 +158,18 @@ __device__ __forceinline__ Lane packet_prologue(const CallArgs& a, const FusedAr
 }
 
 // Waits until every packet set s in `pending` (already loaded once into
-// pk[s]) carries the epoch, re-polling slot_ptr(region, a_idx, s) + j * 4.
-// Bounded: after spin_limit_ns of %globaltimer (or an iteration cap, a
-// backstop in case the timer did not advance; every iteration is at least
-// one L2 round trip) it records a timeout and returns false; it also
-// returns false as soon as another waiter of this call has given up.
-template <int R>
-__device__ __forceinline__ bool wait_packets(const FusedArgs& f, uint64_t* region, int a_idx,
-                                             size_t j, Packets4 (&pk)[R], uint32_t pending,
-                                             uint32_t epoch) {
+// pk[s]) carries `flag`, re-polling ptr(s).  Bounded: after spin_limit_ns of
+// %globaltimer (or an iteration cap, a backstop in case the timer did not
+// advance; every iteration is at least one L2 round trip) it records a
+// timeout and returns false; it also returns false as soon as another
+// waiter of the same call (identified by its base epoch) has given up.
+template <int R, class Ptr>
+__device__ __forceinline__ bool wait_packets_at(const FusedArgs& f, Packets4 (&pk)[R],
+                                                uint32_t pending, uint32_t flag,
+                                                uint32_t call_epoch, int who, Ptr ptr) {
 #pragma unroll
   for (int s = 0; s < R; ++s)
-    if ((pending & (1u << s)) && pk[s].arrived(epoch)) pending &= ~(1u << s);
+    if ((pending & (1u << s)) && pk[s].arrived(flag)) pending &= ~(1u << s);
   if (!pending) return true;
   uint64_t t_first = 0;
   uint32_t spins = 0;
@@ -178,21 +178,31 @@ __device__ __forceinline__ bool wait_packets(const FusedArgs& f, uint64_t* regio
 #pragma unroll
     for (int s = 0; s < R; ++s) {
       if (pending & (1u << s)) {
-        pk[s].load(slot_ptr<R>(region, f.slot_groups, a_idx, s) + j * 4);
-        if (pk[s].arrived(epoch)) pending &= ~(1u << s);
+        pk[s].load(ptr(s));
+        if (pk[s].arrived(flag)) pending &= ~(1u << s);
       }
     }
     if (pending && (++spins & 15u) == 0) {
       const uint64_t now = global_timer_ns();
       if (spins == 16u) t_first = now;
       if (spins > kMaxSpins || (spins > 16u && now - t_first > f.spin_limit_ns)) {
-        report_timeout(f, a_idx, pending, epoch);
+        report_timeout(f, who, pending, call_epoch);
         return false;
       }
-      if (ld_relaxed_u32(&f.state->abort_epoch) == epoch) return false;
+      if (ld_relaxed_u32(&f.state->abort_epoch) == call_epoch) return false;
     }
   }
   return true;
+}
+
+// The same wait on a region laid out like the scatter scratch.
+template <int R>
+__device__ __forceinline__ bool wait_packets(const FusedArgs& f, uint64_t* region, int a_idx,
+                                             size_t j, Packets4 (&pk)[R], uint32_t pending,
+                                             uint32_t epoch) {
+  return wait_packets_at<R>(f, pk, pending, epoch, epoch, a_idx, [&](int s) {
+    return slot_ptr<R>(region, f.slot_groups, a_idx, s) + j * 4;
+  });
 }
 
 // ---- scatter: rank r's slices of every other owner's shard, as packets ----
@@ -201,7 +211,8 @@ __device__ __forceinline__ bool wait_packets(const FusedArgs& f, uint64_t* regio
 template <int R>
 __device__ __forceinline__ void phase_scatter(const CallArgs& a, const FusedArgs& f, const Lane& l,
                                               const uint16_t* my_in) {
-  if (R == 1 || l.r == f.skip_producer) return;
+  if constexpr (R == 1) return;
+  if (l.r == f.skip_producer) return;
   for (size_t j = l.t0; j < l.Vs; j += 2 * l.tstride) {
     const size_t j2 = j + l.tstride;
     uint4 x[R > 1 ? R - 1 : 1], y[R > 1 ? R - 1 : 1];
@@ -233,11 +244,19 @@ __device__ __forceinline__ void phase_scatter(const CallArgs& a, const FusedArgs
 // group into all R outputs.  Otherwise: store it into out_r only and send it
 // as result packets to every other rank's result slot for owner r.
 // Returns false if the call was abandoned after a timeout.
+__device__ __forceinline__ void discard_l2_line(const void* p) {
+  asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
 template <int R, bool kWriteMode>
 __device__ __forceinline__ bool phase_reduce(const CallArgs& a, const FusedArgs& f, const Lane& l,
                                              const uint16_t* my_in, uint16_t* const* s_out) {
   const size_t g0 = (size_t)l.r * l.Vs;
   const size_t n = g0 < a.groups ? min(l.Vs, a.groups - g0) : 0;
+  const bool stream_out = kWriteMode && (f.opts & kFusedOptStreamOutputs);
+  const bool discard = kWriteMode && (f.opts & kFusedOptDiscardPackets);
+  const uint64_t pol_out = l2_policy_evict_first();
+  const int lane = (int)(threadIdx.x & 31u);
   for (size_t j = l.t0; j < n; j += l.tstride) {
     const size_t g = g0 + j;
     const int valid = group_valid(g, a.count);
@@ -250,15 +269,36 @@ __device__ __forceinline__ bool phase_reduce(const CallArgs& a, const FusedArgs&
         pk[s].load(slot_ptr<R>(f.scratch, f.slot_groups, l.r, s) + j * 4);
         pending |= 1u << s;
       }
-    if (!wait_packets<R>(f, f.scratch, l.r, j, pk, pending, l.epoch)) return false;
+    const bool ok = wait_packets<R>(f, f.scratch, l.r, j, pk, pending, l.epoch);
+    if (discard) {
+      // The warp's lanes hold consecutive groups j (the warp's first group
+      // is a multiple of 32), so lanes 4m..4m+3 share one 128-byte line per
+      // source slot.  Every lane of the warp that entered this iteration
+      // meets here; a line is dropped only once all its lanes have read it.
+      const size_t wbase = j - (size_t)lane;
+      const unsigned mask = n - wbase >= 32 ? 0xFFFFFFFFu : ((1u << (n - wbase)) - 1u);
+      const unsigned oks = __ballot_sync(mask, ok);
+      const unsigned quad = 0xFu << (lane & ~3);
+      if ((lane & 3) == 0 && (oks & quad) == (mask & quad)) {
+#pragma unroll
+        for (int s = 0; s < R; ++s)
+          if (s != l.r) discard_l2_line(slot_ptr<R>(f.scratch, f.slot_groups, l.r, s) + j * 4);
+      }
+    }
+    if (!ok) return false;
     Acc8 acc;
     acc.set(l.r == 0 ? own : pk[0].data());
 #pragma unroll
     for (int s = 1; s < R; ++s) acc.add(s == l.r ? own : pk[s].data());
     const uint4 y = acc.round_bf16();
     if (kWriteMode) {
+      if (stream_out) {
 #pragma unroll
-      for (int q = 0; q < R; ++q) store_group(s_out[q], g, y, valid, l.vec);
+        for (int q = 0; q < R; ++q) store_group<true>(s_out[q], g, y, valid, l.vec, pol_out);
+      } else {
+#pragma unroll
+        for (int q = 0; q < R; ++q) store_group(s_out[q], g, y, valid, l.vec);
+      }
     } else {
       store_group(s_out[l.r], g, y, valid, l.vec);
 #pragma unroll
@@ -274,7 +314,7 @@ __device__ __forceinline__ bool phase_reduce(const CallArgs& a, const FusedArgs&
 template <int R>
 __device__ __forceinline__ bool phase_recv(const CallArgs& a, const FusedArgs& f, const Lane& l,
                                            uint16_t* const* s_out) {
-  if (R == 1) return true;
+  if constexpr (R == 1) return true;
   uint16_t* my_out = s_out[l.r];
   for (size_t j = l.t0; j < l.Vs; j += l.tstride) {
     Packets4 pk[R];
@@ -299,7 +339,7 @@ __device__ __forceinline__ bool phase_recv(const CallArgs& a, const FusedArgs& f
 
 // ---- flag rotation: the last CTA of the call's last kernel advances the
 // epoch (skipping 0) and resets the done counter ------------------------------
-__device__ __forceinline__ void epoch_advance(const FusedArgs& f, uint32_t epoch) {
+__device__ __forceinline__ void epoch_advance_to(const FusedArgs& f, uint32_t next) {
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
@@ -307,11 +347,22 @@ __device__ __forceinline__ void epoch_advance(const FusedArgs& f, uint32_t epoch
     if (prev == gridDim.x - 1) {
       __threadfence();
       st_relaxed_u32(&f.state->done, 0u);
-      uint32_t next = epoch + 1u;
-      if (next == 0u) next = 1u;
       st_relaxed_u32(&f.state->epoch, next);
     }
   }
+}
+
+// The epoch sequence skips 0 (the value of zeroed scratch): the k-th value
+// after e, and the number of steps from b forward to a.
+__device__ __forceinline__ uint32_t flag_at(uint32_t e, uint64_t k) {
+  return (uint32_t)(((uint64_t)e - 1u + k) % 0xFFFFFFFFull + 1u);
+}
+__device__ __forceinline__ uint64_t flag_dist(uint32_t a, uint32_t b) {
+  return ((uint64_t)a + 0xFFFFFFFFull - b) % 0xFFFFFFFFull;
+}
+
+__device__ __forceinline__ void epoch_advance(const FusedArgs& f, uint32_t epoch) {
+  epoch_advance_to(f, flag_at(epoch, 1));
 }
 
 // Write mode: scatter -> reduce -> broadcast straight into all R outputs.
@@ -365,7 +416,209 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_packet_recv(CallArgs a, Fu
   epoch_advance(f, l.epoch);
 }
 
+// ---------------------------------------------------------------------------
+// Ring variant of the write-mode kernel.
+//
+// The scratch above holds every packet of a call (about 4(R-1)N bytes), so
+// on a large call its dirty lines leave L2 and are written back to HBM after
+// being read once.  Here each (owner, source, CTA) pair owns a ring of D
+// round slots of T groups; round k of CTA c covers groups
+// j = k*C*T + c*T + t of every shard and uses ring slot k mod D, so the
+// packet footprint is R(R-1)*C*D*T*32 bytes whatever the message size, and
+// L2 keeps rewriting the same lines.
+//
+//   * Flags: round k of a call with epoch e carries flag_at(e, k); the call
+//     moves the epoch on by its number of rounds K, so a slot's previous
+//     contents (an earlier round or call) never carry the flag expected now.
+//   * Credits: owner CTA (o, c) publishes, with a release store,
+//     progress[o][c] = flag of the last round it finished reading; before
+//     producer CTA (s, c) overwrites slot k mod D it waits (acquire) until
+//     every other owner's progress has reached round k - D.
+//   * Schedule of CTA c, iteration k = 0..K: [credits for round k] ->
+//     scatter round k -> reduce round k-1 -> barrier -> publish round k-1.
+//     With D >= 2 and a co-resident grid this cannot deadlock: by induction
+//     on k, iteration k needs only iterations <= k-1 of the other CTAs.
+//   * Every wait is bounded like the others; a timeout abandons the call.
+template <int R>
+__device__ __forceinline__ uint64_t* ring_slot(const FusedArgs& f, int o, int s, int c, int C,
+                                               int p, int tid, int T) {
+  const int pair = o * (R - 1) + (s < o ? s : s - 1);
+  const size_t idx = (((size_t)pair * C + c) * f.ring_depth + p) * T + tid;
+  return f.scratch + idx * 4;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Bounded wait (one thread) until progress word *pp has reached `target`.
+__device__ __noinline__ bool wait_credit(const FusedArgs& f, const uint32_t* pp, uint32_t& pv,
+                                         uint32_t target, int who, uint32_t call_epoch) {
+  uint64_t t_first = 0;
+  uint32_t spins = 0;
+  // 0 is never a flag (zeroed memory): not yet published.
+  while (pv == 0u || flag_dist(pv, target) >= 0x80000000ull) {
+    __nanosleep(64);
+    pv = ld_acquire_u32(pp);
+    if ((++spins & 15u) == 0) {
+      const uint64_t now = global_timer_ns();
+      if (spins == 16u) t_first = now;
+      if (spins > kMaxSpins || (spins > 16u && now - t_first > f.spin_limit_ns)) {
+        report_timeout(f, who, 0u, call_epoch);
+        return false;
+      }
+      if (ld_relaxed_u32(&f.state->abort_epoch) == call_epoch) return false;
+    }
+  }
+  return true;
+}
+
+template <int R>
+__global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8_ring(CallArgs a, FusedArgs f) {
+  __shared__ const uint16_t* s_in[R];
+  __shared__ uint16_t* s_out[R];
+  __shared__ int s_abort;
+  const Lane l = packet_prologue<R>(a, f, s_in, s_out);
+  if (threadIdx.x == 0) s_abort = 0;
+  const int T = blockDim.x, tid = threadIdx.x;
+  const int C = (int)(gridDim.x / R), c = (int)(blockIdx.x / R), r = l.r;
+  const int D = f.ring_depth;
+  const size_t Vs = l.Vs;
+  const size_t per_round = (size_t)C * T;
+  const size_t K = (Vs + per_round - 1) / per_round;  // rounds of this call
+  const uint16_t* my_in = s_in[r];
+  const size_t g0 = (size_t)r * Vs;  // first group of my shard
+  const size_t my_n = g0 < a.groups ? min(Vs, a.groups - g0) : 0;
+  // Threads 0..R-2 each watch one other owner's progress (credits).
+  const int watch = (R > 1 && tid < R - 1) ? (r + 1 + tid) % R : -1;
+  uint32_t* const my_progress = f.progress + (size_t)r * kMaxRingCtas + c;
+  const uint32_t* const watched =
+      watch >= 0 ? f.progress + (size_t)watch * kMaxRingCtas + c : nullptr;
+  uint32_t pv = watch >= 0 ? ld_acquire_u32(watched) : 0u;
+  __syncthreads();
+
+  for (size_t k = 0; k <= K; ++k) {
+    // ---- credits for round k: every other owner has read round k - D ----
+    if (R > 1 && k < K && k >= (size_t)D) {
+      if (watch >= 0 && !wait_credit(f, watched, pv, flag_at(l.epoch, k - D), r, l.epoch))
+        s_abort = 1;
+      __syncthreads();
+      if (s_abort) break;
+    }
+    const size_t jk = k * per_round + (size_t)c * T + tid;  // my group of round k
+    // ---- issue: input loads of round k, packet loads of round k-1 ----------
+    uint4 x[R > 1 ? R - 1 : 1];
+    const bool scatter = R > 1 && k < K && jk < Vs && r != f.skip_producer;
+    if (scatter) {
+#pragma unroll
+      for (int q = 1; q < R; ++q) {
+        const int o = (r + q) % R;
+        const size_t g = (size_t)o * Vs + jk;
+        if (g < a.groups) x[q - 1] = load_group<true>(my_in, g, group_valid(g, a.count), l.vec, l.pol_in);
+      }
+    }
+    const size_t jp = jk - per_round;  // my group of round k-1 (valid when k >= 1)
+    const bool reduce = k >= 1 && jp < my_n;
+    const int pp = (int)((k + D - 1) % D);  // ring slot of round k-1
+    Packets4 pk[R];
+    uint4 own = make_uint4(0, 0, 0, 0);
+    uint32_t pending = 0;
+    if (reduce) {
+      own = load_group<true>(my_in, g0 + jp, group_valid(g0 + jp, a.count), l.vec, l.pol_in);
+#pragma unroll
+      for (int s = 0; s < R; ++s)
+        if (s != r) {
+          pk[s].load(ring_slot<R>(f, r, s, c, C, pp, tid, T));
+          pending |= 1u << s;
+        }
+    }
+    // ---- scatter round k ----------------------------------------------------
+    if (scatter) {
+      const uint32_t flag = flag_at(l.epoch, k);
+      const int p = (int)(k % D);
+#pragma unroll
+      for (int q = 1; q < R; ++q) {
+        const int o = (r + q) % R;
+        if ((size_t)o * Vs + jk < a.groups)
+          st_packets(ring_slot<R>(f, o, r, c, C, p, tid, T), x[q - 1], flag);
+      }
+    }
+    // ---- reduce round k-1 + write-mode broadcast ----------------------------
+    if (reduce) {
+      const uint32_t flag = flag_at(l.epoch, k - 1);
+      const bool ok = wait_packets_at<R>(f, pk, pending, flag, l.epoch, r, [&](int s) {
+        return ring_slot<R>(f, r, s, c, C, pp, tid, T);
+      });
+      if (ok) {
+        Acc8 acc;
+        acc.set(r == 0 ? own : pk[0].data());
+#pragma unroll
+        for (int s = 1; s < R; ++s) acc.add(s == r ? own : pk[s].data());
+        const uint4 y = acc.round_bf16();
+        const size_t g = g0 + jp;
+        const int valid = group_valid(g, a.count);
+        if (f.opts & kFusedOptStreamOutputs) {
+          const uint64_t pol_out = l2_policy_evict_first();
+#pragma unroll
+          for (int q = 0; q < R; ++q) store_group<true>(s_out[q], g, y, valid, l.vec, pol_out);
+        } else {
+#pragma unroll
+          for (int q = 0; q < R; ++q) store_group(s_out[q], g, y, valid, l.vec);
+        }
+      } else {
+        s_abort = 1;
+      }
+    }
+    __syncthreads();  // every thread is done reading ring slot pp
+    if (s_abort) break;
+    if (k >= 1 && tid == 0) st_release_u32(my_progress, flag_at(l.epoch, k - 1));
+  }
+  epoch_advance_to(f, flag_at(l.epoch, K));
+}
+
 }  // namespace
+
+int fused_ring_ctas_per_sm(int R, int threads) {
+  int n = 0;
+  cudaError_t e = cudaErrorInvalidValue;
+#define Q(RR) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_fused_ll8_ring<RR>, threads, 0)
+  switch (R) {
+    case 1: Q(1); break;
+    case 2: Q(2); break;
+    case 3: Q(3); break;
+    case 4: Q(4); break;
+    case 5: Q(5); break;
+    case 6: Q(6); break;
+    case 7: Q(7); break;
+    case 8: Q(8); break;
+    default: return 0;
+  }
+#undef Q
+  return e == cudaSuccess ? n : 0;
+}
+
+cudaError_t launch_fused_ll8_ring(int R, const CallArgs& a, const FusedArgs& f, LaunchCfg cfg,
+                                  cudaStream_t s) {
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3((unsigned)cfg.ctas);
+  lc.blockDim = dim3((unsigned)cfg.threads);
+  lc.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+#define L(RR) return cudaLaunchKernelEx(&lc, k_fused_ll8_ring<RR>, a, f)
+  AR_RANK_SWITCH(R, L)
+#undef L
+  return cudaErrorInvalidValue;
+}
 
 int fused_ctas_per_sm(int R, int threads) {
   int n = 0;
@@ -546,6 +799,9 @@ extern "C" ar_status_t ar_allreduce_fused_noalloc(int R, const void* const* d_in
   f.state = d.state;
   f.spin_limit_ns = 100ull * 1000ull * 1000ull;
   f.skip_producer = -1;
+  f.ring_depth = 0;
+  f.progress = nullptr;
+  f.opts = 0;
   const size_t limit = (size_t)d.ctas_per_sm[R] * (size_t)d.sms / (size_t)R;
   size_t per_rank = (a.shard_groups + kNoAllocThreads - 1) / kNoAllocThreads;
   per_rank = std::max<size_t>(1, std::min(per_rank, limit));

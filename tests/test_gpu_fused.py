@@ -22,6 +22,9 @@ def ar():
     G.release_handles()
 
 
+PACKET_VARIANTS = ["fused_ll8", "fused_ll8_staged", "packet_3op", "fused_ll8_ring"]
+
+
 def _bufs(xs):
     bufs = G.to_device(xs)
     return bufs, [torch.empty_like(b) for b in bufs]
@@ -37,7 +40,11 @@ def test_epoch_advances_once_per_call(ar):
     G.check_all_outputs(outs, G.oracle_expect(xs), "after 5 calls")
 
 
-def test_epoch_wraps_to_one_skipping_zero(ar):
+@pytest.mark.parametrize("variant", ["fused_ll8", "fused_ll8_ring", "packet_3op"])
+def test_epoch_wraps_to_one_skipping_zero(ar, variant):
+    """One call moves the epoch by one step here (the ring kernel moves it by
+    its number of rounds, which is 1 at this size)."""
+    ar.set_variant(variant)
     xs = inputs.make_inputs(R, COUNT, 2)
     want = G.oracle_expect(xs)
     bufs, outs = _bufs(xs)
@@ -51,9 +58,7 @@ def test_epoch_wraps_to_one_skipping_zero(ar):
     ar(bufs, outs)
     assert ar.debug_get_epoch() == 2
     G.check_all_outputs(outs, want, "epoch 1 after wrap")
-
-
-PACKET_VARIANTS = ["fused_ll8", "fused_ll8_staged", "packet_3op"]
+    ar.set_variant("fused_ll8")
 
 
 @pytest.mark.parametrize("variant", PACKET_VARIANTS)
@@ -140,3 +145,31 @@ def test_graph_replay_with_changing_inputs(ar):
         G.check_all_outputs(outs, G.oracle_expect(xs), "replay %d" % rep)
     assert ar.debug_get_epoch() == e0 + 6
     assert ar.device_status() == AR_OK
+
+
+@pytest.mark.parametrize("depth_calls", [(0, 2), (3 * R, 5)])
+def test_ring_many_rounds(depth_calls):
+    """The ring kernel over many rounds (a small grid forces K >> D), so that
+    every ring slot is reused and every credit wait is exercised; several
+    calls in a row with changing inputs."""
+    ctas, calls = depth_calls
+    h = G.handle(R, 3 * 65536 * 8 + 5)
+    h.set_variant("fused_ll8_ring")
+    h.set_launch("fused_ll8_ring", ctas if ctas else R, 128)
+    count = 3 * 65536 * 8 + 5
+    bufs = [torch.empty(count, dtype=torch.bfloat16, device=G.DEV) for _ in range(R)]
+    outs = [torch.empty_like(b) for b in bufs]
+    in_tbl, out_tbl = h.tables(bufs, outs)
+    snaps, wants = [], []
+    for call in range(calls):
+        xs = inputs.make_inputs(R, count, seed=200 + call)
+        wants.append(G.oracle_expect(xs))
+        for b, x in zip(bufs, xs):
+            b.copy_(x)
+        h.allreduce_tables(in_tbl, out_tbl, count)
+        snaps.append([o.clone() for o in outs])
+    torch.cuda.synchronize()
+    assert h.device_status() == AR_OK
+    for call, (snap, want) in enumerate(zip(snaps, wants)):
+        G.check_all_outputs(snap, want, "ring call %d" % call)
+    h.set_launch("fused_ll8_ring", 0, 0)

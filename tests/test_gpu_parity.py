@@ -241,6 +241,22 @@ def test_selector_picks_a_real_variant_and_matches():
         G.check_all_outputs(outs, G.oracle_expect(xs), "auto count=%d" % count)
 
 
+def test_host_buffer_path_pageable():
+    """Pageable host buffers take the staging-copy path."""
+    R, count = 8, 50_003
+    ar = G.handle(R, count)
+    ar.reserve_host_staging()
+    xs = inputs.make_inputs(R, count, seed=16)
+    want = G.oracle_expect(xs)
+    hout = [torch.empty(count, dtype=torch.bfloat16) for _ in range(R)]
+    for variant in ("auto", "fused_ll8", "oneshot_fanout"):
+        ar.set_variant(variant)
+        ar.allreduce_host(xs, hout)
+        torch.cuda.synchronize()
+        for r in range(R):
+            G.assert_bitexact(inputs.bits(hout[r]), want, "pageable %s rank %d" % (variant, r))
+
+
 def test_host_buffer_path():
     R, count = 8, 123_457
     ar = G.handle(R, count)
@@ -249,7 +265,7 @@ def test_host_buffer_path():
     want = G.oracle_expect(xs)
     hin = [x.pin_memory() for x in xs]
     hout = [torch.empty(count, dtype=torch.bfloat16).pin_memory() for _ in range(R)]
-    for variant in G.PARITY_VARIANTS:
+    for variant in G.PARITY_VARIANTS + ["auto"]:
         ar.set_variant(variant)
         ar.allreduce_host(hin, hout)
         torch.cuda.synchronize()
