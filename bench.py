@@ -451,7 +451,18 @@ def run_ours(args):
     t_e2e = max_over_ranks(t_e2e, dev)
     e2e = {"value": round(whole_job_us_per_call(t_e2e, e2e_steps, world), 3), "unit": "us/call",
            "h2d_bytes_per_step": 2 * R * N, "d2h_bytes_per_step": 2 * R * N,
-           "steps": e2e_steps, "api": "ar_allreduce_host"}
+           "steps": e2e_steps,
+           "api": "ar_allreduce_host, page-locked host buffers read and written in place "
+                  "by the %s kernel over NVLink-C2C" % args.variant}
+    if not args.no_extra:
+        ar.set_variant("auto")
+        t_auto = time_e2e(ar, R, N, e2e_steps, 3, stream, host_in, host_out)
+        extra["e2e_auto_us_per_call"] = round(t_auto * 1e6 / e2e_steps, 3)
+        pageable_in = [x.clone() for x in xs0]
+        pageable_out = [torch.empty(N, dtype=torch.bfloat16) for _ in range(R)]
+        ar.set_variant(args.variant)
+        t_pg = time_e2e(ar, R, N, min(e2e_steps, 50), 3, stream, pageable_in, pageable_out)
+        extra["e2e_pageable_staging_us_per_call"] = round(t_pg * 1e6 / min(e2e_steps, 50), 3)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -63,9 +63,8 @@ struct ar_ctx {
   uint64_t* ring = nullptr;      // ring variant's packets
   size_t ring_bytes = 0;
   size_t ring_threads = 0;       // threads per rank the ring can hold (C * T)
-  uint32_t* progress = nullptr;  // ring variant's progress words [R][kMaxRingCtas]
+  uint32_t* progress = nullptr;  // ring variant's progress words [R][kMaxRingCtas][kMaxRingWarps]
   int ring_depth = 2;
-  uint32_t fused_opts = 0;       // kFusedOpt* bits for the write-mode fused kernels
   size_t slot_groups = 0;
   uint64_t spin_limit_ns = 100ull * 1000ull * 1000ull;
   int skip_producer = -1;
@@ -288,7 +287,6 @@ ar_status_t launch(ar_ctx* h, int variant, const TuneRow* row, const void* const
       f.skip_producer = h->skip_producer;
       f.ring_depth = h->ring_depth;
       f.progress = h->progress;
-      f.opts = h->fused_opts;
       h->skip_producer = -1;
       e = ar::launch_fused_ll8_ring(h->R, a, f, cfg, s);
       break;
@@ -305,7 +303,6 @@ ar_status_t launch(ar_ctx* h, int variant, const TuneRow* row, const void* const
       f.skip_producer = h->skip_producer;
       f.ring_depth = h->ring_depth;
       f.progress = h->progress;
-      f.opts = h->fused_opts;
       h->skip_producer = -1;
       e = variant == AR_FUSED_LL8          ? ar::launch_fused_ll8(h->R, a, f, cfg, s)
           : variant == AR_FUSED_LL8_STAGED ? ar::launch_fused_ll8_staged(h->R, a, f, cfg, s)
@@ -392,8 +389,6 @@ ar_status_t ar_create(int R, size_t max_count, int dtype, ar_handle_t* out) {
   h->slot_groups = (ceil_div(groups, (size_t)R) + 3) / 4 * 4;
   h->scratch_bytes = (size_t)R * (size_t)(R - 1) * h->slot_groups * 4 * sizeof(uint64_t);
   h->fused_ctas_per_sm = occupancy(h, AR_FUSED_LL8, h->fused_threads);
-  env = getenv("AR_FUSED_OPTS");
-  if (env && *env) h->fused_opts = (uint32_t)strtoul(env, nullptr, 0) & 3u;
   env = getenv("AR_RING_DEPTH");
   if (env && *env) {
     const long d = strtol(env, nullptr, 10);
@@ -421,7 +416,7 @@ ar_status_t ar_create(int R, size_t max_count, int dtype, ar_handle_t* out) {
     if (cudaMemcpy(h->state, &init, sizeof init, cudaMemcpyHostToDevice) != cudaSuccess)
       st = AR_ERR_CUDA;
   }
-  const size_t progress_bytes = (size_t)R * ar::kMaxRingCtas * sizeof(uint32_t);
+  const size_t progress_bytes = (size_t)R * ar::kRingProgressWords * sizeof(uint32_t);
   if (st == AR_OK && cudaMalloc(&h->progress, progress_bytes) != cudaSuccess) st = AR_ERR_OOM;
   if (st == AR_OK && h->ring_bytes && cudaMalloc(&h->ring, h->ring_bytes) != cudaSuccess)
     st = AR_ERR_OOM;
@@ -686,7 +681,7 @@ ar_status_t ar_debug_set_epoch(ar_handle_t h, uint32_t epoch) {
   if ((h->scratch_bytes && (cudaMemset(h->scratch, 0, h->scratch_bytes) != cudaSuccess ||
                             cudaMemset(h->rscratch, 0, h->scratch_bytes) != cudaSuccess)) ||
       (h->ring_bytes && cudaMemset(h->ring, 0, h->ring_bytes) != cudaSuccess) ||
-      cudaMemset(h->progress, 0, (size_t)h->R * ar::kMaxRingCtas * sizeof(uint32_t)) !=
+      cudaMemset(h->progress, 0, (size_t)h->R * ar::kRingProgressWords * sizeof(uint32_t)) !=
           cudaSuccess ||
       cudaDeviceSynchronize() != cudaSuccess)
     return AR_ERR_CUDA;

@@ -49,25 +49,17 @@ struct FusedArgs {
   uint64_t spin_limit_ns;
   int skip_producer;      // test hook: rank whose packet stores are skipped, or -1
   // Ring variant only: packets live in `scratch` as a ring of ring_depth
-  // rounds per (owner, source, CTA); progress[owner * kMaxRingCtas + c] is
-  // the flag of the last round CTA c of `owner` finished reading.
+  // rounds per (owner, source, CTA); progress[(owner, c, warp)] is the flag
+  // of the last round that warp of CTA c of `owner` finished reading.
   int ring_depth;
   uint32_t* progress;
-  uint32_t opts;          // kFusedOpt* bits
 };
 
-// Options of the write-mode fused kernels.
-//  kFusedOptStreamOutputs: output stores carry an evict-first L2 policy, so
-//    L2 keeps the (reused) packet lines instead of the streamed outputs.
-//  kFusedOptDiscardPackets: once the four groups of a 128-byte packet line
-//    are consumed, the line is dropped from L2 (discard.global.L2) instead
-//    of being written back to HBM; the next call's flag check treats
-//    whatever the line then holds as not yet arrived.
-constexpr uint32_t kFusedOptStreamOutputs = 1u;
-constexpr uint32_t kFusedOptDiscardPackets = 2u;
-
 constexpr int kMaxRingCtas = 1024;  // CTAs per rank the ring progress array can hold
+constexpr int kMaxRingWarps = 16;   // warps per CTA (512 threads)
 constexpr int kMaxRingDepth = 4;
+// Progress words per rank: one per (CTA, warp).
+constexpr size_t kRingProgressWords = (size_t)kMaxRingCtas * kMaxRingWarps;
 
 // ---------------------------------------------------------------------------
 // Small device helpers.

@@ -244,19 +244,11 @@ __device__ __forceinline__ void phase_scatter(const CallArgs& a, const FusedArgs
 // group into all R outputs.  Otherwise: store it into out_r only and send it
 // as result packets to every other rank's result slot for owner r.
 // Returns false if the call was abandoned after a timeout.
-__device__ __forceinline__ void discard_l2_line(const void* p) {
-  asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
-}
-
 template <int R, bool kWriteMode>
 __device__ __forceinline__ bool phase_reduce(const CallArgs& a, const FusedArgs& f, const Lane& l,
                                              const uint16_t* my_in, uint16_t* const* s_out) {
   const size_t g0 = (size_t)l.r * l.Vs;
   const size_t n = g0 < a.groups ? min(l.Vs, a.groups - g0) : 0;
-  const bool stream_out = kWriteMode && (f.opts & kFusedOptStreamOutputs);
-  const bool discard = kWriteMode && (f.opts & kFusedOptDiscardPackets);
-  const uint64_t pol_out = l2_policy_evict_first();
-  const int lane = (int)(threadIdx.x & 31u);
   for (size_t j = l.t0; j < n; j += l.tstride) {
     const size_t g = g0 + j;
     const int valid = group_valid(g, a.count);
@@ -270,21 +262,6 @@ __device__ __forceinline__ bool phase_reduce(const CallArgs& a, const FusedArgs&
         pending |= 1u << s;
       }
     const bool ok = wait_packets<R>(f, f.scratch, l.r, j, pk, pending, l.epoch);
-    if (discard) {
-      // The warp's lanes hold consecutive groups j (the warp's first group
-      // is a multiple of 32), so lanes 4m..4m+3 share one 128-byte line per
-      // source slot.  Every lane of the warp that entered this iteration
-      // meets here; a line is dropped only once all its lanes have read it.
-      const size_t wbase = j - (size_t)lane;
-      const unsigned mask = n - wbase >= 32 ? 0xFFFFFFFFu : ((1u << (n - wbase)) - 1u);
-      const unsigned oks = __ballot_sync(mask, ok);
-      const unsigned quad = 0xFu << (lane & ~3);
-      if ((lane & 3) == 0 && (oks & quad) == (mask & quad)) {
-#pragma unroll
-        for (int s = 0; s < R; ++s)
-          if (s != l.r) discard_l2_line(slot_ptr<R>(f.scratch, f.slot_groups, l.r, s) + j * 4);
-      }
-    }
     if (!ok) return false;
     Acc8 acc;
     acc.set(l.r == 0 ? own : pk[0].data());
@@ -292,13 +269,8 @@ __device__ __forceinline__ bool phase_reduce(const CallArgs& a, const FusedArgs&
     for (int s = 1; s < R; ++s) acc.add(s == l.r ? own : pk[s].data());
     const uint4 y = acc.round_bf16();
     if (kWriteMode) {
-      if (stream_out) {
 #pragma unroll
-        for (int q = 0; q < R; ++q) store_group<true>(s_out[q], g, y, valid, l.vec, pol_out);
-      } else {
-#pragma unroll
-        for (int q = 0; q < R; ++q) store_group(s_out[q], g, y, valid, l.vec);
-      }
+      for (int q = 0; q < R; ++q) store_group(s_out[q], g, y, valid, l.vec);
     } else {
       store_group(s_out[l.r], g, y, valid, l.vec);
 #pragma unroll
@@ -430,15 +402,22 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_packet_recv(CallArgs a, Fu
 //   * Flags: round k of a call with epoch e carries flag_at(e, k); the call
 //     moves the epoch on by its number of rounds K, so a slot's previous
 //     contents (an earlier round or call) never carry the flag expected now.
-//   * Credits: owner CTA (o, c) publishes, with a release store,
-//     progress[o][c] = flag of the last round it finished reading; before
-//     producer CTA (s, c) overwrites slot k mod D it waits (acquire) until
-//     every other owner's progress has reached round k - D.
-//   * Schedule of CTA c, iteration k = 0..K: [credits for round k] ->
-//     scatter round k -> reduce round k-1 -> barrier -> publish round k-1.
+//   * Credits: warp w of owner CTA (o, c) publishes, with a release store
+//     after a warp barrier, progress[o][c][w] = flag of the last round it
+//     finished reading; before warp w of producer CTA (s, c) overwrites slot
+//     k mod D it waits (acquire) until every other owner's warp w has
+//     reached round k - D.  Producer thread t writes only slots that
+//     consumer thread t reads, so warps need no CTA-wide barrier.
+//   * Schedule of every warp, iteration k = 0..K: [credits for round k] ->
+//     scatter round k -> reduce round k-1 -> warp barrier -> publish k-1.
 //     With D >= 2 and a co-resident grid this cannot deadlock: by induction
-//     on k, iteration k needs only iterations <= k-1 of the other CTAs.
+//     on k, iteration k needs only iterations <= k-1 of the other warps.
 //   * Every wait is bounded like the others; a timeout abandons the call.
+// Progress word of (owner, CTA c, warp w).
+__device__ __forceinline__ size_t ring_progress_index(int owner, int c, int w) {
+  return ((size_t)owner * kMaxRingCtas + c) * kMaxRingWarps + w;
+}
+
 template <int R>
 __device__ __forceinline__ uint64_t* ring_slot(const FusedArgs& f, int o, int s, int c, int C,
                                                int p, int tid, int T) {
@@ -483,10 +462,8 @@ template <int R>
 __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8_ring(CallArgs a, FusedArgs f) {
   __shared__ const uint16_t* s_in[R];
   __shared__ uint16_t* s_out[R];
-  __shared__ int s_abort;
   const Lane l = packet_prologue<R>(a, f, s_in, s_out);
-  if (threadIdx.x == 0) s_abort = 0;
-  const int T = blockDim.x, tid = threadIdx.x;
+  const int T = blockDim.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int C = (int)(gridDim.x / R), c = (int)(blockIdx.x / R), r = l.r;
   const int D = f.ring_depth;
   const size_t Vs = l.Vs;
@@ -495,21 +472,22 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8_ring(CallArgs a,
   const uint16_t* my_in = s_in[r];
   const size_t g0 = (size_t)r * Vs;  // first group of my shard
   const size_t my_n = g0 < a.groups ? min(Vs, a.groups - g0) : 0;
-  // Threads 0..R-2 each watch one other owner's progress (credits).
-  const int watch = (R > 1 && tid < R - 1) ? (r + 1 + tid) % R : -1;
-  uint32_t* const my_progress = f.progress + (size_t)r * kMaxRingCtas + c;
+  // Thread t of producer CTA (s, c) writes exactly the ring slots that
+  // thread t of consumer CTA (o, c) reads, so credits are per warp: lanes
+  // 0..R-2 each watch one other owner's progress word for this warp.
+  const int watch = (R > 1 && lane < R - 1) ? (r + 1 + lane) % R : -1;
+  uint32_t* const my_progress = f.progress + ring_progress_index(r, c, warp);
   const uint32_t* const watched =
-      watch >= 0 ? f.progress + (size_t)watch * kMaxRingCtas + c : nullptr;
+      watch >= 0 ? f.progress + ring_progress_index(watch, c, warp) : nullptr;
   uint32_t pv = watch >= 0 ? ld_acquire_u32(watched) : 0u;
-  __syncthreads();
 
   for (size_t k = 0; k <= K; ++k) {
-    // ---- credits for round k: every other owner has read round k - D ----
+    // ---- credits for round k: every other owner's warp has read round k - D
     if (R > 1 && k < K && k >= (size_t)D) {
-      if (watch >= 0 && !wait_credit(f, watched, pv, flag_at(l.epoch, k - D), r, l.epoch))
-        s_abort = 1;
-      __syncthreads();
-      if (s_abort) break;
+      const bool ok =
+          watch < 0 || wait_credit(f, watched, pv, flag_at(l.epoch, k - D), r, l.epoch);
+      __syncwarp();
+      if (!__all_sync(0xFFFFFFFFu, ok)) break;
     }
     const size_t jk = k * per_round + (size_t)c * T + tid;  // my group of round k
     // ---- issue: input loads of round k, packet loads of round k-1 ----------
@@ -550,9 +528,10 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8_ring(CallArgs a,
       }
     }
     // ---- reduce round k-1 + write-mode broadcast ----------------------------
+    bool ok = true;
     if (reduce) {
       const uint32_t flag = flag_at(l.epoch, k - 1);
-      const bool ok = wait_packets_at<R>(f, pk, pending, flag, l.epoch, r, [&](int s) {
+      ok = wait_packets_at<R>(f, pk, pending, flag, l.epoch, r, [&](int s) {
         return ring_slot<R>(f, r, s, c, C, pp, tid, T);
       });
       if (ok) {
@@ -563,21 +542,14 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8_ring(CallArgs a,
         const uint4 y = acc.round_bf16();
         const size_t g = g0 + jp;
         const int valid = group_valid(g, a.count);
-        if (f.opts & kFusedOptStreamOutputs) {
-          const uint64_t pol_out = l2_policy_evict_first();
 #pragma unroll
-          for (int q = 0; q < R; ++q) store_group<true>(s_out[q], g, y, valid, l.vec, pol_out);
-        } else {
-#pragma unroll
-          for (int q = 0; q < R; ++q) store_group(s_out[q], g, y, valid, l.vec);
-        }
-      } else {
-        s_abort = 1;
+        for (int q = 0; q < R; ++q) store_group(s_out[q], g, y, valid, l.vec);
       }
     }
-    __syncthreads();  // every thread is done reading ring slot pp
-    if (s_abort) break;
-    if (k >= 1 && tid == 0) st_release_u32(my_progress, flag_at(l.epoch, k - 1));
+    // Every lane of the warp is done reading ring slot pp: publish it.
+    __syncwarp();
+    if (!__all_sync(0xFFFFFFFFu, ok)) break;
+    if (k >= 1 && lane == 0) st_release_u32(my_progress, flag_at(l.epoch, k - 1));
   }
   epoch_advance_to(f, flag_at(l.epoch, K));
 }
@@ -801,7 +773,6 @@ extern "C" ar_status_t ar_allreduce_fused_noalloc(int R, const void* const* d_in
   f.skip_producer = -1;
   f.ring_depth = 0;
   f.progress = nullptr;
-  f.opts = 0;
   const size_t limit = (size_t)d.ctas_per_sm[R] * (size_t)d.sms / (size_t)R;
   size_t per_rank = (a.shard_groups + kNoAllocThreads - 1) / kNoAllocThreads;
   per_rank = std::max<size_t>(1, std::min(per_rank, limit));
