@@ -25,6 +25,7 @@ CFLAGS = [
     "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
     "-fexcess-precision=standard", "-fPIC", "-shared",
 ]
+LIBS = ["-lm"]
 
 _lock = threading.Lock()
 _lib = None
@@ -36,7 +37,7 @@ def build(force: bool = False, src: str = _SRC, out: str = _LIB) -> str:
             and os.path.getmtime(out) >= os.path.getmtime(src)):
         return out
     tmp = out + ".tmp%d" % os.getpid()
-    subprocess.check_call(["gcc", *CFLAGS, src, "-o", tmp])
+    subprocess.check_call(["gcc", *CFLAGS, src, "-o", tmp, *LIBS])
     os.replace(tmp, out)
     return out
 
@@ -64,6 +65,20 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_allreduce_bf16.argtypes = [
         ctypes.c_int, ctypes.c_size_t, ctypes.POINTER(u16p), ctypes.POINTER(u16p)]
     lib.oracle_allreduce_bf16.restype = ctypes.c_int
+    lib.oracle_f16_to_f32.argtypes = [ctypes.c_uint16]
+    lib.oracle_f16_to_f32.restype = ctypes.c_float
+    lib.oracle_f32_to_f16_rne.argtypes = [ctypes.c_float]
+    lib.oracle_f32_to_f16_rne.restype = ctypes.c_uint16
+    lib.oracle_f32_to_f16_array.argtypes = [
+        ctypes.POINTER(ctypes.c_float), u16p, ctypes.c_size_t]
+    lib.oracle_f32_to_f16_array.restype = None
+    f32p = ctypes.POINTER(ctypes.c_float)
+    lib.oracle_allreduce_f16.argtypes = [
+        ctypes.c_int, ctypes.c_size_t, ctypes.POINTER(u16p), ctypes.POINTER(u16p)]
+    lib.oracle_allreduce_f16.restype = ctypes.c_int
+    lib.oracle_allreduce_f32.argtypes = [
+        ctypes.c_int, ctypes.c_size_t, ctypes.POINTER(f32p), ctypes.POINTER(f32p)]
+    lib.oracle_allreduce_f32.restype = ctypes.c_int
     for name in ("oracle_reduce_scatter_bf16", "oracle_all_gather_bf16"):
         fn = getattr(lib, name)
         fn.argtypes = [ctypes.c_int, ctypes.c_size_t, ctypes.POINTER(u16p), ctypes.POINTER(u16p)]
@@ -146,5 +161,41 @@ def all_gather_bf16(inputs, lib: ctypes.CDLL | None = None):
         raise ValueError("inputs must hold the same element count")
     outs = [np.empty(R * sc, np.uint16) for _ in range(R)]
     if lib.oracle_all_gather_bf16(R, sc, _tables(ins), _tables(outs)) != 0:
+        raise ValueError("oracle rejected R=%d" % R)
+    return outs
+
+
+def f32_to_f16(x: np.ndarray, lib: ctypes.CDLL | None = None) -> np.ndarray:
+    """Round an fp32 array to fp16 bit patterns (round to nearest, ties to even)."""
+    lib = lib or load()
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    y = np.empty(x.shape, dtype=np.uint16)
+    lib.oracle_f32_to_f16_array(
+        x.ctypes.data_as(ctypes.POINTER(ctypes.c_float)),
+        y.ctypes.data_as(ctypes.POINTER(ctypes.c_uint16)), x.size)
+    return y
+
+
+def allreduce_f16(inputs, lib: ctypes.CDLL | None = None):
+    """Allreduce of R fp16 buffers (uint16 bit patterns); returns output 0."""
+    lib = lib or load()
+    ins = [_u16(a) for a in inputs]
+    R, count = len(ins), ins[0].size
+    outs = [np.empty(count, np.uint16) for _ in range(R)]
+    if lib.oracle_allreduce_f16(R, count, _tables(ins), _tables(outs)) != 0:
+        raise ValueError("oracle rejected R=%d" % R)
+    return outs
+
+
+def allreduce_f32(inputs, lib: ctypes.CDLL | None = None):
+    """Allreduce of R fp32 buffers; returns the R outputs."""
+    lib = lib or load()
+    ins = [np.ascontiguousarray(a, dtype=np.float32) for a in inputs]
+    R, count = len(ins), ins[0].size
+    outs = [np.empty(count, np.float32) for _ in range(R)]
+    f32p = ctypes.POINTER(ctypes.c_float)
+    it = (f32p * R)(*[a.ctypes.data_as(f32p) for a in ins])
+    ot = (f32p * R)(*[o.ctypes.data_as(f32p) for o in outs])
+    if lib.oracle_allreduce_f32(R, count, it, ot) != 0:
         raise ValueError("oracle rejected R=%d" % R)
     return outs

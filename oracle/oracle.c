@@ -26,6 +26,7 @@
  * Build: gcc -O2 -std=c11 -ffp-contract=off -fno-fast-math
  *        -fexcess-precision=standard -fPIC -shared oracle.c -o liboracle.so
  */
+#include <math.h>
 #include <stddef.h>
 #include <stdint.h>
 #include <string.h>
@@ -138,5 +139,109 @@ int oracle_all_gather_bf16(int R, size_t sendcount, const uint16_t* const* in,
   for (int r = 0; r < R; ++r)
     for (int s = 0; s < R; ++s)
       for (size_t j = 0; j < sendcount; ++j) out[r][(size_t)s * sendcount + j] = in[s][j];
+  return 0;
+}
+
+/* ------------------------------------------------------------------------
+ * Other element types: IEEE binary16 (fp16) and binary32 (fp32).  The
+ * reduction is the same rank-order fp32 accumulation; fp16 is widened
+ * exactly and rounded once at the end, fp32 is not rounded at all.
+ */
+
+/* fp16 -> fp32, exact.  exponent field e, fraction f (10 bits):
+ * e = 0: f * 2^-24 (zero or subnormal); e = 31: inf (f = 0) or NaN;
+ * otherwise (1024 + f) * 2^(e - 25). */
+float oracle_f16_to_f32(uint16_t h) {
+  const uint32_t sign = (uint32_t)(h >> 15) & 1u;
+  const uint32_t e = (uint32_t)(h >> 10) & 0x1Fu;
+  const uint32_t f = (uint32_t)h & 0x3FFu;
+  float mag;
+  if (e == 0u) {
+    mag = ldexpf((float)f, -24);
+  } else if (e == 31u) {
+    uint32_t u = f ? (0x7FC00000u | (f << 13)) : 0x7F800000u;
+    memcpy(&mag, &u, sizeof mag);
+  } else {
+    mag = ldexpf((float)(1024u + f), (int)e - 25);
+  }
+  return sign ? -mag : mag;
+}
+
+/*
+ * fp32 -> fp16, IEEE 754 round to nearest, ties to even.
+ *
+ * A finite fp32 value is M * 2^E with M an integer (the 24-bit significand
+ * with its implicit bit, or the 23-bit fraction of a subnormal) and
+ * E = max(exponent field, 1) - 150.  fp16 represents multiples of the
+ * quantum q = 2^(b - 10) in the binade [2^b, 2^(b+1)) for b >= -14, and of
+ * 2^-24 below 2^-14.  The value divided by q is rounded to the nearest
+ * integer n, ties to the even one; n is then the fp16 significand: below
+ * 2^-14 the encoding is n itself (n = 1024 is exactly the smallest normal),
+ * in a normal binade it is ((b + 15) << 10) + n - 1024, and n = 2048 moves
+ * to the next binade.  Exponents past 15 give infinity.  NaN becomes a
+ * quiet NaN keeping the sign and the top fraction bits.
+ */
+uint16_t oracle_f32_to_f16_rne(float x) {
+  uint32_t u;
+  memcpy(&u, &x, sizeof u);
+  const uint16_t sign = (uint16_t)((u >> 16) & 0x8000u);
+  const uint32_t ef = (u >> 23) & 0xFFu;
+  const uint32_t frac = u & 0x7FFFFFu;
+  if (ef == 0xFFu) {
+    if (frac) return (uint16_t)(sign | 0x7E00u | (frac >> 13));
+    return (uint16_t)(sign | 0x7C00u);
+  }
+  if (ef == 0u && frac == 0u) return sign;
+  const uint64_t M = ef ? (uint64_t)(frac | 0x800000u) : (uint64_t)frac;
+  const int E = (ef ? (int)ef : 1) - 150;
+  /* binade of |x|: position of M's top bit */
+  int top = 63;
+  while (!((M >> top) & 1u)) --top;
+  const int b = top + E;
+  const int qexp = b >= -14 ? b - 10 : -24;
+  const int shift = qexp - E; /* value / q = M / 2^shift */
+  uint64_t n;
+  if (shift <= 0) {
+    n = M << (-shift);
+  } else if (shift >= 64) {
+    n = 0;
+  } else {
+    const uint64_t lo = M & ((1ull << shift) - 1ull);
+    const uint64_t half = 1ull << (shift - 1);
+    n = M >> shift;
+    if (lo > half || (lo == half && (n & 1ull))) n += 1;
+  }
+  if (b < -14) return (uint16_t)(sign | (uint16_t)n); /* subnormal, or exactly 2^-14 */
+  int eb = b;
+  if (n == 2048u) {
+    n = 1024u;
+    eb += 1;
+  }
+  if (eb > 15) return (uint16_t)(sign | 0x7C00u);
+  return (uint16_t)(sign | (uint16_t)(((uint32_t)(eb + 15) << 10) + (uint32_t)(n - 1024u)));
+}
+
+void oracle_f32_to_f16_array(const float* x, uint16_t* y, size_t n) {
+  for (size_t i = 0; i < n; ++i) y[i] = oracle_f32_to_f16_rne(x[i]);
+}
+
+int oracle_allreduce_f16(int R, size_t count, const uint16_t* const* in, uint16_t* const* out) {
+  if (R < 1 || R > 64) return -1;
+  for (size_t i = 0; i < count; ++i) {
+    float acc = oracle_f16_to_f32(in[0][i]);
+    for (int r = 1; r < R; ++r) acc = acc + oracle_f16_to_f32(in[r][i]);
+    const uint16_t y = oracle_f32_to_f16_rne(acc);
+    for (int r = 0; r < R; ++r) out[r][i] = y;
+  }
+  return 0;
+}
+
+int oracle_allreduce_f32(int R, size_t count, const float* const* in, float* const* out) {
+  if (R < 1 || R > 64) return -1;
+  for (size_t i = 0; i < count; ++i) {
+    float acc = in[0][i];
+    for (int r = 1; r < R; ++r) acc = acc + in[r][i];
+    for (int r = 0; r < R; ++r) out[r][i] = acc;
+  }
   return 0;
 }

@@ -64,7 +64,8 @@ struct ar_ctx {
   size_t ring_bytes = 0;
   size_t ring_threads = 0;       // threads per rank the ring can hold (C * T)
   uint32_t* progress = nullptr;  // ring variant's progress words [R][kMaxRingCtas][kMaxRingWarps]
-  int ring_depth = 2;
+  int ring_depth = 4;            // measured best on GB300 (2..4 allowed)
+  int ring_threads_default = 128;
   size_t slot_groups = 0;
   uint64_t spin_limit_ns = 100ull * 1000ull * 1000ull;
   int skip_producer = -1;
@@ -214,7 +215,7 @@ LaunchCfg shape(ar_ctx* h, int variant, const TuneRow* row, size_t groups, size_
     }
     case AR_FUSED_LL8_RING: {
       // Co-resident, at most kMaxRingCtas per rank, and C * T within the ring.
-      if (c.threads <= 0) c.threads = h->fused_threads;
+      if (c.threads <= 0) c.threads = h->ring_threads_default;
       const int per_sm = occupancy(h, variant, c.threads);
       size_t limit = (size_t)per_sm * (size_t)h->num_sms / (size_t)R;
       limit = std::min(limit, (size_t)ar::kMaxRingCtas);
