@@ -13,7 +13,6 @@ written next to its case.
 from __future__ import annotations
 
 import struct
-from fractions import Fraction
 
 import numpy as np
 import torch
@@ -274,11 +273,106 @@ def pin_all_gather_exact(lib):
     return fails
 
 
+# --------------------------------------------------------------------------
+# fp16 and fp32 element types.
+
+def f16_bits_of(x: float) -> int:
+    """Bits of a value exactly representable in fp16 (checked with numpy)."""
+    h = np.array([x], dtype=np.float16)
+    if float(h[0]) != x and x == x:
+        raise ValueError("%r is not exactly representable in fp16" % x)
+    return int(h.view(np.uint16)[0])
+
+
+def compare_rounding_f16(lib, u32: np.ndarray):
+    f = u32.view(np.float32)
+    mine = oracle.f32_to_f16(f, lib=lib)
+    ref = torch.from_numpy(f.copy()).to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+    nan_in = np.isnan(f)
+    mine_nan = ((mine & 0x7C00) == 0x7C00) & ((mine & 0x3FF) != 0)
+    bad = (~nan_in & (mine != ref)) | (nan_in & ~mine_nan)
+    return u32[bad]
+
+
+def pin_f16_rounding(lib):
+    hi = np.arange(1 << 16, dtype=np.uint32) << 16
+    lows = [0x0000, 0x0001, 0x0FFF, 0x1000, 0x1001, 0x1FFF, 0x2000, 0x2001, 0x7FFF, 0x8000,
+            0xFFFF]
+    rng = np.random.default_rng(99)
+    parts = [hi | np.uint32(lo) for lo in lows]
+    parts.append(rng.integers(0, 1 << 32, 1 << 22, dtype=np.uint64).astype(np.uint32))
+    bad = compare_rounding_f16(lib, np.concatenate(parts))
+    return ["fp32->fp16 differs from torch at %s" % [hex(int(v)) for v in bad[:4]]] if bad.size else []
+
+
+def pin_f16_widening(lib):
+    h = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    mine = np.array([lib.oracle_f16_to_f32(int(v)) for v in h], dtype=np.float32)
+    ref = torch.from_numpy(h.view(np.int16)).view(torch.float16).float().numpy()
+    nan = np.isnan(ref)
+    bad = (~nan & (mine.view(np.uint32) != ref.view(np.uint32))) | (nan & ~np.isnan(mine))
+    return ["fp16->fp32 differs from torch at %s" % [hex(int(v)) for v in h[bad][:4]]] if bad.any() else []
+
+
+F16_CLOSED_FORMS = [
+    ([1.0, 2.0 ** -11], 1.0, "1+2^-11 is halfway between 1 and 1+2^-10; tie to even -> 1."),
+    ([1.0 + 2.0 ** -10, 2.0 ** -11], 1.0 + 2.0 ** -9,
+     "halfway between 1+2^-10 (odd) and 1+2^-9 (even) -> 1+2^-9."),
+    ([1.0, 2.0 ** -12, 2.0 ** -12, 2.0 ** -12], 1.0 + 2.0 ** -10,
+     "1+3*2^-12 is exact in fp32; one rounding: 3/4 of an fp16 spacing -> 1+2^-10."),
+    ([65504.0, 16.0], float("inf"),
+     "65520 is halfway between 65504 (odd last bit) and 65536 (= overflow) -> inf."),
+    ([65504.0, 15.0], 65504.0, "65519 is below the halfway point 65520 -> 65504."),
+    ([2.0 ** -24] * 8, 2.0 ** -21, "8 x smallest subnormal = 2^-21, exact, no flush."),
+    ([2.0 ** -14, -(2.0 ** -24)], 2.0 ** -14 - 2.0 ** -24, "largest subnormal, exact."),
+    ([2.0 ** -25, 2.0 ** -26], 2.0 ** -24,
+     "3*2^-26 is 3/4 of the subnormal spacing 2^-24 -> 2^-24."),
+    ([2.0 ** -25], 0.0, "2^-25 is halfway between 0 (even) and 2^-24 -> +0."),
+    ([-0.0, -0.0], -0.0, "(-0)+(-0) = -0."),
+]
+
+
+def pin_f16_closed_forms(lib):
+    fails = []
+    for vals, expect, why in F16_CLOSED_FORMS:
+        # 2^-25 and 2^-26 are not fp16 values: feed them as fp32 sums of fp16 inputs where
+        # needed; every input below is exact in fp16 except those two, which only appear
+        # in the rounding cases and are applied through the fp32 -> fp16 routine directly.
+        if any(v != 0 and abs(v) < 2.0 ** -24 for v in vals):
+            acc = np.float32(vals[0])
+            for v in vals[1:]:
+                acc = np.float32(acc + np.float32(v))
+            got = int(oracle.f32_to_f16(np.array([acc], np.float32), lib=lib)[0])
+        else:
+            xs = [np.array([f16_bits_of(v)], np.uint16) for v in vals]
+            got = int(oracle.allreduce_f16(xs, lib=lib)[0][0])
+        want = f16_bits_of(expect)
+        if got != want:
+            fails.append("fp16 closed form %s: got %s want %s (%s)" % (vals, hex(got), hex(want), why))
+    return fails
+
+
+def pin_f32_exact(lib):
+    fails = []
+    for R in (1, 3, 8):
+        xs = [np.array([((7 * i + 13 * r) % 17) - 8 for i in range(301)], np.float32)
+              for r in range(R)]
+        exact = np.sum(np.stack(xs).astype(np.int64), axis=0).astype(np.float32)
+        outs = oracle.allreduce_f32(xs, lib=lib)
+        if not all(np.array_equal(o, exact) for o in outs):
+            fails.append("fp32 integer sums R=%d" % R)
+    outs = oracle.allreduce_f32([np.array([v], np.float32) for v in (P24, 1.0, 1.0, -P24)], lib=lib)
+    if float(outs[0][0]) != 0.0:
+        fails.append("fp32 rank order closed form gave %r" % float(outs[0][0]))
+    return fails
+
+
 ALL_PINS = [
     pin_identity, pin_all_ones, pin_small_integers, pin_position_fill,
     pin_closed_forms, pin_rounding, pin_tiny_brute_force,
     pin_outputs_identical_and_in_place, pin_reduce_scatter_exact, pin_reduce_scatter_order,
-    pin_all_gather_exact,
+    pin_all_gather_exact, pin_f16_rounding, pin_f16_widening, pin_f16_closed_forms,
+    pin_f32_exact,
 ]
 
 

@@ -72,6 +72,18 @@ MUTANTS = [
      "out[r][(size_t)s * sendcount + j] = in[r][j];"),
     ("all-gather blocks in the wrong order", "out[r][(size_t)s * sendcount + j] = in[s][j];",
      "out[r][(size_t)(R - 1 - s) * sendcount + j] = in[s][j];"),
+    ("fp16 ties away from zero", "if (lo > half || (lo == half && (n & 1ull))) n += 1;",
+     "if (lo >= half) n += 1;"),
+    ("fp16 truncation", "if (lo > half || (lo == half && (n & 1ull))) n += 1;", "(void)lo;"),
+    ("fp16 subnormal quantum off by one", "const int qexp = b >= -14 ? b - 10 : -24;",
+     "const int qexp = b >= -14 ? b - 10 : -25;"),
+    ("fp16 binade carry dropped", "  if (n == 2048u) {\n    n = 1024u;\n    eb += 1;\n  }",
+     "  if (n == 2048u) {\n    n = 1023u;\n  }"),
+    ("fp16 overflow threshold off by one", "if (eb > 15) return (uint16_t)(sign | 0x7C00u);",
+     "if (eb > 16) return (uint16_t)(sign | 0x7C00u);"),
+    ("fp16 widening of subnormals", "mag = ldexpf((float)f, -24);", "mag = ldexpf((float)f, -25);"),
+    ("fp32 accumulation in reverse", "float acc = in[0][i];\n    for (int r = 1; r < R; ++r) acc = acc + in[r][i];",
+     "float acc = in[R - 1][i];\n    for (int r = R - 2; r >= 0; --r) acc = acc + in[r][i];"),
 ]
 
 
