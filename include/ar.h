@@ -1,17 +1,18 @@
 /*
- * ar.h -- C ABI of the GB300 virtual-rank bf16 allreduce library
+ * ar.h -- C ABI of the GB300 virtual-rank allreduce library
  *         (libar_gb300.so).
  *
- * R "virtual ranks" are R separate bf16 buffers in the HBM of ONE GPU.  An
+ * R "virtual ranks" are R separate buffers in the HBM of ONE GPU.  An
  * allreduce leaves, in every rank's output buffer, the element-wise sum of
  * all R input buffers:
  *
- *     out_r[i] = bf16_rne( ((float)in_0[i] + (float)in_1[i]) + ... + (float)in_{R-1}[i] )
+ *     out_r[i] = rne( ((float)in_0[i] + (float)in_1[i]) + ... + (float)in_{R-1}[i] )
  *
  * for every r in [0, R) and i in [0, count): fp32 additions in rank order
  * 0..R-1 (seeded with rank 0's value, no fused multiply-add), one final
- * round-to-nearest-even to bf16.  Every variant below produces this result
- * bit for bit; they differ only in how the data moves.
+ * round-to-nearest-even to the element type (bf16 or fp16; none for fp32).
+ * Every variant below produces this result bit for bit; they differ only in
+ * how the data moves.
  *
  * Where each operation comes from:
  *   - the input/output pointer tables mirror the broadcast table of output
@@ -70,18 +71,21 @@
 extern "C" {
 #endif
 
-#define AR_MAX_RANKS 8
+#define AR_MAX_RANKS 16        /* one-shot, two-phase, reduce-scatter, all-gather */
+#define AR_MAX_PACKET_RANKS 8  /* the LL8 packet variants */
 
 typedef struct ar_ctx* ar_handle_t;
 
 typedef enum {
-  AR_BF16 = 0 /* the only element type: IEEE bfloat16, 2 bytes */
+  AR_BF16 = 0, /* bfloat16, 2 bytes: fp32 accumulation, one round to nearest even */
+  AR_FP16 = 1, /* IEEE binary16, 2 bytes: fp32 accumulation, one round to nearest even */
+  AR_FP32 = 2  /* IEEE binary32, 4 bytes: fp32 accumulation, no final rounding */
 } ar_dtype_t;
 
 typedef enum {
   AR_OK = 0,
   AR_ERR_INVALID_ARG = 1, /* bad R, count, pointer, variant or handle */
-  AR_ERR_UNSUPPORTED = 2, /* dtype other than AR_BF16, or no sm_103 device */
+  AR_ERR_UNSUPPORTED = 2, /* unknown dtype, a packet variant with R > 8, or no sm_103 device */
   AR_ERR_OOM = 3,         /* device allocation failed in ar_create */
   AR_ERR_CUDA = 4,        /* a CUDA runtime call failed (launch, copy, sync) */
   AR_ERR_TIMEOUT = 5      /* a packet wait inside the fused kernel gave up */
@@ -116,14 +120,16 @@ typedef struct {
 /*
  * ar_create -- make a handle for R virtual ranks of up to `max_count`
  * elements each, on the current CUDA device.
- *   R          1 .. AR_MAX_RANKS.
+ *   R          1 .. AR_MAX_RANKS (the LL8 packet variants need R <=
+ *              AR_MAX_PACKET_RANKS; their scratch is allocated only then).
  *   max_count  >= 1; bounds `count` of later calls and sizes the scratch.
- *   dtype      must be AR_BF16.
+ *   dtype      AR_BF16, AR_FP16 or AR_FP32 (element type of every buffer).
  *   out        receives the handle (set to NULL on failure).
  * Allocates, on the current device, two packet scratch regions (scatter
  * packets and the staged variants' result packets), each
- * 32 * R * (R-1) * S bytes with S = ceil(ceil(max_count/8)/R) rounded up
- * to a multiple of 4 (about 4*(R-1)*max_count); the ring variant's packet ring (32 * R * (R-1) * 4 *
+ * 32 * R * (R-1) * S bytes with S = ceil(ceil(max_count/G)/R) rounded up
+ * to a multiple of 4, G = 8 elements per 16-byte group for bf16/fp16 and 4
+ * for fp32 (about 4*(R-1)*max_count bytes for 2-byte types); the ring variant's packet ring (32 * R * (R-1) * 4 *
  * the co-resident threads per rank, independent of max_count) and its
  * progress words; all zeroed here so that no flag matches a live epoch; and
  * a small state block (epoch, done counter, error word).  Synchronous; not
@@ -134,14 +140,14 @@ typedef struct {
 ar_status_t ar_create(int R, size_t max_count, int dtype, ar_handle_t* out);
 
 /*
- * ar_allreduce -- out_r[i] = bf16_rne(sum over s in rank order of in_s[i])
+ * ar_allreduce -- out_r[i] = rne(sum over s in rank order of in_s[i])
  * for every r < R and i < count.
  *   h          handle from ar_create.
  *   d_in_tbl   DEVICE pointer to an array of R device pointers (8 bytes each,
  *              e.g. a CUDA int64 tensor of data_ptr()s); entry r is rank r's
- *              input buffer of `count` bf16 elements, contiguous.
+ *              input buffer of `count` elements of the handle's dtype.
  *   d_out_tbl  DEVICE pointer to an array of R device pointers; entry r is
- *              rank r's output buffer of `count` bf16 elements.
+ *              rank r's output buffer of `count` elements.
  *   count      elements per rank, 0 .. max_count.  0 returns AR_OK, no launch.
  *   stream     cudaStream_t (as void*) the kernels are launched on.
  * The caller owns the buffers and both tables; they must stay valid and
@@ -158,7 +164,8 @@ ar_status_t ar_create(int R, size_t max_count, int dtype, ar_handle_t* out);
  * graph; the fused kernel's epoch lives on the device and rotates on every
  * execution, including graph replays.
  * Errors: AR_ERR_INVALID_ARG (NULL handle or table, count > max_count),
- * AR_ERR_CUDA (launch failure).  A packet wait that exceeds the spin limit
+ * AR_ERR_UNSUPPORTED (a packet variant forced with R > 8), AR_ERR_CUDA
+ * (launch failure).  A packet wait that exceeds the spin limit
  * is reported later by ar_get_device_status (the outputs of that call are
  * then undefined).
  */
@@ -167,7 +174,7 @@ ar_status_t ar_allreduce(ar_handle_t h, const void* const* d_in_tbl,
 
 /*
  * ar_reduce_scatter -- rank r keeps block r of the sum:
- *   out_r[j] = bf16_rne(sum over s in rank order of in_s[r*recvcount + j]),
+ *   out_r[j] = rne(sum over s in rank order of in_s[r*recvcount + j]),
  * j < recvcount.  Same numerics as ar_allreduce.  Each input holds
  * R*recvcount elements, each output recvcount elements; R*recvcount <=
  * max_count.  It is the "srcStride = recvCount, ownOffset = slot *
@@ -205,7 +212,7 @@ ar_status_t ar_select(ar_handle_t h, size_t count, int* variant);
  * (0 = automatic).  ctas is the total grid for AR_FUSED_LL8 (rounded down to
  * a multiple of R, clamped to the co-resident limit and raised to at least
  * R), and the grid-stride CTA count for the others.  threads must be a
- * multiple of 32 in [64, 1024] (the fused and fan-out kernels accept
+ * multiple of 32 in [64, 512] (the packet and fan-out kernels accept
  * 128..512). */
 ar_status_t ar_set_launch(ar_handle_t h, int variant, int ctas, int threads);
 
@@ -283,7 +290,8 @@ ar_status_t ar_debug_get_epoch(ar_handle_t h, uint32_t* epoch);
  * allocations, or a process that must not allocate once it has started
  * serving.
  *
- * ar_allreduce_fused_noalloc -- the AR_FUSED_LL8 allreduce without a handle.
+ * ar_allreduce_fused_noalloc -- the AR_FUSED_LL8 allreduce of bf16 buffers
+ * (R <= AR_MAX_PACKET_RANKS) without a handle.
  * Same arguments and result as ar_allreduce (R = rank count, 1..AR_MAX_RANKS;
  * device pointer tables; count elements per rank; stream), but the packet
  * scratch and the epoch/counter/error block live in fixed arrays inside the

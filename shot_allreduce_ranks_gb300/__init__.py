@@ -9,8 +9,9 @@ from __future__ import annotations
 
 import ctypes
 
-from ._lib import (AR_AUTO, AR_FUSED_LL8, AR_ONESHOT_FANOUT, AR_ONESHOT_PULL,  # noqa: F401
-                   AR_TWOPHASE, AR_MAX_RANKS, VARIANTS, ArError, ArInfo, check, load)
+from ._lib import (AR_AUTO, AR_BF16, AR_FP16, AR_FP32, AR_FUSED_LL8,  # noqa: F401
+                   AR_MAX_PACKET_RANKS, AR_MAX_RANKS, AR_ONESHOT_FANOUT, AR_ONESHOT_PULL,
+                   AR_TWOPHASE, VARIANTS, ArError, ArInfo, check, load)
 
 __all__ = ["AllReduce", "ArError", "VARIANTS", "allreduce_fused_noalloc", "load"]
 
@@ -23,6 +24,14 @@ def _variant_id(v) -> int:
     return int(v)
 
 
+def _dtype_code(dtype) -> int:
+    import torch
+    codes = {torch.bfloat16: AR_BF16, torch.float16: AR_FP16, torch.float32: AR_FP32}
+    if dtype not in codes:
+        raise ValueError("dtype must be torch.bfloat16, torch.float16 or torch.float32")
+    return codes[dtype]
+
+
 def _stream_handle(stream) -> int:
     import torch
     if stream is None:
@@ -31,24 +40,27 @@ def _stream_handle(stream) -> int:
 
 
 class AllReduce:
-    """A handle for R virtual ranks of up to ``max_count`` bf16 elements each.
+    """A handle for R virtual ranks of up to ``max_count`` elements each.
 
     ``ar(inputs, outputs)`` leaves in every ``outputs[r]`` the rank-order fp32
-    sum of all ``inputs``, rounded once to bf16.  Buffers are contiguous CUDA
-    bf16 tensors on the handle's device; ``outputs`` may be ``inputs`` (in
-    place).  Calls are asynchronous on the current (or given) stream.
+    sum of all ``inputs``, rounded once to the element type (bf16, fp16; fp32
+    is not rounded).  Buffers are contiguous CUDA tensors of ``dtype`` on the
+    handle's device; ``outputs`` may be ``inputs`` (in place).  Calls are
+    asynchronous on the current (or given) stream.
     """
 
-    def __init__(self, R: int, max_count: int, device=None):
+    def __init__(self, R: int, max_count: int, device=None, dtype=None):
         import torch
         self._lib = load()
         self.R = int(R)
         self.max_count = int(max_count)
+        self.dtype = torch.bfloat16 if dtype is None else dtype
+        code = _dtype_code(self.dtype)
         self.device = torch.device("cuda", torch.cuda.current_device() if device is None
                                    else torch.device(device).index or 0)
         h = ctypes.c_void_p()
         with torch.cuda.device(self.device):
-            check(self._lib.ar_create(self.R, self.max_count, 0, ctypes.byref(h)), "ar_create")
+            check(self._lib.ar_create(self.R, self.max_count, code, ctypes.byref(h)), "ar_create")
         self._h = h
         self._tables = {}
 
@@ -93,8 +105,8 @@ class AllReduce:
         if len(bufs) != self.R:
             raise ValueError("expected %d buffers, got %d" % (self.R, len(bufs)))
         for t in bufs:
-            if t.dtype != torch.bfloat16 or not t.is_cuda or t.device != self.device:
-                raise ValueError("buffers must be bf16 CUDA tensors on %s" % self.device)
+            if t.dtype != self.dtype or not t.is_cuda or t.device != self.device:
+                raise ValueError("buffers must be %s CUDA tensors on %s" % (self.dtype, self.device))
             if not t.is_contiguous() or t.numel() < count:
                 raise ValueError("buffers must be contiguous with >= %d elements" % count)
 
@@ -126,7 +138,7 @@ class AllReduce:
         if recvcount is None:
             recvcount = inputs[0].numel() // self.R
         if outputs is None:
-            outputs = [torch.empty(recvcount, dtype=torch.bfloat16, device=self.device)
+            outputs = [torch.empty(recvcount, dtype=self.dtype, device=self.device)
                        for _ in range(self.R)]
         self._check_buffers(inputs, self.R * recvcount)
         self._check_buffers(outputs, recvcount)
@@ -142,7 +154,7 @@ class AllReduce:
         if sendcount is None:
             sendcount = inputs[0].numel()
         if outputs is None:
-            outputs = [torch.empty(self.R * sendcount, dtype=torch.bfloat16, device=self.device)
+            outputs = [torch.empty(self.R * sendcount, dtype=self.dtype, device=self.device)
                        for _ in range(self.R)]
         self._check_buffers(inputs, sendcount)
         self._check_buffers(outputs, self.R * sendcount)

@@ -48,6 +48,8 @@ static const TuneRow kBuiltinTable[] = {
 
 struct ar_ctx {
   int R = 0;
+  int dtype = AR_BF16;
+  size_t elem_bytes = 2;
   size_t max_count = 0;
   int device = 0;
   int num_sms = 0;
@@ -79,14 +81,19 @@ struct ar_ctx {
   int bulk_ctas_per_sm = 0;    // bulk fan-out (fixed 256 threads)
 
   // host-buffer path
-  uint16_t* staging = nullptr;        // 2 * R * max_count elements
-  uint16_t** staging_tables = nullptr;  // device: R input pointers, then R output pointers
-  uint16_t** direct_tables = nullptr;   // device: the caller's buffers, when device-accessible
+  char* staging = nullptr;        // 2 * R buffers of max_count elements
+  char** staging_tables = nullptr;  // device: R input pointers, then R output pointers
+  char** direct_tables = nullptr;   // device: the caller's buffers, when device-accessible
 };
 
 namespace {
 
 ar_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? AR_OK : AR_ERR_CUDA; }
+
+bool is_packet_variant(int v) {
+  return v == AR_FUSED_LL8 || v == AR_FUSED_LL8_STAGED || v == AR_PACKET_3OP ||
+         v == AR_FUSED_LL8_RING;
+}
 
 size_t ceil_div(size_t a, size_t b) { return (a + b - 1) / b; }
 
@@ -153,10 +160,11 @@ int occupancy(ar_ctx* h, int variant, int threads) {
   const int k = threads / 32;
   if (k < 0 || k > 32) return 0;
   if (cache[k] == 0) {
-    const int n = variant == AR_FUSED_LL8          ? ar::fused_ctas_per_sm(h->R, threads)
-                  : variant == AR_FUSED_LL8_STAGED ? ar::fused_staged_ctas_per_sm(h->R, threads)
-                  : variant == AR_FUSED_LL8_RING   ? ar::fused_ring_ctas_per_sm(h->R, threads)
-                                                   : ar::fanout_ctas_per_sm(h->R, threads);
+    const int R = h->R, dt = h->dtype;
+    const int n = variant == AR_FUSED_LL8          ? ar::fused_ctas_per_sm(R, dt, threads)
+                  : variant == AR_FUSED_LL8_STAGED ? ar::fused_staged_ctas_per_sm(R, dt, threads)
+                  : variant == AR_FUSED_LL8_RING   ? ar::fused_ring_ctas_per_sm(R, dt, threads)
+                                                   : ar::fanout_ctas_per_sm(R, dt, threads);
     cache[k] = n > 0 ? n : -1;
   }
   return cache[k] > 0 ? cache[k] : 0;
@@ -252,10 +260,11 @@ ar_status_t check_device(const ar_ctx* h) {
 ar_status_t launch(ar_ctx* h, int variant, const TuneRow* row, const void* const* d_in,
                    void* const* d_out, size_t count, cudaStream_t s) {
   CallArgs a;
-  a.in_tbl = reinterpret_cast<const uint16_t* const*>(d_in);
-  a.out_tbl = reinterpret_cast<uint16_t* const*>(d_out);
+  if (is_packet_variant(variant) && h->R > AR_MAX_PACKET_RANKS) return AR_ERR_UNSUPPORTED;
+  a.in_tbl = reinterpret_cast<const char* const*>(d_in);
+  a.out_tbl = reinterpret_cast<char* const*>(d_out);
   a.count = count;
-  a.groups = ceil_div(count, (size_t)ar::kVecElems);
+  a.groups = ceil_div(count, (size_t)ar::group_elems(h->dtype));
   a.shard_groups = ceil_div(a.groups, (size_t)h->R);
   a.state = h->state;
   a.spin_limit_ns = h->spin_limit_ns;
@@ -267,16 +276,16 @@ ar_status_t launch(ar_ctx* h, int variant, const TuneRow* row, const void* const
   cudaError_t e = cudaErrorInvalidValue;
   switch (variant) {
     case AR_ONESHOT_PULL:
-      e = ar::launch_oneshot_pull(h->R, a, cfg, s);
+      e = ar::launch_oneshot_pull(h->R, h->dtype, a, cfg, s);
       break;
     case AR_ONESHOT_FANOUT:
-      e = ar::launch_oneshot_fanout(h->R, a, cfg, s);
+      e = ar::launch_oneshot_fanout(h->R, h->dtype, a, cfg, s);
       break;
     case AR_TWOPHASE:
-      e = ar::launch_twophase(h->R, a, cfg, s);
+      e = ar::launch_twophase(h->R, h->dtype, a, cfg, s);
       break;
     case AR_ONESHOT_FANOUT_BULK:
-      e = ar::launch_oneshot_fanout_bulk(h->R, a, cfg.ctas, s);
+      e = ar::launch_oneshot_fanout_bulk(h->R, h->dtype, a, cfg.ctas, s);
       break;
     case AR_FUSED_LL8_RING: {
       FusedArgs f;
@@ -289,7 +298,7 @@ ar_status_t launch(ar_ctx* h, int variant, const TuneRow* row, const void* const
       f.ring_depth = h->ring_depth;
       f.progress = h->progress;
       h->skip_producer = -1;
-      e = ar::launch_fused_ll8_ring(h->R, a, f, cfg, s);
+      e = ar::launch_fused_ll8_ring(h->R, h->dtype, a, f, cfg, s);
       break;
     }
     case AR_FUSED_LL8:
@@ -305,9 +314,10 @@ ar_status_t launch(ar_ctx* h, int variant, const TuneRow* row, const void* const
       f.ring_depth = h->ring_depth;
       f.progress = h->progress;
       h->skip_producer = -1;
-      e = variant == AR_FUSED_LL8          ? ar::launch_fused_ll8(h->R, a, f, cfg, s)
-          : variant == AR_FUSED_LL8_STAGED ? ar::launch_fused_ll8_staged(h->R, a, f, cfg, s)
-                                           : ar::launch_packet_3op(h->R, a, f, cfg, s);
+      const int dt = h->dtype;
+      e = variant == AR_FUSED_LL8          ? ar::launch_fused_ll8(h->R, dt, a, f, cfg, s)
+          : variant == AR_FUSED_LL8_STAGED ? ar::launch_fused_ll8_staged(h->R, dt, a, f, cfg, s)
+                                           : ar::launch_packet_3op(h->R, dt, a, f, cfg, s);
       break;
     }
     default:
@@ -352,7 +362,7 @@ ar_status_t ar_create(int R, size_t max_count, int dtype, ar_handle_t* out) {
   *out = nullptr;
   if (R < 1 || R > AR_MAX_RANKS || max_count == 0) return AR_ERR_INVALID_ARG;
   if (max_count > ((size_t)1 << 40)) return AR_ERR_INVALID_ARG;
-  if (dtype != AR_BF16) return AR_ERR_UNSUPPORTED;
+  if (dtype != AR_BF16 && dtype != AR_FP16 && dtype != AR_FP32) return AR_ERR_UNSUPPORTED;
   int dev = 0, major = 0, minor = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return AR_ERR_CUDA;
   if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
@@ -364,6 +374,8 @@ ar_status_t ar_create(int R, size_t max_count, int dtype, ar_handle_t* out) {
   ar_ctx* h = new (std::nothrow) ar_ctx();
   if (!h) return AR_ERR_OOM;
   h->R = R;
+  h->dtype = dtype;
+  h->elem_bytes = dtype == AR_FP32 ? 4 : 2;
   h->max_count = max_count;
   h->device = dev;
   h->num_sms = sms;
@@ -385,23 +397,26 @@ ar_status_t ar_create(int R, size_t max_count, int dtype, ar_handle_t* out) {
   env = getenv("AR_LOG");
   h->log = env && env[0] == '1';
 
-  const size_t groups = ceil_div(max_count, (size_t)ar::kVecElems);
+  const size_t groups = ceil_div(max_count, (size_t)ar::group_elems(dtype));
   // Rounded up to 4 groups so that every slot starts on a 128-byte line.
+  // The packet variants (and their scratch) exist for R <= AR_MAX_PACKET_RANKS.
+  const bool packets = R <= AR_MAX_PACKET_RANKS;
   h->slot_groups = (ceil_div(groups, (size_t)R) + 3) / 4 * 4;
-  h->scratch_bytes = (size_t)R * (size_t)(R - 1) * h->slot_groups * 4 * sizeof(uint64_t);
-  h->fused_ctas_per_sm = occupancy(h, AR_FUSED_LL8, h->fused_threads);
+  h->scratch_bytes =
+      packets ? (size_t)R * (size_t)(R - 1) * h->slot_groups * 4 * sizeof(uint64_t) : 0;
+  h->fused_ctas_per_sm = packets ? occupancy(h, AR_FUSED_LL8, h->fused_threads) : 0;
   env = getenv("AR_RING_DEPTH");
   if (env && *env) {
     const long d = strtol(env, nullptr, 10);
     if (d >= 2 && d <= ar::kMaxRingDepth) h->ring_depth = (int)d;
   }
-  for (int t = 128; t <= 512; t *= 2) {
+  for (int t = 128; packets && t <= 512; t *= 2) {
     const size_t per_rank = std::min<size_t>(
         (size_t)occupancy(h, AR_FUSED_LL8_RING, t) * (size_t)sms / (size_t)R, ar::kMaxRingCtas);
     h->ring_threads = std::max(h->ring_threads, per_rank * (size_t)t);
   }
   h->ring_bytes = (size_t)R * (size_t)(R - 1) * ar::kMaxRingDepth * h->ring_threads * 32;
-  if (ar::bulk_prepare(R) == cudaSuccess) h->bulk_ctas_per_sm = ar::bulk_ctas_per_sm(R);
+  if (ar::bulk_prepare(R, dtype) == cudaSuccess) h->bulk_ctas_per_sm = ar::bulk_ctas_per_sm(R, dtype);
   cudaGetLastError();
 
   ar_status_t st = AR_OK;
@@ -474,7 +489,7 @@ ar_status_t ar_select(ar_handle_t h, size_t count, int* variant) {
 ar_status_t ar_set_launch(ar_handle_t h, int variant, int ctas, int threads) {
   if (!h || variant <= AR_AUTO || variant >= AR_NUM_VARIANTS) return AR_ERR_INVALID_ARG;
   if (ctas < 0 || threads < 0) return AR_ERR_INVALID_ARG;
-  if (threads && (threads % 32 || threads < 64 || threads > 1024)) return AR_ERR_INVALID_ARG;
+  if (threads && (threads % 32 || threads < 64 || threads > 512)) return AR_ERR_INVALID_ARG;
   if ((variant == AR_FUSED_LL8 || variant == AR_ONESHOT_FANOUT) && threads &&
       (threads < 128 || threads > 512))
     return AR_ERR_INVALID_ARG;
@@ -491,7 +506,7 @@ ar_status_t ar_set_spin_limit_ns(ar_handle_t h, uint64_t ns) {
 ar_status_t ar_query(ar_handle_t h, ar_info_t* info) {
   if (!h || !info) return AR_ERR_INVALID_ARG;
   info->R = h->R;
-  info->dtype = AR_BF16;
+  info->dtype = h->dtype;
   info->max_count = h->max_count;
   info->scratch_bytes = 2 * h->scratch_bytes + h->ring_bytes;
   info->num_sms = h->num_sms;
@@ -522,10 +537,10 @@ static ar_status_t launch_block_collective(ar_handle_t h, bool rs, const void* c
   ar_status_t st = check_device(h);
   if (st != AR_OK) return st;
   CallArgs a;
-  a.in_tbl = reinterpret_cast<const uint16_t* const*>(d_in);
-  a.out_tbl = reinterpret_cast<uint16_t* const*>(d_out);
+  a.in_tbl = reinterpret_cast<const char* const*>(d_in);
+  a.out_tbl = reinterpret_cast<char* const*>(d_out);
   a.count = block;
-  a.groups = ceil_div(block, (size_t)ar::kVecElems);
+  a.groups = ceil_div(block, (size_t)ar::group_elems(h->dtype));
   a.shard_groups = a.groups;
   a.state = h->state;
   a.spin_limit_ns = h->spin_limit_ns;
@@ -537,8 +552,8 @@ static ar_status_t launch_block_collective(ar_handle_t h, bool rs, const void* c
     fprintf(stderr, "[ar] R=%d %s block=%zu ctas=%dx%d threads=%d\n", h->R,
             rs ? "reduce_scatter" : "all_gather", block, cfg.ctas, h->R, cfg.threads);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return cuda_status(rs ? ar::launch_reduce_scatter(h->R, a, cfg, s)
-                        : ar::launch_all_gather(h->R, a, cfg, s));
+  return cuda_status(rs ? ar::launch_reduce_scatter(h->R, h->dtype, a, cfg, s)
+                        : ar::launch_all_gather(h->R, h->dtype, a, cfg, s));
 }
 
 ar_status_t ar_reduce_scatter(ar_handle_t h, const void* const* d_in_tbl, void* const* d_out_tbl,
@@ -579,13 +594,13 @@ ar_status_t ar_reserve_host_staging(ar_handle_t h) {
   if (h->staging) return AR_OK;
   const size_t per_rank = (h->max_count + 127) / 128 * 128;  // keep every buffer 256-byte aligned
   const size_t elems = 2 * (size_t)h->R * per_rank;
-  if (cudaMalloc(&h->staging, elems * sizeof(uint16_t)) != cudaSuccess) {
+  if (cudaMalloc(&h->staging, elems * h->elem_bytes) != cudaSuccess) {
     cudaGetLastError();
     h->staging = nullptr;
     return AR_ERR_OOM;
   }
-  if (cudaMalloc(&h->staging_tables, 2 * (size_t)h->R * sizeof(uint16_t*)) != cudaSuccess ||
-      cudaMalloc(&h->direct_tables, 2 * (size_t)h->R * sizeof(uint16_t*)) != cudaSuccess) {
+  if (cudaMalloc(&h->staging_tables, 2 * (size_t)h->R * sizeof(char*)) != cudaSuccess ||
+      cudaMalloc(&h->direct_tables, 2 * (size_t)h->R * sizeof(char*)) != cudaSuccess) {
     cudaGetLastError();
     cudaFree(h->staging);
     if (h->staging_tables) cudaFree(h->staging_tables);
@@ -594,9 +609,9 @@ ar_status_t ar_reserve_host_staging(ar_handle_t h) {
     h->direct_tables = nullptr;
     return AR_ERR_OOM;
   }
-  std::vector<uint16_t*> ptrs(2 * (size_t)h->R);
-  for (size_t i = 0; i < ptrs.size(); ++i) ptrs[i] = h->staging + i * per_rank;
-  if (cudaMemcpy(h->staging_tables, ptrs.data(), ptrs.size() * sizeof(uint16_t*),
+  std::vector<char*> ptrs(2 * (size_t)h->R);
+  for (size_t i = 0; i < ptrs.size(); ++i) ptrs[i] = h->staging + i * per_rank * h->elem_bytes;
+  if (cudaMemcpy(h->staging_tables, ptrs.data(), ptrs.size() * sizeof(char*),
                  cudaMemcpyHostToDevice) != cudaSuccess)
     return AR_ERR_CUDA;
   return AR_OK;
@@ -649,9 +664,10 @@ ar_status_t ar_allreduce_host(ar_handle_t h, const void* const* h_in, void* cons
 
   // Staging path (pageable host memory): one copy per rank each way.
   const size_t per_rank = (h->max_count + 127) / 128 * 128;
-  const size_t bytes = count * sizeof(uint16_t);
+  const size_t bytes = count * h->elem_bytes;
   for (int r = 0; r < h->R; ++r) {
-    if (cudaMemcpyAsync(h->staging + (size_t)r * per_rank, h_in[r], bytes, cudaMemcpyHostToDevice,
+    if (cudaMemcpyAsync(h->staging + (size_t)r * per_rank * h->elem_bytes, h_in[r], bytes,
+                        cudaMemcpyHostToDevice,
                         s) != cudaSuccess)
       return AR_ERR_CUDA;
   }
@@ -661,7 +677,7 @@ ar_status_t ar_allreduce_host(ar_handle_t h, const void* const* h_in, void* cons
               reinterpret_cast<void* const*>(h->staging_tables + h->R), count, s);
   if (st != AR_OK) return st;
   for (int r = 0; r < h->R; ++r) {
-    if (cudaMemcpyAsync(h_out[r], h->staging + (size_t)(h->R + r) * per_rank, bytes,
+    if (cudaMemcpyAsync(h_out[r], h->staging + (size_t)(h->R + r) * per_rank * h->elem_bytes, bytes,
                         cudaMemcpyDeviceToHost, s) != cudaSuccess)
       return AR_ERR_CUDA;
   }

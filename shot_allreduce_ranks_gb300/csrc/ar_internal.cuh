@@ -1,6 +1,8 @@
 // Internal declarations shared by the library's CUDA translation units.
 // Device helpers are header-only (static inline) so no device linking is
-// needed; every kernel is instantiated for a compile-time rank count R.
+// needed; every kernel is instantiated for a compile-time rank count R and
+// element type E.  Data moves in 16-byte "groups": 8 bf16, 8 fp16 or 4 fp32
+// elements; an LL8 packet carries one 32-bit word of a group.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -11,7 +13,7 @@
 
 namespace ar {
 
-constexpr int kVecElems = 8;  // bf16 elements per 16-byte vector ("group")
+constexpr int kGroupBytes = 16;  // bytes per vector access ("group")
 
 // ---------------------------------------------------------------------------
 // Device-resident state of one handle (one per handle, 64 bytes).
@@ -31,10 +33,10 @@ enum DevError : uint32_t { kDevErrNone = 0, kDevErrTimeout = 1, kDevErrCopyTimeo
 
 // Everything a kernel needs about one call, passed by value.
 struct CallArgs {
-  const uint16_t* const* in_tbl;  // device array of R input pointers
-  uint16_t* const* out_tbl;       // device array of R output pointers
+  const char* const* in_tbl;      // device array of R input pointers
+  char* const* out_tbl;           // device array of R output pointers
   size_t count;                   // elements per rank
-  size_t groups;                  // ceil(count / 8)
+  size_t groups;                  // ceil(count / elements per group)
   size_t shard_groups;            // ceil(groups / R): groups owned by each rank
   DevState* state;                // the handle's state block (error word)
   uint64_t spin_limit_ns;         // bound of every device-side wait
@@ -67,7 +69,7 @@ constexpr size_t kRingProgressWords = (size_t)kMaxRingCtas * kMaxRingWarps;
 // 16-byte global accesses that bypass L1 allocation.  With kHint the access
 // carries an L2 cache policy (createpolicy) chosen by the caller.
 template <bool kHint = false>
-__device__ __forceinline__ uint4 ld_v4_stream(const uint16_t* p, uint64_t pol = 0) {
+__device__ __forceinline__ uint4 ld_v4_stream(const char* p, uint64_t pol = 0) {
   uint4 v;
   if (kHint) {
     asm volatile("ld.global.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
@@ -82,7 +84,7 @@ __device__ __forceinline__ uint4 ld_v4_stream(const uint16_t* p, uint64_t pol = 
 }
 
 template <bool kHint = false>
-__device__ __forceinline__ void st_v4_stream(uint16_t* p, uint4 v, uint64_t pol = 0) {
+__device__ __forceinline__ void st_v4_stream(char* p, uint4 v, uint64_t pol = 0) {
   if (kHint) {
     asm volatile("st.global.L1::no_allocate.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;" ::"l"(p),
                  "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol)
@@ -102,76 +104,70 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   return pol;
 }
 
-__device__ __forceinline__ uint16_t ld_u16(const uint16_t* p) {
-  unsigned short v;
-  asm volatile("ld.global.u16 %0, [%1];" : "=h"(v) : "l"(p));
-  return v;
-}
+// ---------------------------------------------------------------------------
+// Element types.  Each gives the elements per group, the element size, and
+// exact widening to fp32 / round-to-nearest-even narrowing from fp32 of one
+// element's bits.  Widening is exact for all three; fp32 is not rounded.
 
-__device__ __forceinline__ void st_u16(uint16_t* p, uint16_t v) {
-  asm volatile("st.global.u16 [%0], %1;" ::"l"(p), "h"((unsigned short)v) : "memory");
-}
-
-// Load group g (8 elements) of a buffer.  `valid` < 8 only for the last,
-// partial group; `vec` is false when some pointer of the call is not
-// 16-byte aligned.  Missing elements read as +0 (never stored back).
-template <bool kHint = false>
-__device__ __forceinline__ uint4 load_group(const uint16_t* base, size_t g, int valid, bool vec,
-                                            uint64_t pol = 0) {
-  const uint16_t* p = base + g * kVecElems;
-  if (vec && valid == kVecElems) return ld_v4_stream<kHint>(p, pol);
-  uint32_t w0 = 0u, w1 = 0u, w2 = 0u, w3 = 0u;
-#pragma unroll
-  for (int e = 0; e < kVecElems; ++e) {
-    if (e < valid) {
-      const uint32_t h = (uint32_t)ld_u16(p + e) << (16 * (e & 1));
-      if (e < 2) w0 |= h;
-      else if (e < 4) w1 |= h;
-      else if (e < 6) w2 |= h;
-      else w3 |= h;
-    }
-  }
-  return make_uint4(w0, w1, w2, w3);
-}
-
-template <bool kHint = false>
-__device__ __forceinline__ void store_group(uint16_t* base, size_t g, uint4 v, int valid, bool vec,
-                                            uint64_t pol = 0) {
-  uint16_t* p = base + g * kVecElems;
-  if (vec && valid == kVecElems) {
-    st_v4_stream<kHint>(p, v, pol);
-    return;
-  }
-#pragma unroll
-  for (int e = 0; e < kVecElems; ++e) {
-    if (e < valid) {
-      const uint32_t w = e < 2 ? v.x : e < 4 ? v.y : e < 6 ? v.z : v.w;
-      st_u16(p + e, (uint16_t)(w >> (16 * (e & 1))));
-    }
-  }
-}
-
-// bf16 -> fp32 is exact: the bf16 bits are the upper half of the fp32 word.
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-// Two fp32 -> one word of two bf16, each rounded to nearest even
-// (cvt.rn.bf16x2.f32 puts its first source in the upper half).
-__device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
+__device__ __forceinline__ uint32_t cvt_rn_bf16x2(float lo, float hi) {
   uint32_t d;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));  // first source -> upper half
   return d;
 }
 
-// Eight fp32 accumulators for one group.
-struct Acc8 {
+__device__ __forceinline__ uint32_t cvt_rn_f16x2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+__device__ __forceinline__ float cvt_f32_f16(uint32_t h) {
+  float f;
+  const unsigned short hs = (unsigned short)h;
+  asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"(hs));
+  return f;
+}
+
+struct Bf16 {
+  static constexpr int kGroup = 8;
+  static constexpr int kBytes = 2;
+  __device__ static float lo(uint32_t w) { return __uint_as_float(w << 16); }
+  __device__ static float hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+  __device__ static uint32_t pack(float lo, float hi) { return cvt_rn_bf16x2(lo, hi); }
+  __device__ static float to_f32(uint32_t bits) { return __uint_as_float(bits << 16); }
+  __device__ static uint32_t from_f32(float x) { return cvt_rn_bf16x2(x, 0.0f) & 0xFFFFu; }
+};
+
+struct F16 {
+  static constexpr int kGroup = 8;
+  static constexpr int kBytes = 2;
+  __device__ static float lo(uint32_t w) { return cvt_f32_f16(w & 0xFFFFu); }
+  __device__ static float hi(uint32_t w) { return cvt_f32_f16(w >> 16); }
+  __device__ static uint32_t pack(float lo, float hi) { return cvt_rn_f16x2(lo, hi); }
+  __device__ static float to_f32(uint32_t bits) { return cvt_f32_f16(bits); }
+  __device__ static uint32_t from_f32(float x) { return cvt_rn_f16x2(x, 0.0f) & 0xFFFFu; }
+};
+
+struct F32 {
+  static constexpr int kGroup = 4;
+  static constexpr int kBytes = 4;
+  __device__ static float to_f32(uint32_t bits) { return __uint_as_float(bits); }
+  __device__ static uint32_t from_f32(float x) { return __float_as_uint(x); }
+};
+
+// Accumulators for one group: the rank-order fp32 sum of its elements.
+template <class E>
+struct Acc;
+
+template <class E>
+struct AccHalf {  // bf16 / fp16: two elements per 32-bit word
   float v[8];
   __device__ __forceinline__ void set(uint4 x) {
     const uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      v[2 * k] = bf16_lo(w[k]);
-      v[2 * k + 1] = bf16_hi(w[k]);
+      v[2 * k] = E::lo(w[k]);
+      v[2 * k + 1] = E::hi(w[k]);
     }
   }
   // One rank-order step: acc = acc + x (plain fp32 add, round to nearest).
@@ -179,36 +175,131 @@ struct Acc8 {
     const uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      v[2 * k] = __fadd_rn(v[2 * k], bf16_lo(w[k]));
-      v[2 * k + 1] = __fadd_rn(v[2 * k + 1], bf16_hi(w[k]));
+      v[2 * k] = __fadd_rn(v[2 * k], E::lo(w[k]));
+      v[2 * k + 1] = __fadd_rn(v[2 * k + 1], E::hi(w[k]));
     }
   }
-  __device__ __forceinline__ uint4 round_bf16() const {
-    return make_uint4(pack_bf16x2_rn(v[0], v[1]), pack_bf16x2_rn(v[2], v[3]),
-                      pack_bf16x2_rn(v[4], v[5]), pack_bf16x2_rn(v[6], v[7]));
+  __device__ __forceinline__ uint4 round() const {
+    return make_uint4(E::pack(v[0], v[1]), E::pack(v[2], v[3]), E::pack(v[4], v[5]),
+                      E::pack(v[6], v[7]));
   }
 };
 
+template <>
+struct Acc<Bf16> : AccHalf<Bf16> {};
+template <>
+struct Acc<F16> : AccHalf<F16> {};
+
+template <>
+struct Acc<F32> {
+  float v[4];
+  __device__ __forceinline__ void set(uint4 x) {
+    v[0] = __uint_as_float(x.x);
+    v[1] = __uint_as_float(x.y);
+    v[2] = __uint_as_float(x.z);
+    v[3] = __uint_as_float(x.w);
+  }
+  __device__ __forceinline__ void add(uint4 x) {
+    v[0] = __fadd_rn(v[0], __uint_as_float(x.x));
+    v[1] = __fadd_rn(v[1], __uint_as_float(x.y));
+    v[2] = __fadd_rn(v[2], __uint_as_float(x.z));
+    v[3] = __fadd_rn(v[3], __uint_as_float(x.w));
+  }
+  __device__ __forceinline__ uint4 round() const {
+    return make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]),
+                      __float_as_uint(v[3]));
+  }
+};
+
+// One element's bits (2 or 4 bytes) at p.
+template <int kBytes>
+__device__ __forceinline__ uint32_t ld_elem(const char* p) {
+  if (kBytes == 2) {
+    unsigned short v;
+    asm volatile("ld.global.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
+  } else {
+    uint32_t v;
+    asm volatile("ld.global.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+  }
+}
+
+template <int kBytes>
+__device__ __forceinline__ void st_elem(char* p, uint32_t v) {
+  if (kBytes == 2) {
+    asm volatile("st.global.u16 [%0], %1;" ::"l"(p), "h"((unsigned short)v) : "memory");
+  } else {
+    asm volatile("st.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+  }
+}
+
+// Load group g (16 bytes) of a buffer.  `valid` < E::kGroup only for the
+// last, partial group; `vec` is false when some pointer of the call is not
+// 16-byte aligned.  Missing elements read as zero bits (never stored back).
+template <class E, bool kHint = false>
+__device__ __forceinline__ uint4 load_group(const char* base, size_t g, int valid, bool vec,
+                                            uint64_t pol = 0) {
+  const char* p = base + g * kGroupBytes;
+  if (vec && valid == E::kGroup) return ld_v4_stream<kHint>(p, pol);
+  uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int e = 0; e < E::kGroup; ++e) {
+    if (e < valid) {
+      const uint32_t bits = ld_elem<E::kBytes>(p + e * E::kBytes);
+      constexpr int per_word = 4 / E::kBytes;
+      const uint32_t h = bits << (8 * E::kBytes * (e % per_word));
+      if (e / per_word == 0) w[0] |= h;
+      else if (e / per_word == 1) w[1] |= h;
+      else if (e / per_word == 2) w[2] |= h;
+      else w[3] |= h;
+    }
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+template <class E, bool kHint = false>
+__device__ __forceinline__ void store_group(char* base, size_t g, uint4 v, int valid, bool vec,
+                                            uint64_t pol = 0) {
+  char* p = base + g * kGroupBytes;
+  if (vec && valid == E::kGroup) {
+    st_v4_stream<kHint>(p, v, pol);
+    return;
+  }
+#pragma unroll
+  for (int e = 0; e < E::kGroup; ++e) {
+    if (e < valid) {
+      constexpr int per_word = 4 / E::kBytes;
+      const int wi = e / per_word;
+      const uint32_t w = wi == 0 ? v.x : wi == 1 ? v.y : wi == 2 ? v.z : v.w;
+      const uint32_t bits =
+          E::kBytes == 4 ? w : (w >> (8 * E::kBytes * (e % per_word))) & 0xFFFFu;
+      st_elem<E::kBytes>(p + e * E::kBytes, bits);
+    }
+  }
+}
+
 // Number of valid elements in group g of a buffer of `count` elements.
+template <class E>
 __device__ __forceinline__ int group_valid(size_t g, size_t count) {
-  const size_t first = g * kVecElems;
+  const size_t first = g * E::kGroup;
   const size_t left = count - first;
-  return left >= (size_t)kVecElems ? kVecElems : (int)left;
+  return left >= (size_t)E::kGroup ? E::kGroup : (int)left;
 }
 
 // Copy the R input and output pointers of a call into shared memory, and
 // decide (CTA-uniformly) whether every pointer allows 16-byte vectors.
 template <int R>
-__device__ __forceinline__ bool load_tables(const CallArgs& a, const uint16_t** s_in, uint16_t** s_out) {
+__device__ __forceinline__ bool load_tables(const CallArgs& a, const char** s_in, char** s_out) {
   __shared__ int s_misaligned;
   if (threadIdx.x == 0) s_misaligned = 0;
   __syncthreads();
   if (threadIdx.x < R) {
-    const uint16_t* p = a.in_tbl[threadIdx.x];
+    const char* p = a.in_tbl[threadIdx.x];
     s_in[threadIdx.x] = p;
     if (reinterpret_cast<uintptr_t>(p) & 15u) atomicOr(&s_misaligned, 1);
   } else if (threadIdx.x < 2 * R) {
-    uint16_t* p = a.out_tbl[threadIdx.x - R];
+    char* p = a.out_tbl[threadIdx.x - R];
     s_out[threadIdx.x - R] = p;
     if (reinterpret_cast<uintptr_t>(p) & 15u) atomicOr(&s_misaligned, 1);
   }
@@ -230,52 +321,77 @@ struct LaunchCfg {
   int threads;
 };
 
-// Launchers (defined in the kernel translation units).  Each returns the
-// CUDA error of its launch(es).
-cudaError_t launch_oneshot_pull(int R, const CallArgs& a, LaunchCfg cfg, cudaStream_t s);
-cudaError_t launch_oneshot_fanout(int R, const CallArgs& a, LaunchCfg cfg, cudaStream_t s);
-cudaError_t launch_twophase(int R, const CallArgs& a, LaunchCfg cfg, cudaStream_t s);
-cudaError_t launch_fused_ll8(int R, const CallArgs& a, const FusedArgs& f, LaunchCfg cfg,
-                             cudaStream_t s);
-cudaError_t launch_fused_ll8_staged(int R, const CallArgs& a, const FusedArgs& f, LaunchCfg cfg,
-                                    cudaStream_t s);
-cudaError_t launch_packet_3op(int R, const CallArgs& a, const FusedArgs& f, LaunchCfg cfg,
-                              cudaStream_t s);
-int fused_staged_ctas_per_sm(int R, int threads);
-cudaError_t launch_fused_ll8_ring(int R, const CallArgs& a, const FusedArgs& f, LaunchCfg cfg,
+// Launchers (defined in the kernel translation units).  `dtype` is an
+// ar_dtype_t; each returns the CUDA error of its launch(es).
+cudaError_t launch_oneshot_pull(int R, int dtype, const CallArgs& a, LaunchCfg cfg, cudaStream_t s);
+cudaError_t launch_oneshot_fanout(int R, int dtype, const CallArgs& a, LaunchCfg cfg,
                                   cudaStream_t s);
-int fused_ring_ctas_per_sm(int R, int threads);
+cudaError_t launch_twophase(int R, int dtype, const CallArgs& a, LaunchCfg cfg, cudaStream_t s);
+cudaError_t launch_fused_ll8(int R, int dtype, const CallArgs& a, const FusedArgs& f,
+                             LaunchCfg cfg, cudaStream_t s);
+cudaError_t launch_fused_ll8_staged(int R, int dtype, const CallArgs& a, const FusedArgs& f,
+                                    LaunchCfg cfg, cudaStream_t s);
+cudaError_t launch_packet_3op(int R, int dtype, const CallArgs& a, const FusedArgs& f,
+                              LaunchCfg cfg, cudaStream_t s);
+cudaError_t launch_fused_ll8_ring(int R, int dtype, const CallArgs& a, const FusedArgs& f,
+                                  LaunchCfg cfg, cudaStream_t s);
 // Reduce-scatter / all-gather (k_rs_ag.cu): a.count is the block length;
 // the grid is (cfg.ctas, R).
-cudaError_t launch_reduce_scatter(int R, const CallArgs& a, LaunchCfg cfg, cudaStream_t s);
-cudaError_t launch_all_gather(int R, const CallArgs& a, LaunchCfg cfg, cudaStream_t s);
+cudaError_t launch_reduce_scatter(int R, int dtype, const CallArgs& a, LaunchCfg cfg,
+                                  cudaStream_t s);
+cudaError_t launch_all_gather(int R, int dtype, const CallArgs& a, LaunchCfg cfg, cudaStream_t s);
 
-// Occupancy (CTAs per SM) of the fused and fan-out kernels for R ranks and
+// Occupancy (CTAs per SM) of the grid-sized kernels for R ranks, dtype and
 // `threads` threads per CTA.
-int fused_ctas_per_sm(int R, int threads);
-int fanout_ctas_per_sm(int R, int threads);
+int fused_ctas_per_sm(int R, int dtype, int threads);
+int fused_staged_ctas_per_sm(int R, int dtype, int threads);
+int fused_ring_ctas_per_sm(int R, int dtype, int threads);
+int fanout_ctas_per_sm(int R, int dtype, int threads);
 
 // Bulk-copy fan-out (k_oneshot_bulk.cu): fixed 256 threads per CTA, dynamic
 // shared memory per CTA, CTAs per SM, and a one-time attribute set-up.
 constexpr int kBulkThreads = 256;
 size_t bulk_smem_bytes(int R);
-int bulk_ctas_per_sm(int R);
-cudaError_t bulk_prepare(int R);
-cudaError_t launch_oneshot_fanout_bulk(int R, const CallArgs& a, int ctas, cudaStream_t s);
+int bulk_ctas_per_sm(int R, int dtype);
+cudaError_t bulk_prepare(int R, int dtype);
+cudaError_t launch_oneshot_fanout_bulk(int R, int dtype, const CallArgs& a, int ctas,
+                                       cudaStream_t s);
+
+// Elements per 16-byte group of an ar_dtype_t (0 for an unknown one).
+inline int group_elems(int dtype) {
+  return dtype == AR_FP32 ? 4 : (dtype == AR_BF16 || dtype == AR_FP16) ? 8 : 0;
+}
 
 }  // namespace ar
 
-// Expands CALL(1) .. CALL(8) on a runtime rank count inside a launcher that
-// returns cudaError_t.
-#define AR_RANK_SWITCH(R, CALL)            \
-  switch (R) {                             \
-    case 1: CALL(1); break;                \
-    case 2: CALL(2); break;                \
-    case 3: CALL(3); break;                \
-    case 4: CALL(4); break;                \
-    case 5: CALL(5); break;                \
-    case 6: CALL(6); break;                \
-    case 7: CALL(7); break;                \
-    case 8: CALL(8); break;                \
-    default: return cudaErrorInvalidValue; \
+// Dispatch on a runtime (R, dtype) to CALL(RR, EE) with RR a compile-time
+// rank count and EE an element type, inside a function returning
+// cudaError_t (an unsupported pair returns cudaErrorInvalidValue).
+#define AR_R_CASE(CALL, EE, RR) \
+  case RR:                      \
+    CALL(RR, EE);               \
+    break;
+#define AR_SWITCH_R8(R, CALL, EE)                                                           \
+  switch (R) {                                                                            \
+    AR_R_CASE(CALL, EE, 1) AR_R_CASE(CALL, EE, 2) AR_R_CASE(CALL, EE, 3)                  \
+    AR_R_CASE(CALL, EE, 4) AR_R_CASE(CALL, EE, 5) AR_R_CASE(CALL, EE, 6)                  \
+    AR_R_CASE(CALL, EE, 7) AR_R_CASE(CALL, EE, 8)                                         \
+    default: return cudaErrorInvalidValue;                                                \
+  }
+#define AR_SWITCH_R16(R, CALL, EE)                                                          \
+  switch (R) {                                                                            \
+    AR_R_CASE(CALL, EE, 1) AR_R_CASE(CALL, EE, 2) AR_R_CASE(CALL, EE, 3)                  \
+    AR_R_CASE(CALL, EE, 4) AR_R_CASE(CALL, EE, 5) AR_R_CASE(CALL, EE, 6)                  \
+    AR_R_CASE(CALL, EE, 7) AR_R_CASE(CALL, EE, 8) AR_R_CASE(CALL, EE, 9)                  \
+    AR_R_CASE(CALL, EE, 10) AR_R_CASE(CALL, EE, 11) AR_R_CASE(CALL, EE, 12)               \
+    AR_R_CASE(CALL, EE, 13) AR_R_CASE(CALL, EE, 14) AR_R_CASE(CALL, EE, 15)               \
+    AR_R_CASE(CALL, EE, 16)                                                               \
+    default: return cudaErrorInvalidValue;                                                \
+  }
+#define AR_DISPATCH(DT, R, CALL, SWITCH)          \
+  switch (DT) {                                   \
+    case AR_BF16: SWITCH(R, CALL, ::ar::Bf16) break; \
+    case AR_FP16: SWITCH(R, CALL, ::ar::F16) break;  \
+    case AR_FP32: SWITCH(R, CALL, ::ar::F32) break;  \
+    default: return cudaErrorInvalidValue;        \
   }

@@ -149,7 +149,7 @@ __device__ __forceinline__ Lane make_lane(const CallArgs& a, uint32_t epoch, boo
 // call's epoch read once by thread 0 and shared with the CTA.
 template <int R>
 __device__ __forceinline__ Lane packet_prologue(const CallArgs& a, const FusedArgs& f,
-                                                const uint16_t** s_in, uint16_t** s_out) {
+                                                const char** s_in, char** s_out) {
   __shared__ uint32_t s_epoch;
   const bool vec = load_tables<R>(a, s_in, s_out);
   if (threadIdx.x == 0) s_epoch = ld_relaxed_u32(&f.state->epoch);
@@ -208,9 +208,9 @@ __device__ __forceinline__ bool wait_packets(const FusedArgs& f, uint64_t* regio
 // ---- scatter: rank r's slices of every other owner's shard, as packets ----
 // Two groups (j, j + tstride) per iteration: all 2(R-1) loads are issued
 // before the first packet store.
-template <int R>
+template <int R, class E>
 __device__ __forceinline__ void phase_scatter(const CallArgs& a, const FusedArgs& f, const Lane& l,
-                                              const uint16_t* my_in) {
+                                              const char* my_in) {
   if constexpr (R == 1) return;
   if (l.r == f.skip_producer) return;
   for (size_t j = l.t0; j < l.Vs; j += 2 * l.tstride) {
@@ -221,10 +221,10 @@ __device__ __forceinline__ void phase_scatter(const CallArgs& a, const FusedArgs
       const int o = (l.r + k) % R;
       const size_t g = (size_t)o * l.Vs + j;
       if (g < a.groups)
-        x[k - 1] = load_group<true>(my_in, g, group_valid(g, a.count), l.vec, l.pol_in);
+        x[k - 1] = load_group<E, true>(my_in, g, group_valid<E>(g, a.count), l.vec, l.pol_in);
       const size_t g2 = (size_t)o * l.Vs + j2;
       if (j2 < l.Vs && g2 < a.groups)
-        y[k - 1] = load_group<true>(my_in, g2, group_valid(g2, a.count), l.vec, l.pol_in);
+        y[k - 1] = load_group<E, true>(my_in, g2, group_valid<E>(g2, a.count), l.vec, l.pol_in);
     }
 #pragma unroll
     for (int k = 1; k < R; ++k) {
@@ -244,15 +244,15 @@ __device__ __forceinline__ void phase_scatter(const CallArgs& a, const FusedArgs
 // group into all R outputs.  Otherwise: store it into out_r only and send it
 // as result packets to every other rank's result slot for owner r.
 // Returns false if the call was abandoned after a timeout.
-template <int R, bool kWriteMode>
+template <int R, class E, bool kWriteMode>
 __device__ __forceinline__ bool phase_reduce(const CallArgs& a, const FusedArgs& f, const Lane& l,
-                                             const uint16_t* my_in, uint16_t* const* s_out) {
+                                             const char* my_in, char* const* s_out) {
   const size_t g0 = (size_t)l.r * l.Vs;
   const size_t n = g0 < a.groups ? min(l.Vs, a.groups - g0) : 0;
   for (size_t j = l.t0; j < n; j += l.tstride) {
     const size_t g = g0 + j;
-    const int valid = group_valid(g, a.count);
-    const uint4 own = load_group<true>(my_in, g, valid, l.vec, l.pol_in);
+    const int valid = group_valid<E>(g, a.count);
+    const uint4 own = load_group<E, true>(my_in, g, valid, l.vec, l.pol_in);
     Packets4 pk[R];
     uint32_t pending = 0;
 #pragma unroll
@@ -263,16 +263,16 @@ __device__ __forceinline__ bool phase_reduce(const CallArgs& a, const FusedArgs&
       }
     const bool ok = wait_packets<R>(f, f.scratch, l.r, j, pk, pending, l.epoch);
     if (!ok) return false;
-    Acc8 acc;
+    Acc<E> acc;
     acc.set(l.r == 0 ? own : pk[0].data());
 #pragma unroll
     for (int s = 1; s < R; ++s) acc.add(s == l.r ? own : pk[s].data());
-    const uint4 y = acc.round_bf16();
+    const uint4 y = acc.round();
     if (kWriteMode) {
 #pragma unroll
-      for (int q = 0; q < R; ++q) store_group(s_out[q], g, y, valid, l.vec);
+      for (int q = 0; q < R; ++q) store_group<E>(s_out[q], g, y, valid, l.vec);
     } else {
-      store_group(s_out[l.r], g, y, valid, l.vec);
+      store_group<E>(s_out[l.r], g, y, valid, l.vec);
 #pragma unroll
       for (int q = 0; q < R; ++q)
         if (q != l.r) st_packets(slot_ptr<R>(f.rscratch, f.slot_groups, q, l.r) + j * 4, y, l.epoch);
@@ -283,11 +283,11 @@ __device__ __forceinline__ bool phase_reduce(const CallArgs& a, const FusedArgs&
 
 // ---- receive: rank r copies every other owner's reduced shard out of its
 // result slots into out_r (the staged variants' last step) -------------------
-template <int R>
+template <int R, class E>
 __device__ __forceinline__ bool phase_recv(const CallArgs& a, const FusedArgs& f, const Lane& l,
-                                           uint16_t* const* s_out) {
+                                           char* const* s_out) {
   if constexpr (R == 1) return true;
-  uint16_t* my_out = s_out[l.r];
+  char* my_out = s_out[l.r];
   for (size_t j = l.t0; j < l.Vs; j += l.tstride) {
     Packets4 pk[R];
     uint32_t pending = 0;
@@ -303,7 +303,7 @@ __device__ __forceinline__ bool phase_recv(const CallArgs& a, const FusedArgs& f
     for (int o = 0; o < R; ++o)
       if (present & (1u << o)) {
         const size_t g = (size_t)o * l.Vs + j;
-        store_group(my_out, g, pk[o].data(), group_valid(g, a.count), l.vec);
+        store_group<E>(my_out, g, pk[o].data(), group_valid<E>(g, a.count), l.vec);
       }
   }
   return true;
@@ -338,53 +338,53 @@ __device__ __forceinline__ void epoch_advance(const FusedArgs& f, uint32_t epoch
 }
 
 // Write mode: scatter -> reduce -> broadcast straight into all R outputs.
-template <int R>
+template <int R, class E>
 __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, FusedArgs f) {
-  __shared__ const uint16_t* s_in[R];
-  __shared__ uint16_t* s_out[R];
+  __shared__ const char* s_in[R];
+  __shared__ char* s_out[R];
   const Lane l = packet_prologue<R>(a, f, s_in, s_out);
-  phase_scatter<R>(a, f, l, s_in[l.r]);
-  phase_reduce<R, true>(a, f, l, s_in[l.r], s_out);
+  phase_scatter<R, E>(a, f, l, s_in[l.r]);
+  phase_reduce<R, E, true>(a, f, l, s_in[l.r], s_out);
   epoch_advance(f, l.epoch);
 }
 
 // Without write mode (the packet broadcast of the ARK page): scatter ->
 // reduce -> result packets to every rank -> every rank copies them out.
-template <int R>
+template <int R, class E>
 __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8_staged(CallArgs a, FusedArgs f) {
-  __shared__ const uint16_t* s_in[R];
-  __shared__ uint16_t* s_out[R];
+  __shared__ const char* s_in[R];
+  __shared__ char* s_out[R];
   const Lane l = packet_prologue<R>(a, f, s_in, s_out);
-  phase_scatter<R>(a, f, l, s_in[l.r]);
-  if (phase_reduce<R, false>(a, f, l, s_in[l.r], s_out)) phase_recv<R>(a, f, l, s_out);
+  phase_scatter<R, E>(a, f, l, s_in[l.r]);
+  if (phase_reduce<R, E, false>(a, f, l, s_in[l.r], s_out)) phase_recv<R, E>(a, f, l, s_out);
   epoch_advance(f, l.epoch);
 }
 
 // The three-launch decomposition the ARK page replaced (send_packet ->
 // recv_reduce_send_packet -> recv_packet): the same phases, one kernel each,
 // ordered by kernel boundaries instead of by co-residency.
-template <int R>
+template <int R, class E>
 __global__ void __launch_bounds__(kFusedMaxThreads) k_packet_send(CallArgs a, FusedArgs f) {
-  __shared__ const uint16_t* s_in[R];
-  __shared__ uint16_t* s_out[R];
+  __shared__ const char* s_in[R];
+  __shared__ char* s_out[R];
   const Lane l = packet_prologue<R>(a, f, s_in, s_out);
-  phase_scatter<R>(a, f, l, s_in[l.r]);
+  phase_scatter<R, E>(a, f, l, s_in[l.r]);
 }
 
-template <int R>
+template <int R, class E>
 __global__ void __launch_bounds__(kFusedMaxThreads) k_packet_reduce_send(CallArgs a, FusedArgs f) {
-  __shared__ const uint16_t* s_in[R];
-  __shared__ uint16_t* s_out[R];
+  __shared__ const char* s_in[R];
+  __shared__ char* s_out[R];
   const Lane l = packet_prologue<R>(a, f, s_in, s_out);
-  phase_reduce<R, false>(a, f, l, s_in[l.r], s_out);
+  phase_reduce<R, E, false>(a, f, l, s_in[l.r], s_out);
 }
 
-template <int R>
+template <int R, class E>
 __global__ void __launch_bounds__(kFusedMaxThreads) k_packet_recv(CallArgs a, FusedArgs f) {
-  __shared__ const uint16_t* s_in[R];
-  __shared__ uint16_t* s_out[R];
+  __shared__ const char* s_in[R];
+  __shared__ char* s_out[R];
   const Lane l = packet_prologue<R>(a, f, s_in, s_out);
-  phase_recv<R>(a, f, l, s_out);
+  phase_recv<R, E>(a, f, l, s_out);
   epoch_advance(f, l.epoch);
 }
 
@@ -458,10 +458,10 @@ __device__ __noinline__ bool wait_credit(const FusedArgs& f, const uint32_t* pp,
   return true;
 }
 
-template <int R>
+template <int R, class E>
 __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8_ring(CallArgs a, FusedArgs f) {
-  __shared__ const uint16_t* s_in[R];
-  __shared__ uint16_t* s_out[R];
+  __shared__ const char* s_in[R];
+  __shared__ char* s_out[R];
   const Lane l = packet_prologue<R>(a, f, s_in, s_out);
   const int T = blockDim.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int C = (int)(gridDim.x / R), c = (int)(blockIdx.x / R), r = l.r;
@@ -469,7 +469,7 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8_ring(CallArgs a,
   const size_t Vs = l.Vs;
   const size_t per_round = (size_t)C * T;
   const size_t K = (Vs + per_round - 1) / per_round;  // rounds of this call
-  const uint16_t* my_in = s_in[r];
+  const char* my_in = s_in[r];
   const size_t g0 = (size_t)r * Vs;  // first group of my shard
   const size_t my_n = g0 < a.groups ? min(Vs, a.groups - g0) : 0;
   // Thread t of producer CTA (s, c) writes exactly the ring slots that
@@ -498,7 +498,7 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8_ring(CallArgs a,
       for (int q = 1; q < R; ++q) {
         const int o = (r + q) % R;
         const size_t g = (size_t)o * Vs + jk;
-        if (g < a.groups) x[q - 1] = load_group<true>(my_in, g, group_valid(g, a.count), l.vec, l.pol_in);
+        if (g < a.groups) x[q - 1] = load_group<E, true>(my_in, g, group_valid<E>(g, a.count), l.vec, l.pol_in);
       }
     }
     const size_t jp = jk - per_round;  // my group of round k-1 (valid when k >= 1)
@@ -508,7 +508,7 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8_ring(CallArgs a,
     uint4 own = make_uint4(0, 0, 0, 0);
     uint32_t pending = 0;
     if (reduce) {
-      own = load_group<true>(my_in, g0 + jp, group_valid(g0 + jp, a.count), l.vec, l.pol_in);
+      own = load_group<E, true>(my_in, g0 + jp, group_valid<E>(g0 + jp, a.count), l.vec, l.pol_in);
 #pragma unroll
       for (int s = 0; s < R; ++s)
         if (s != r) {
@@ -535,15 +535,15 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8_ring(CallArgs a,
         return ring_slot<R>(f, r, s, c, C, pp, tid, T);
       });
       if (ok) {
-        Acc8 acc;
+        Acc<E> acc;
         acc.set(r == 0 ? own : pk[0].data());
 #pragma unroll
         for (int s = 1; s < R; ++s) acc.add(s == r ? own : pk[s].data());
-        const uint4 y = acc.round_bf16();
+        const uint4 y = acc.round();
         const size_t g = g0 + jp;
-        const int valid = group_valid(g, a.count);
+        const int valid = group_valid<E>(g, a.count);
 #pragma unroll
-        for (int q = 0; q < R; ++q) store_group(s_out[q], g, y, valid, l.vec);
+        for (int q = 0; q < R; ++q) store_group<E>(s_out[q], g, y, valid, l.vec);
       }
     }
     // Every lane of the warp is done reading ring slot pp: publish it.
@@ -556,126 +556,103 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8_ring(CallArgs a,
 
 }  // namespace
 
-int fused_ring_ctas_per_sm(int R, int threads) {
-  int n = 0;
-  cudaError_t e = cudaErrorInvalidValue;
-#define Q(RR) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_fused_ll8_ring<RR>, threads, 0)
-  switch (R) {
-    case 1: Q(1); break;
-    case 2: Q(2); break;
-    case 3: Q(3); break;
-    case 4: Q(4); break;
-    case 5: Q(5); break;
-    case 6: Q(6); break;
-    case 7: Q(7); break;
-    case 8: Q(8); break;
-    default: return 0;
-  }
-#undef Q
-  return e == cudaSuccess ? n : 0;
-}
+namespace {
 
-cudaError_t launch_fused_ll8_ring(int R, const CallArgs& a, const FusedArgs& f, LaunchCfg cfg,
-                                  cudaStream_t s) {
-  cudaLaunchConfig_t lc = {};
-  lc.gridDim = dim3((unsigned)cfg.ctas);
-  lc.blockDim = dim3((unsigned)cfg.threads);
-  lc.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  lc.attrs = attr;
-  lc.numAttrs = 1;
-#define L(RR) return cudaLaunchKernelEx(&lc, k_fused_ll8_ring<RR>, a, f)
-  AR_RANK_SWITCH(R, L)
-#undef L
-  return cudaErrorInvalidValue;
-}
-
-int fused_ctas_per_sm(int R, int threads) {
-  int n = 0;
-  cudaError_t e = cudaErrorInvalidValue;
-#define Q(RR) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_fused_ll8<RR>, threads, 0)
-  switch (R) {
-    case 1: Q(1); break;
-    case 2: Q(2); break;
-    case 3: Q(3); break;
-    case 4: Q(4); break;
-    case 5: Q(5); break;
-    case 6: Q(6); break;
-    case 7: Q(7); break;
-    case 8: Q(8); break;
-    default: return 0;
-  }
-#undef Q
-  return e == cudaSuccess ? n : 0;
-}
-
-cudaError_t launch_fused_ll8_staged(int R, const CallArgs& a, const FusedArgs& f, LaunchCfg cfg,
-                                    cudaStream_t s) {
-  cudaLaunchConfig_t lc = {};
-  lc.gridDim = dim3((unsigned)cfg.ctas);
-  lc.blockDim = dim3((unsigned)cfg.threads);
-  lc.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  lc.attrs = attr;
-  lc.numAttrs = 1;
-#define L(RR) return cudaLaunchKernelEx(&lc, k_fused_ll8_staged<RR>, a, f)
-  AR_RANK_SWITCH(R, L)
-#undef L
-  return cudaErrorInvalidValue;
-}
-
-cudaError_t launch_packet_3op(int R, const CallArgs& a, const FusedArgs& f, LaunchCfg cfg,
-                              cudaStream_t s) {
-  cudaError_t e = cudaSuccess;
-#define L(RR)                                                                  \
-  k_packet_send<RR><<<cfg.ctas, cfg.threads, 0, s>>>(a, f);                    \
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;                       \
-  k_packet_reduce_send<RR><<<cfg.ctas, cfg.threads, 0, s>>>(a, f);             \
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;                       \
-  k_packet_recv<RR><<<cfg.ctas, cfg.threads, 0, s>>>(a, f);                    \
-  return cudaGetLastError()
-  AR_RANK_SWITCH(R, L)
-#undef L
-  return cudaErrorInvalidValue;
-}
-
-int fused_staged_ctas_per_sm(int R, int threads) {
-  int n = 0;
-  cudaError_t e = cudaErrorInvalidValue;
-#define Q(RR) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_fused_ll8_staged<RR>, threads, 0)
-  switch (R) {
-    case 1: Q(1); break;
-    case 2: Q(2); break;
-    case 3: Q(3); break;
-    case 4: Q(4); break;
-    case 5: Q(5); break;
-    case 6: Q(6); break;
-    case 7: Q(7); break;
-    case 8: Q(8); break;
-    default: return 0;
-  }
-#undef Q
-  return e == cudaSuccess ? n : 0;
-}
-
-cudaError_t launch_fused_ll8(int R, const CallArgs& a, const FusedArgs& f, LaunchCfg cfg,
-                             cudaStream_t s) {
+cudaLaunchConfig_t cooperative_config(LaunchCfg cfg, cudaStream_t s, cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3((unsigned)cfg.ctas);
   lc.blockDim = dim3((unsigned)cfg.threads);
   lc.dynamicSmemBytes = 0;
   lc.stream = s;
-  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
   lc.attrs = attr;
   lc.numAttrs = 1;
-#define L(RR) return cudaLaunchKernelEx(&lc, k_fused_ll8<RR>, a, f)
-  AR_RANK_SWITCH(R, L)
+  return lc;
+}
+
+cudaError_t occ_fused(int R, int dtype, int threads, int* n) {
+#define Q(RR, EE) \
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, k_fused_ll8<RR, EE>, threads, 0)
+  AR_DISPATCH(dtype, R, Q, AR_SWITCH_R8)
+#undef Q
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t occ_staged(int R, int dtype, int threads, int* n) {
+#define Q(RR, EE) \
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, k_fused_ll8_staged<RR, EE>, threads, 0)
+  AR_DISPATCH(dtype, R, Q, AR_SWITCH_R8)
+#undef Q
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t occ_ring(int R, int dtype, int threads, int* n) {
+#define Q(RR, EE) \
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, k_fused_ll8_ring<RR, EE>, threads, 0)
+  AR_DISPATCH(dtype, R, Q, AR_SWITCH_R8)
+#undef Q
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+int fused_ctas_per_sm(int R, int dtype, int threads) {
+  int n = 0;
+  return occ_fused(R, dtype, threads, &n) == cudaSuccess ? n : 0;
+}
+
+int fused_staged_ctas_per_sm(int R, int dtype, int threads) {
+  int n = 0;
+  return occ_staged(R, dtype, threads, &n) == cudaSuccess ? n : 0;
+}
+
+int fused_ring_ctas_per_sm(int R, int dtype, int threads) {
+  int n = 0;
+  return occ_ring(R, dtype, threads, &n) == cudaSuccess ? n : 0;
+}
+
+cudaError_t launch_fused_ll8(int R, int dtype, const CallArgs& a, const FusedArgs& f,
+                             LaunchCfg cfg, cudaStream_t s) {
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t lc = cooperative_config(cfg, s, attr);
+#define L(RR, EE) return cudaLaunchKernelEx(&lc, k_fused_ll8<RR, EE>, a, f)
+  AR_DISPATCH(dtype, R, L, AR_SWITCH_R8)
+#undef L
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_fused_ll8_staged(int R, int dtype, const CallArgs& a, const FusedArgs& f,
+                                    LaunchCfg cfg, cudaStream_t s) {
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t lc = cooperative_config(cfg, s, attr);
+#define L(RR, EE) return cudaLaunchKernelEx(&lc, k_fused_ll8_staged<RR, EE>, a, f)
+  AR_DISPATCH(dtype, R, L, AR_SWITCH_R8)
+#undef L
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_fused_ll8_ring(int R, int dtype, const CallArgs& a, const FusedArgs& f,
+                                  LaunchCfg cfg, cudaStream_t s) {
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t lc = cooperative_config(cfg, s, attr);
+#define L(RR, EE) return cudaLaunchKernelEx(&lc, k_fused_ll8_ring<RR, EE>, a, f)
+  AR_DISPATCH(dtype, R, L, AR_SWITCH_R8)
+#undef L
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_packet_3op(int R, int dtype, const CallArgs& a, const FusedArgs& f,
+                              LaunchCfg cfg, cudaStream_t s) {
+  cudaError_t e = cudaSuccess;
+#define L(RR, EE)                                                       \
+  k_packet_send<RR, EE><<<cfg.ctas, cfg.threads, 0, s>>>(a, f);         \
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;                \
+  k_packet_reduce_send<RR, EE><<<cfg.ctas, cfg.threads, 0, s>>>(a, f);  \
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;                \
+  k_packet_recv<RR, EE><<<cfg.ctas, cfg.threads, 0, s>>>(a, f);         \
+  return cudaGetLastError()
+  AR_DISPATCH(dtype, R, L, AR_SWITCH_R8)
 #undef L
   return cudaErrorInvalidValue;
 }
@@ -703,7 +680,7 @@ struct NoAllocDevice {
   uint64_t* scratch;     // device address of g_noalloc_scratch on this device
   ar::DevState* state;   // device address of g_noalloc_state on this device
   int sms;
-  int ctas_per_sm[AR_MAX_RANKS + 1];
+  int ctas_per_sm[AR_MAX_PACKET_RANKS + 1];
 };
 
 NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
@@ -735,7 +712,7 @@ ar_status_t noalloc_setup(int dev, int R, NoAllocDevice* out) {
     d.sms = sms;
     d.ready = true;
   }
-  if (d.ctas_per_sm[R] == 0) d.ctas_per_sm[R] = ar::fused_ctas_per_sm(R, kNoAllocThreads);
+  if (d.ctas_per_sm[R] == 0) d.ctas_per_sm[R] = ar::fused_ctas_per_sm(R, AR_BF16, kNoAllocThreads);
   *out = d;
   return AR_OK;
 }
@@ -745,7 +722,7 @@ ar_status_t noalloc_setup(int dev, int R, NoAllocDevice* out) {
 extern "C" ar_status_t ar_allreduce_fused_noalloc(int R, const void* const* d_in_tbl,
                                                   void* const* d_out_tbl, size_t count,
                                                   void* stream) {
-  if (R < 1 || R > AR_MAX_RANKS || !d_in_tbl || !d_out_tbl) return AR_ERR_INVALID_ARG;
+  if (R < 1 || R > AR_MAX_PACKET_RANKS || !d_in_tbl || !d_out_tbl) return AR_ERR_INVALID_ARG;
   if (count == 0) return AR_OK;
   if (count > AR_NOALLOC_MAX_COUNT(R)) return AR_ERR_INVALID_ARG;
   int dev = -1;
@@ -757,10 +734,10 @@ extern "C" ar_status_t ar_allreduce_fused_noalloc(int R, const void* const* d_in
   if (d.ctas_per_sm[R] <= 0) return AR_ERR_CUDA;
 
   ar::CallArgs a;
-  a.in_tbl = reinterpret_cast<const uint16_t* const*>(d_in_tbl);
-  a.out_tbl = reinterpret_cast<uint16_t* const*>(d_out_tbl);
+  a.in_tbl = reinterpret_cast<const char* const*>(d_in_tbl);
+  a.out_tbl = reinterpret_cast<char* const*>(d_out_tbl);
   a.count = count;
-  a.groups = (count + ar::kVecElems - 1) / ar::kVecElems;
+  a.groups = (count + 7) / 8;  // bf16: 8 elements per 16-byte group
   a.shard_groups = (a.groups + (size_t)R - 1) / (size_t)R;
   a.state = d.state;
   a.spin_limit_ns = 100ull * 1000ull * 1000ull;
@@ -777,7 +754,8 @@ extern "C" ar_status_t ar_allreduce_fused_noalloc(int R, const void* const* d_in
   size_t per_rank = (a.shard_groups + kNoAllocThreads - 1) / kNoAllocThreads;
   per_rank = std::max<size_t>(1, std::min(per_rank, limit));
   ar::LaunchCfg cfg = {(int)(per_rank * (size_t)R), kNoAllocThreads};
-  return ar::launch_fused_ll8(R, a, f, cfg, static_cast<cudaStream_t>(stream)) == cudaSuccess
+  return ar::launch_fused_ll8(R, AR_BF16, a, f, cfg, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
              ? AR_OK
              : AR_ERR_CUDA;
 }

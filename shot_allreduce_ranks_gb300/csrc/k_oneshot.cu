@@ -8,69 +8,73 @@
 //              one chunk run together and share its lines in L2.
 //  * fanout -- the same read, combined with the write mode of "optimize
 //              allreduce write mode by broadcast output ptr" (ROCm/aiter
-//              #1910, Motivation): one thread reads the 8-element group of
-//              every rank once, reduces it, and stores the result into all R
-//              outputs through the output-pointer table.  4*R*N bytes move,
-//              the minimum for this operation.
+//              #1910, Motivation): one thread reads a 16-byte group of every
+//              rank once, reduces it, and stores the result into all R
+//              outputs through the output-pointer table.  4*R*N bytes move
+//              for 2-byte elements (8*R*N for fp32), the minimum.
 //
 // Both handle any count (the last group may be partial) and fall back to
-// 2-byte accesses for a call whose pointers are not all 16-byte aligned.
+// element-sized accesses for a call whose pointers are not all 16-byte
+// aligned.
 #include "ar_internal.cuh"
 
 namespace ar {
 namespace {
 
-template <int R>
-__device__ __forceinline__ uint4 reduce_group(const uint16_t* const* s_in, size_t g, int valid,
+template <int R, class E>
+__device__ __forceinline__ uint4 reduce_group(const char* const* s_in, size_t g, int valid,
                                               bool vec) {
   uint4 x[R];
 #pragma unroll
-  for (int s = 0; s < R; ++s) x[s] = load_group(s_in[s], g, valid, vec);
-  Acc8 acc;
+  for (int s = 0; s < R; ++s) x[s] = load_group<E>(s_in[s], g, valid, vec);
+  Acc<E> acc;
   acc.set(x[0]);
 #pragma unroll
   for (int s = 1; s < R; ++s) acc.add(x[s]);
-  return acc.round_bf16();
+  return acc.round();
 }
 
-// Grid-stride over groups, two groups (g, g + stride) per iteration so that
-// 2R independent 16-byte loads are in flight per thread before any store.
-template <int R>
+// Grid-stride over groups, two groups (g, g + stride) per iteration for
+// R <= 8 so that 2R independent 16-byte loads are in flight per thread
+// before any store; one group per iteration above 8 ranks (registers).
+template <int R, class E>
 __global__ void __launch_bounds__(512) k_oneshot_fanout(CallArgs a) {
-  __shared__ const uint16_t* s_in[R];
-  __shared__ uint16_t* s_out[R];
+  __shared__ const char* s_in[R];
+  __shared__ char* s_out[R];
   const bool vec = load_tables<R>(a, s_in, s_out);
   const size_t stride = (size_t)gridDim.x * blockDim.x;
   size_t g = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  for (; g + stride < a.groups; g += 2 * stride) {
-    const size_t g2 = g + stride;
-    const int valid2 = group_valid(g2, a.count);
-    uint4 x[R], y[R];
+  if constexpr (R <= 8) {
+    for (; g + stride < a.groups; g += 2 * stride) {
+      const size_t g2 = g + stride;
+      const int valid2 = group_valid<E>(g2, a.count);
+      uint4 x[R], y[R];
 #pragma unroll
-    for (int s = 0; s < R; ++s) {
-      x[s] = load_group(s_in[s], g, kVecElems, vec);
-      y[s] = load_group(s_in[s], g2, valid2, vec);
-    }
-    Acc8 ax, ay;
-    ax.set(x[0]);
-    ay.set(y[0]);
+      for (int s = 0; s < R; ++s) {
+        x[s] = load_group<E>(s_in[s], g, E::kGroup, vec);
+        y[s] = load_group<E>(s_in[s], g2, valid2, vec);
+      }
+      Acc<E> ax, ay;
+      ax.set(x[0]);
+      ay.set(y[0]);
 #pragma unroll
-    for (int s = 1; s < R; ++s) {
-      ax.add(x[s]);
-      ay.add(y[s]);
-    }
-    const uint4 rx = ax.round_bf16(), ry = ay.round_bf16();
+      for (int s = 1; s < R; ++s) {
+        ax.add(x[s]);
+        ay.add(y[s]);
+      }
+      const uint4 rx = ax.round(), ry = ay.round();
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-      store_group(s_out[r], g, rx, kVecElems, vec);
-      store_group(s_out[r], g2, ry, valid2, vec);
+      for (int r = 0; r < R; ++r) {
+        store_group<E>(s_out[r], g, rx, E::kGroup, vec);
+        store_group<E>(s_out[r], g2, ry, valid2, vec);
+      }
     }
   }
-  if (g < a.groups) {
-    const int valid = group_valid(g, a.count);
-    const uint4 y = reduce_group<R>(s_in, g, valid, vec);
+  for (; g < a.groups; g += stride) {
+    const int valid = group_valid<E>(g, a.count);
+    const uint4 y = reduce_group<R, E>(s_in, g, valid, vec);
 #pragma unroll
-    for (int r = 0; r < R; ++r) store_group(s_out[r], g, y, valid, vec);
+    for (int r = 0; r < R; ++r) store_group<E>(s_out[r], g, y, valid, vec);
   }
 }
 
@@ -79,10 +83,10 @@ __global__ void __launch_bounds__(512) k_oneshot_fanout(CallArgs a) {
 // writing out_r could overwrite data another rank's CTA has yet to read, so
 // the kernel detects that case on the device and lets the rank-0 CTA of each
 // chunk write every output instead (the fan-out order, alias-safe).
-template <int R>
-__global__ void __launch_bounds__(1024) k_oneshot_pull(CallArgs a) {
-  __shared__ const uint16_t* s_in[R];
-  __shared__ uint16_t* s_out[R];
+template <int R, class E>
+__global__ void __launch_bounds__(512) k_oneshot_pull(CallArgs a) {
+  __shared__ const char* s_in[R];
+  __shared__ char* s_out[R];
   __shared__ int s_alias;
   const bool vec = load_tables<R>(a, s_in, s_out);
   if (threadIdx.x == 0) {
@@ -98,48 +102,44 @@ __global__ void __launch_bounds__(1024) k_oneshot_pull(CallArgs a) {
   const size_t chunks = gridDim.x / R;
   const size_t stride = chunks * blockDim.x;
   for (size_t g = (size_t)(blockIdx.x / R) * blockDim.x + threadIdx.x; g < a.groups; g += stride) {
-    const int valid = group_valid(g, a.count);
-    const uint4 y = reduce_group<R>(s_in, g, valid, vec);
+    const int valid = group_valid<E>(g, a.count);
+    const uint4 y = reduce_group<R, E>(s_in, g, valid, vec);
     if (alias) {
 #pragma unroll
-      for (int q = 0; q < R; ++q) store_group(s_out[q], g, y, valid, vec);
+      for (int q = 0; q < R; ++q) store_group<E>(s_out[q], g, y, valid, vec);
     } else {
-      store_group(s_out[r], g, y, valid, vec);
+      store_group<E>(s_out[r], g, y, valid, vec);
     }
   }
 }
 
 }  // namespace
 
-cudaError_t launch_oneshot_fanout(int R, const CallArgs& a, LaunchCfg cfg, cudaStream_t s) {
-#define L(RR) k_oneshot_fanout<RR><<<cfg.ctas, cfg.threads, 0, s>>>(a)
-  AR_RANK_SWITCH(R, L)
+static cudaError_t fanout_occ(int R, int dtype, int threads, int* n) {
+#define Q(RR, EE) \
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, k_oneshot_fanout<RR, EE>, threads, 0)
+  AR_DISPATCH(dtype, R, Q, AR_SWITCH_R16)
+#undef Q
+  return cudaErrorInvalidValue;
+}
+
+int fanout_ctas_per_sm(int R, int dtype, int threads) {
+  int n = 0;
+  return fanout_occ(R, dtype, threads, &n) == cudaSuccess ? n : 0;
+}
+
+cudaError_t launch_oneshot_fanout(int R, int dtype, const CallArgs& a, LaunchCfg cfg,
+                                  cudaStream_t s) {
+#define L(RR, EE) k_oneshot_fanout<RR, EE><<<cfg.ctas, cfg.threads, 0, s>>>(a)
+  AR_DISPATCH(dtype, R, L, AR_SWITCH_R16)
 #undef L
   return cudaGetLastError();
 }
 
-int fanout_ctas_per_sm(int R, int threads) {
-  int n = 0;
-  cudaError_t e = cudaErrorInvalidValue;
-#define Q(RR) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_oneshot_fanout<RR>, threads, 0)
-  switch (R) {
-    case 1: Q(1); break;
-    case 2: Q(2); break;
-    case 3: Q(3); break;
-    case 4: Q(4); break;
-    case 5: Q(5); break;
-    case 6: Q(6); break;
-    case 7: Q(7); break;
-    case 8: Q(8); break;
-    default: return 0;
-  }
-#undef Q
-  return e == cudaSuccess ? n : 0;
-}
-
-cudaError_t launch_oneshot_pull(int R, const CallArgs& a, LaunchCfg cfg, cudaStream_t s) {
-#define L(RR) k_oneshot_pull<RR><<<cfg.ctas, cfg.threads, 0, s>>>(a)
-  AR_RANK_SWITCH(R, L)
+cudaError_t launch_oneshot_pull(int R, int dtype, const CallArgs& a, LaunchCfg cfg,
+                                cudaStream_t s) {
+#define L(RR, EE) k_oneshot_pull<RR, EE><<<cfg.ctas, cfg.threads, 0, s>>>(a)
+  AR_DISPATCH(dtype, R, L, AR_SWITCH_R16)
 #undef L
   return cudaGetLastError();
 }

@@ -12,12 +12,12 @@
 // rank order, round once, write the result tile to shared memory, and one
 // thread sends it to all R outputs with R bulk stores.
 //
-// Tile = 256 threads x 8 elements = 2048 elements (4 KiB per rank).  Tile t
-// covers elements [2048 t, 2048 t + 2048) of every rank; CTA b takes tiles
-// b, b + G, b + 2G, ...  Only the first count - count % 8 elements go through
-// tiles (bulk copies move multiples of 16 bytes); the last count % 8
-// elements are summed by the last CTA with 2-byte accesses.  A call whose
-// pointers are not all 16-byte aligned runs the element path in every CTA.
+// Tile = 256 threads x 16 bytes = 4 KiB per rank.  Tile t covers bytes
+// [4096 t, 4096 t + 4096) of every rank; CTA b takes tiles b, b + G, ...
+// Only whole 16-byte groups go through tiles (bulk copies move multiples of
+// 16 bytes); the last partial group is summed by the last CTA with
+// element-sized accesses.  A call whose pointers are not all 16-byte aligned
+// runs the element path in every CTA.
 //
 // Every wait on an mbarrier is bounded by the handle's spin limit; on expiry
 // the CTA records kDevErrCopyTimeout, waits (bounded again) for the copies it
@@ -27,8 +27,8 @@
 namespace ar {
 namespace {
 
-constexpr int kTileElems = kBulkThreads * kVecElems;         // 2048
-constexpr uint32_t kTileBytes = kTileElems * sizeof(uint16_t);  // 4096
+constexpr uint32_t kTileBytes = kBulkThreads * kGroupBytes;  // 4096
+constexpr int kTileGroups = kBulkThreads;                     // one group per thread
 
 // Stages of the input ring: about 128 KiB of tiles in flight per CTA.
 template <int R>
@@ -132,57 +132,58 @@ __device__ __noinline__ void report_copy_timeout(DevState* st) {
   atomicAdd(&st->timeouts, 1u);
 }
 
-__device__ __forceinline__ uint32_t bulk_tile_elems(size_t t, size_t n8) {
-  const size_t left = n8 - t * kTileElems;
-  return left < (size_t)kTileElems ? (uint32_t)left : (uint32_t)kTileElems;
+// Whole groups of tile t (the tiles cover `full` groups).
+__device__ __forceinline__ uint32_t bulk_tile_groups(size_t t, size_t full) {
+  const size_t left = full - t * kTileGroups;
+  return left < (size_t)kTileGroups ? (uint32_t)left : (uint32_t)kTileGroups;
 }
 
 // Thread 0: start the R bulk loads of this CTA's i-th tile into stage i % S.
 template <int R, int S>
-__device__ __forceinline__ void bulk_issue(uint8_t* in_tiles, const uint16_t* const* s_in,
-                                           uint64_t* full, size_t i, size_t n8, uint64_t pol) {
+__device__ __forceinline__ void bulk_issue(uint8_t* in_tiles, const char* const* s_in,
+                                           uint64_t* full, size_t i, size_t nfull, uint64_t pol) {
   const size_t t = (size_t)blockIdx.x + i * gridDim.x;
   const int s = (int)(i % S);
-  const uint32_t bytes = bulk_tile_elems(t, n8) * (uint32_t)sizeof(uint16_t);
+  const uint32_t bytes = bulk_tile_groups(t, nfull) * (uint32_t)kGroupBytes;
   mbar_arrive_expect_tx(&full[s], bytes * R);
 #pragma unroll
   for (int r = 0; r < R; ++r)
-    bulk_load(in_tiles + ((size_t)s * R + r) * kTileBytes, s_in[r] + t * kTileElems, bytes,
+    bulk_load(in_tiles + ((size_t)s * R + r) * kTileBytes, s_in[r] + t * kTileBytes, bytes,
               &full[s], pol);
 }
 
-template <int R>
+template <int R, class E>
 __global__ void __launch_bounds__(kBulkThreads) k_oneshot_fanout_bulk(CallArgs a) {
   constexpr int S = bulk_stages<R>();
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full[S];
-  __shared__ const uint16_t* s_in[R];
-  __shared__ uint16_t* s_out[R];
+  __shared__ const char* s_in[R];
+  __shared__ char* s_out[R];
   const bool vec = load_tables<R>(a, s_in, s_out);
   const int tid = threadIdx.x;
 
   if (!vec) {  // element path: some pointer is not 16-byte aligned
     const size_t stride = (size_t)gridDim.x * blockDim.x;
     for (size_t g = (size_t)blockIdx.x * blockDim.x + tid; g < a.groups; g += stride) {
-      const int valid = group_valid(g, a.count);
+      const int valid = group_valid<E>(g, a.count);
       uint4 x[R];
 #pragma unroll
-      for (int s = 0; s < R; ++s) x[s] = load_group(s_in[s], g, valid, false);
-      Acc8 acc;
+      for (int s = 0; s < R; ++s) x[s] = load_group<E>(s_in[s], g, valid, false);
+      Acc<E> acc;
       acc.set(x[0]);
 #pragma unroll
       for (int s = 1; s < R; ++s) acc.add(x[s]);
-      const uint4 y = acc.round_bf16();
+      const uint4 y = acc.round();
 #pragma unroll
-      for (int r = 0; r < R; ++r) store_group(s_out[r], g, y, valid, false);
+      for (int r = 0; r < R; ++r) store_group<E>(s_out[r], g, y, valid, false);
     }
     return;
   }
 
   uint8_t* in_tiles = smem;                               // [S][R][kTileBytes]
   uint8_t* res_tiles = smem + (size_t)S * R * kTileBytes;  // [2][kTileBytes]
-  const size_t n8 = a.count & ~(size_t)7;
-  const size_t ntiles = (n8 + kTileElems - 1) / kTileElems;
+  const size_t nfull = a.count / E::kGroup;  // whole groups
+  const size_t ntiles = (nfull + kTileGroups - 1) / kTileGroups;
   const size_t my_n =
       blockIdx.x < ntiles ? (ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
 
@@ -196,37 +197,37 @@ __global__ void __launch_bounds__(kBulkThreads) k_oneshot_fanout_bulk(CallArgs a
   const uint64_t pol = l2_policy_evict_first();
   if (tid == 0)
     for (size_t i = 0; i < my_n && i < (size_t)S; ++i)
-      bulk_issue<R, S>(in_tiles, s_in, full, i, n8, pol);
+      bulk_issue<R, S>(in_tiles, s_in, full, i, nfull, pol);
 
   size_t i = 0;
   for (; i < my_n; ++i) {
     const int s = (int)(i % S);
     const uint32_t parity = (uint32_t)((i / S) & 1);
     const size_t t = (size_t)blockIdx.x + i * gridDim.x;
-    const uint32_t elems = bulk_tile_elems(t, n8);
+    const uint32_t groups = bulk_tile_groups(t, nfull);
     const bool ok = mbar_wait_bounded(&full[s], parity, a.spin_limit_ns);
     if (tid == 0) bulk_wait_read<1>();  // stores of tile i-2 have read res[i & 1]
     if (__syncthreads_or(!ok)) break;
     uint8_t* res = res_tiles + (i & 1) * kTileBytes;
-    if ((uint32_t)tid * kVecElems < elems) {
-      const uint8_t* base = in_tiles + (size_t)s * R * kTileBytes + (size_t)tid * 16;
+    if ((uint32_t)tid < groups) {
+      const uint8_t* base = in_tiles + (size_t)s * R * kTileBytes + (size_t)tid * kGroupBytes;
       uint4 x[R];
 #pragma unroll
       for (int r = 0; r < R; ++r) x[r] = lds_v4(base + (size_t)r * kTileBytes);
-      Acc8 acc;
+      Acc<E> acc;
       acc.set(x[0]);
 #pragma unroll
       for (int r = 1; r < R; ++r) acc.add(x[r]);
-      sts_v4(res + (size_t)tid * 16, acc.round_bf16());
+      sts_v4(res + (size_t)tid * kGroupBytes, acc.round());
     }
     fence_proxy_async_smem();
     __syncthreads();
     if (tid == 0) {
-      const uint32_t bytes = elems * (uint32_t)sizeof(uint16_t);
+      const uint32_t bytes = groups * (uint32_t)kGroupBytes;
 #pragma unroll
-      for (int r = 0; r < R; ++r) bulk_store(s_out[r] + t * kTileElems, res, bytes);
+      for (int r = 0; r < R; ++r) bulk_store(s_out[r] + t * kTileBytes, res, bytes);
       bulk_commit();
-      if (i + S < my_n) bulk_issue<R, S>(in_tiles, s_in, full, i + S, n8, pol);
+      if (i + S < my_n) bulk_issue<R, S>(in_tiles, s_in, full, i + S, nfull, pol);
     }
   }
 
@@ -243,66 +244,60 @@ __global__ void __launch_bounds__(kBulkThreads) k_oneshot_fanout_bulk(CallArgs a
   }
   if (tid == 0) bulk_wait<0>();
 
-  // The last count % 8 elements.
-  if (blockIdx.x == gridDim.x - 1 && (size_t)tid < a.count - n8) {
-    const size_t e = n8 + tid;
-    float acc = bf16_lo((uint32_t)ld_u16(s_in[0] + e));
+  // The elements of the last, partial group.
+  const size_t first_tail = nfull * E::kGroup;
+  if (blockIdx.x == gridDim.x - 1 && (size_t)tid < a.count - first_tail) {
+    const size_t off = (first_tail + tid) * E::kBytes;
+    float acc = E::to_f32(ld_elem<E::kBytes>(s_in[0] + off));
 #pragma unroll
-    for (int r = 1; r < R; ++r) acc = __fadd_rn(acc, bf16_lo((uint32_t)ld_u16(s_in[r] + e)));
-    const uint16_t y = (uint16_t)(pack_bf16x2_rn(acc, 0.0f) & 0xFFFFu);
+    for (int r = 1; r < R; ++r) acc = __fadd_rn(acc, E::to_f32(ld_elem<E::kBytes>(s_in[r] + off)));
+    const uint32_t y = E::from_f32(acc);
 #pragma unroll
-    for (int r = 0; r < R; ++r) st_u16(s_out[r] + e, y);
+    for (int r = 0; r < R; ++r) st_elem<E::kBytes>(s_out[r] + off, y);
   }
 }
 
 }  // namespace
 
-#define AR_BULK_SWITCH(R, CALL) \
-  switch (R) {                  \
-    case 1: CALL(1); break;     \
-    case 2: CALL(2); break;     \
-    case 3: CALL(3); break;     \
-    case 4: CALL(4); break;     \
-    case 5: CALL(5); break;     \
-    case 6: CALL(6); break;     \
-    case 7: CALL(7); break;     \
-    case 8: CALL(8); break;     \
-    default: break;             \
-  }
-
 size_t bulk_smem_bytes(int R) {
-  size_t n = 0;
-#define B(RR) n = bulk_smem<RR>()
-  AR_BULK_SWITCH(R, B)
+  switch (R) {
+#define B(RR) \
+  case RR:    \
+    return bulk_smem<RR>();
+    B(1) B(2) B(3) B(4) B(5) B(6) B(7) B(8) B(9) B(10) B(11) B(12) B(13) B(14) B(15) B(16)
 #undef B
-  return n;
+    default:
+      return 0;
+  }
 }
 
-cudaError_t bulk_prepare(int R) {
-  cudaError_t e = cudaErrorInvalidValue;
-#define P(RR)                                                                         \
-  e = cudaFuncSetAttribute(k_oneshot_fanout_bulk<RR>,                                 \
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bulk_smem<RR>())
-  AR_BULK_SWITCH(R, P)
+cudaError_t bulk_prepare(int R, int dtype) {
+#define P(RR, EE)                                                                   \
+  return cudaFuncSetAttribute(k_oneshot_fanout_bulk<RR, EE>,                        \
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bulk_smem<RR>())
+  AR_DISPATCH(dtype, R, P, AR_SWITCH_R16)
 #undef P
-  return e;
+  return cudaErrorInvalidValue;
 }
 
-int bulk_ctas_per_sm(int R) {
-  int n = 0;
-  cudaError_t e = cudaErrorInvalidValue;
-#define Q(RR)                                                                                 \
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_oneshot_fanout_bulk<RR>, kBulkThreads, \
-                                                    bulk_smem<RR>())
-  AR_BULK_SWITCH(R, Q)
+static cudaError_t bulk_occ(int R, int dtype, int* n) {
+#define Q(RR, EE)                                                                              \
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, k_oneshot_fanout_bulk<RR, EE>,       \
+                                                       kBulkThreads, bulk_smem<RR>())
+  AR_DISPATCH(dtype, R, Q, AR_SWITCH_R16)
 #undef Q
-  return e == cudaSuccess ? n : 0;
+  return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_oneshot_fanout_bulk(int R, const CallArgs& a, int ctas, cudaStream_t s) {
-#define L(RR) \
-  k_oneshot_fanout_bulk<RR><<<ctas, kBulkThreads, bulk_smem<RR>(), s>>>(a)
-  AR_RANK_SWITCH(R, L)
+int bulk_ctas_per_sm(int R, int dtype) {
+  int n = 0;
+  return bulk_occ(R, dtype, &n) == cudaSuccess ? n : 0;
+}
+
+cudaError_t launch_oneshot_fanout_bulk(int R, int dtype, const CallArgs& a, int ctas,
+                                       cudaStream_t s) {
+#define L(RR, EE) k_oneshot_fanout_bulk<RR, EE><<<ctas, kBulkThreads, bulk_smem<RR>(), s>>>(a)
+  AR_DISPATCH(dtype, R, L, AR_SWITCH_R16)
 #undef L
   return cudaGetLastError();
 }

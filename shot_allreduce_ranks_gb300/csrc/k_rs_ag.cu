@@ -7,72 +7,74 @@
 // recvCount; allreduce: both 0).  Here the same one-shot read serves both:
 //
 //   reduce-scatter: rank s's input holds R blocks of `recvcount` elements;
-//     out_r[j] = bf16_rne(sum over s in rank order of in_s[r*recvcount + j]).
+//     out_r[j] = round(sum over s in rank order of in_s[r*recvcount + j]).
 //     The CTAs of grid row r (blockIdx.y = r) read block r of all R inputs
-//     once and write out_r: 2*R*R*recvcount + 2*R*recvcount bytes.
+//     once and write out_r: (R*R + R)*recvcount elements moved.
 //   all-gather: out_r[s*sendcount + j] = in_s[j] for every r; grid row s
 //     reads in_s once and writes it into all R outputs (write mode):
-//     2*R*sendcount + 2*R*R*sendcount bytes.
+//     (R + R*R)*sendcount elements moved.
 //
 // Vector (16-byte) accesses need every pointer 16-byte aligned and the block
-// length a multiple of 8 elements (so every block starts aligned); otherwise
-// the call uses 2-byte accesses.  Outputs must not overlap inputs.
+// length a multiple of the group (8 elements of 2 bytes, 4 of fp32) so that
+// every block starts aligned; otherwise the call uses element-sized
+// accesses.  Outputs must not overlap inputs.
 #include "ar_internal.cuh"
 
 namespace ar {
 namespace {
 
-template <int R>
+template <int R, class E>
 __global__ void __launch_bounds__(512) k_reduce_scatter(CallArgs a) {
-  __shared__ const uint16_t* s_in[R];
-  __shared__ uint16_t* s_out[R];
-  const bool vec = load_tables<R>(a, s_in, s_out) && (a.count % kVecElems == 0);
+  __shared__ const char* s_in[R];
+  __shared__ char* s_out[R];
+  const bool vec = load_tables<R>(a, s_in, s_out) && (a.count % E::kGroup == 0);
   const int r = blockIdx.y;
-  const size_t base = (size_t)r * a.count;  // element offset of block r
+  const size_t base = (size_t)r * a.count * E::kBytes;  // byte offset of block r
   const size_t stride = (size_t)gridDim.x * blockDim.x;
   for (size_t j = (size_t)blockIdx.x * blockDim.x + threadIdx.x; j < a.groups; j += stride) {
-    const int valid = group_valid(j, a.count);
+    const int valid = group_valid<E>(j, a.count);
     uint4 x[R];
 #pragma unroll
-    for (int s = 0; s < R; ++s) x[s] = load_group(s_in[s] + base, j, valid, vec);
-    Acc8 acc;
+    for (int s = 0; s < R; ++s) x[s] = load_group<E>(s_in[s] + base, j, valid, vec);
+    Acc<E> acc;
     acc.set(x[0]);
 #pragma unroll
     for (int s = 1; s < R; ++s) acc.add(x[s]);
-    store_group(s_out[r], j, acc.round_bf16(), valid, vec);
+    store_group<E>(s_out[r], j, acc.round(), valid, vec);
   }
 }
 
-template <int R>
+template <int R, class E>
 __global__ void __launch_bounds__(512) k_all_gather(CallArgs a) {
-  __shared__ const uint16_t* s_in[R];
-  __shared__ uint16_t* s_out[R];
-  const bool vec = load_tables<R>(a, s_in, s_out) && (a.count % kVecElems == 0);
+  __shared__ const char* s_in[R];
+  __shared__ char* s_out[R];
+  const bool vec = load_tables<R>(a, s_in, s_out) && (a.count % E::kGroup == 0);
   const int s = blockIdx.y;
-  const size_t base = (size_t)s * a.count;  // element offset of block s in every output
+  const size_t base = (size_t)s * a.count * E::kBytes;  // byte offset of block s in every output
   const size_t stride = (size_t)gridDim.x * blockDim.x;
   for (size_t j = (size_t)blockIdx.x * blockDim.x + threadIdx.x; j < a.groups; j += stride) {
-    const int valid = group_valid(j, a.count);
-    const uint4 x = load_group(s_in[s], j, valid, vec);
+    const int valid = group_valid<E>(j, a.count);
+    const uint4 x = load_group<E>(s_in[s], j, valid, vec);
 #pragma unroll
-    for (int r = 0; r < R; ++r) store_group(s_out[r] + base, j, x, valid, vec);
+    for (int r = 0; r < R; ++r) store_group<E>(s_out[r] + base, j, x, valid, vec);
   }
 }
 
 }  // namespace
 
-cudaError_t launch_reduce_scatter(int R, const CallArgs& a, LaunchCfg cfg, cudaStream_t s) {
+cudaError_t launch_reduce_scatter(int R, int dtype, const CallArgs& a, LaunchCfg cfg,
+                                  cudaStream_t s) {
   const dim3 grid((unsigned)cfg.ctas, (unsigned)R);
-#define L(RR) k_reduce_scatter<RR><<<grid, cfg.threads, 0, s>>>(a)
-  AR_RANK_SWITCH(R, L)
+#define L(RR, EE) k_reduce_scatter<RR, EE><<<grid, cfg.threads, 0, s>>>(a)
+  AR_DISPATCH(dtype, R, L, AR_SWITCH_R16)
 #undef L
   return cudaGetLastError();
 }
 
-cudaError_t launch_all_gather(int R, const CallArgs& a, LaunchCfg cfg, cudaStream_t s) {
+cudaError_t launch_all_gather(int R, int dtype, const CallArgs& a, LaunchCfg cfg, cudaStream_t s) {
   const dim3 grid((unsigned)cfg.ctas, (unsigned)R);
-#define L(RR) k_all_gather<RR><<<grid, cfg.threads, 0, s>>>(a)
-  AR_RANK_SWITCH(R, L)
+#define L(RR, EE) k_all_gather<RR, EE><<<grid, cfg.threads, 0, s>>>(a)
+  AR_DISPATCH(dtype, R, L, AR_SWITCH_R16)
 #undef L
   return cudaGetLastError();
 }

@@ -67,32 +67,39 @@ def generator(seed: int, rank: int) -> torch.Generator:
     return g
 
 
-def rank_input(count: int, rank: int, seed: int = 0, fill: str = "normal") -> torch.Tensor:
-    """One rank's input as a CPU bf16 tensor of ``count`` elements."""
+def rank_input(count: int, rank: int, seed: int = 0, fill: str = "normal",
+               dtype=torch.bfloat16) -> torch.Tensor:
+    """One rank's input as a CPU tensor of ``count`` elements of ``dtype``
+    (bf16 by default; fp16 and fp32 draw the same fp32 numbers)."""
     if fill == "normal":
         x = torch.randn(count, dtype=torch.float32, generator=generator(seed, rank))
-        return x.to(torch.bfloat16)
+        return x.to(dtype)
     if fill == "ints":
         x = torch.randint(-8, 9, (count,), dtype=torch.int32, generator=generator(seed, rank))
-        return x.to(torch.bfloat16)
+        return x.to(dtype)
     if fill == "position":
         i = torch.arange(count, dtype=torch.int64)
-        return (((7 * i + 13 * rank) % 17) - 8).to(torch.bfloat16)
+        return (((7 * i + 13 * rank) % 17) - 8).to(dtype)
     if fill == "ones":
-        return torch.ones(count, dtype=torch.bfloat16)
+        return torch.ones(count, dtype=dtype)
     raise ValueError("unknown fill %r" % fill)
 
 
-def make_inputs(R: int, count: int, seed: int = 0, fill: str = "normal"):
-    """All R ranks' inputs as CPU bf16 tensors."""
-    return [rank_input(count, r, seed, fill) for r in range(R)]
+def make_inputs(R: int, count: int, seed: int = 0, fill: str = "normal", dtype=torch.bfloat16):
+    """All R ranks' inputs as CPU tensors."""
+    return [rank_input(count, r, seed, fill, dtype) for r in range(R)]
 
 
 def bits(t: torch.Tensor) -> np.ndarray:
-    """The uint16 bit patterns of a CPU bf16 tensor (no copy)."""
-    if t.dtype != torch.bfloat16 or t.device.type != "cpu":
-        raise TypeError("expected a CPU bf16 tensor")
-    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    """The bit patterns of a CPU tensor (uint16 for bf16/fp16, uint32 for
+    fp32; no copy)."""
+    if t.device.type != "cpu":
+        raise TypeError("expected a CPU tensor")
+    if t.dtype in (torch.bfloat16, torch.float16):
+        return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    if t.dtype == torch.float32:
+        return t.contiguous().view(torch.int32).numpy().view(np.uint32)
+    raise TypeError("expected a bf16, fp16 or fp32 tensor")
 
 
 def from_bits(a: np.ndarray) -> torch.Tensor:

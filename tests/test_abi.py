@@ -46,7 +46,8 @@ def test_create_rejects_bad_arguments_before_touching_the_device(lib):
     assert lib.ar_create(_lib.AR_MAX_RANKS + 1, 16, 0, ctypes.byref(h)) == _lib.AR_ERR_INVALID_ARG
     assert lib.ar_create(8, 0, 0, ctypes.byref(h)) == _lib.AR_ERR_INVALID_ARG
     assert lib.ar_create(8, 16, 0, None) == _lib.AR_ERR_INVALID_ARG
-    assert lib.ar_create(8, 16, 1, ctypes.byref(h)) == _lib.AR_ERR_UNSUPPORTED
+    assert lib.ar_create(8, 16, 3, ctypes.byref(h)) == _lib.AR_ERR_UNSUPPORTED
+    assert lib.ar_create(8, 16, -1, ctypes.byref(h)) == _lib.AR_ERR_UNSUPPORTED
 
 
 def test_null_handle_calls(lib):
