@@ -37,14 +37,19 @@ struct TuneRow {
   int threads;
 };
 
-// Measured on GB300 (R = 8, CUDA-graph replay, inputs larger than L2 between
-// reuses): one-shot pull is fastest up to 64 Ki elements per rank (2.4-3.0
-// us) and fan-out with 128-thread CTAs from 128 Ki up (3.4 us at 128 Ki,
-// 13.0 us at 440x5120, 174 us at 32 Mi); the curves cross near 112 Ki.
-static const TuneRow kBuiltinTable[] = {
-    {0, 114688, AR_ONESHOT_PULL, 0, 256},
-    {0, (size_t)-1, AR_ONESHOT_FANOUT, 0, 128},
-};
+// Measured on GB300 (bf16, CUDA-graph replay, inputs larger than L2 between
+// reuses): one-shot pull is fastest for small messages and fan-out with
+// 128-thread CTAs above.  The curves cross near 115 Ki elements per rank at
+// R = 8 (pull 2.95 us vs 3.25 at 64 Ki; 3.44 vs 3.36 at 128 Ki) and near
+// 230 Ki at R = 4 (2.54 vs 2.68 at 128 Ki; 2.79 vs 2.76 at 256 Ki): pull
+// reads R^2 N bytes through L2, so the crossover scales as 1/R, about
+// 0.92 Mi / R elements.  Rows are generated per R from that rule.
+constexpr size_t kPullCrossoverTimesR = 917504;
+
+std::vector<TuneRow> builtin_table(int R) {
+  const size_t pull_max = kPullCrossoverTimesR / (size_t)R / 64 * 64;
+  return {{R, pull_max, AR_ONESHOT_PULL, 0, 256}, {R, (size_t)-1, AR_ONESHOT_FANOUT, 0, 128}};
+}
 
 struct ar_ctx {
   int R = 0;
@@ -379,7 +384,7 @@ ar_status_t ar_create(int R, size_t max_count, int dtype, ar_handle_t* out) {
   h->max_count = max_count;
   h->device = dev;
   h->num_sms = sms;
-  h->table.assign(kBuiltinTable, kBuiltinTable + sizeof kBuiltinTable / sizeof kBuiltinTable[0]);
+  h->table = builtin_table(R);
   const char* env = getenv("AR_TUNING_FILE");
   if (env && *env && !load_table_file(env, &h->table)) {
     fprintf(stderr, "[ar] cannot use AR_TUNING_FILE=%s; keeping the built-in table\n", env);

@@ -271,3 +271,34 @@ def test_host_buffer_path():
         torch.cuda.synchronize()
         for r in range(R):
             G.assert_bitexact(inputs.bits(hout[r]), want, "host path %s rank %d" % (variant, r))
+
+
+@pytest.mark.parametrize("R", [2, 4, 8, 16])
+def test_selector_boundaries_bracket_the_measured_crossover(R):
+    """Pull below the crossover (about 0.92 Mi / R elements), fan-out above."""
+    from shot_allreduce_ranks_gb300 import AllReduce
+    edge = 917504 // R // 64 * 64
+    with AllReduce(R, edge + 4096) as ar:
+        assert ar.select(1) == "oneshot_pull"
+        assert ar.select(edge) == "oneshot_pull"
+        assert ar.select(edge + 1) == "oneshot_fanout"
+        assert ar.select(edge + 4096) == "oneshot_fanout"
+        ar.set_variant("fused_ll8" if R <= 8 else "twophase")
+        assert ar.select(5) == ("fused_ll8" if R <= 8 else "twophase")
+
+
+def test_tuning_file_and_forced_variant_env(tmp_path, monkeypatch):
+    from shot_allreduce_ranks_gb300 import AllReduce
+    table = tmp_path / "table.txt"
+    table.write_text("# R max_count variant ctas threads\n8 1000 twophase 0 128\n0 -1 fused_ll8\n")
+    monkeypatch.setenv("AR_TUNING_FILE", str(table))
+    with AllReduce(8, 5000) as ar:
+        assert ar.select(1000) == "twophase"
+        assert ar.select(1001) == "fused_ll8"
+        xs = inputs.make_inputs(8, 3000, seed=8)
+        outs = G.run_variant(ar, G.to_device(xs), "auto")
+        G.check_all_outputs(outs, G.oracle_expect(xs), "tuning-file auto")
+    monkeypatch.delenv("AR_TUNING_FILE")
+    monkeypatch.setenv("AR_VARIANT", "twophase")
+    with AllReduce(4, 100) as ar:
+        assert ar.select(10) == "twophase"
