@@ -567,6 +567,62 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------------------------
+# sweep mode: every variant over the benchmark message sizes
+
+SWEEP_VARIANTS = ["oneshot_pull", "oneshot_fanout", "oneshot_fanout_bulk", "twophase",
+                  "fused_ll8", "fused_ll8_ring", "fused_ll8_staged", "packet_3op"]
+
+
+def sweep_counts():
+    from shot_allreduce_ranks_gb300 import inputs
+    counts = {4096 << k for k in range(14)}
+    counts |= {w.count for w in inputs.WORKLOADS.values()}
+    return sorted(counts)
+
+
+def run_sweep(args):
+    """One JSON line per (count, variant): graph-replay us/call and
+    algorithmic GB/s, inputs rotating over more than L2."""
+    import torch
+    from shot_allreduce_ranks_gb300 import AllReduce
+    from shot_allreduce_ranks_gb300 import build as lib_build
+    lib_build.build()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(device=dev)
+    dtype = {"bf16": torch.bfloat16, "fp16": torch.float16, "fp32": torch.float32}[args.dtype]
+    ebytes = 4 if args.dtype == "fp32" else 2
+    R = args.sweep_r
+    counts = sweep_counts()
+    variants = [v for v in SWEEP_VARIANTS
+                if not (R > 8 and v in ("fused_ll8", "fused_ll8_ring", "fused_ll8_staged",
+                                        "packet_3op"))]
+    ar = AllReduce(R, max(counts), device=dev, dtype=dtype)
+    peak, _ = measured_peaks()
+    for N in counts:
+        per = 2 * ebytes * R * N
+        nsets = min(16, max(2, math.ceil(3 * L2_BYTES / per)))
+        sets = []
+        for _ in range(nsets):
+            xin = [torch.randn(N, device=dev).to(dtype) for _ in range(R)]
+            sets.append((None, xin, [torch.empty_like(x) for x in xin]))
+        steps = max(100, min(2000, int(2e5 / (per / 1e6 + 5))))
+        for v in variants:
+            t, _, _, _ = time_variant(ar, sets, N, v, steps, 20, stream, "graph")
+            us = t * 1e6 / steps
+            alg = alg_bytes(v, R, N) * ebytes // 2
+            print(json.dumps({"R": R, "count": N, "dtype": args.dtype, "variant": v,
+                              "us_per_call": round(us, 3),
+                              "alg_GBps": round(alg / (us * 1e3), 1),
+                              "frac_of_measured": round(alg / (us * 1e3) / peak, 4),
+                              "auto_selects": ar.select(N)}), flush=True)
+        del sets
+        torch.cuda.empty_cache()
+    if ar.device_status() != 0:
+        raise RuntimeError("device error word set during the sweep")
+    ar.close()
+
+
 def parse_args(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
@@ -583,6 +639,11 @@ def parse_args(argv=None):
     p.add_argument("--e2e-steps", type=int, default=200)
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-extra", action="store_true")
+    p.add_argument("--sweep", action="store_true",
+                   help="time every variant over the benchmark message sizes (JSON lines)")
+    p.add_argument("--sweep-r", type=int, default=8)
+    p.add_argument("--dtype", choices=["bf16", "fp16", "fp32"], default="bf16",
+                   help="element type of --sweep")
     p.add_argument("--no-clocks", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     a = p.parse_args(argv)
@@ -593,7 +654,9 @@ def parse_args(argv=None):
 
 def main(argv=None):
     args = parse_args(argv)
-    if args.impl == "reference":
+    if args.sweep:
+        run_sweep(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
