@@ -55,10 +55,8 @@ def alg_bytes(variant: str, R: int, N: int) -> int:
     reduced shards read back from their owners' outputs in stage 2 (2N; the
     stage-1 stores are already outputs).  fused LL8: 4RN plus each of the
     R-1 foreign shards per rank as 4-byte-per-element packets, written once
-    and read once (8(R-1)N).  fused LL8 with cluster packets: the packets go
-    from SM to SM through distributed shared memory and never reach L2 or
-    HBM, so its HBM bytes are the minimum 4RN."""
-    if variant in ("oneshot_fanout", "oneshot_fanout_bulk", "fused_ll8_cluster"):
+    and read once (8(R-1)N)."""
+    if variant in ("oneshot_fanout", "oneshot_fanout_bulk"):
         return 4 * R * N
     if variant == "oneshot_pull":
         return 2 * R * R * N + 2 * R * N
@@ -144,7 +142,6 @@ def measured_peaks():
 KERNEL_SOURCES = {
     "fused_ll8": "k_fused_ll8.cu", "fused_ll8_staged": "k_fused_ll8.cu",
     "packet_3op": "k_fused_ll8.cu", "fused_ll8_ring": "k_fused_ll8.cu",
-    "fused_ll8_cluster": "k_fused_cluster.cu",
     "oneshot_fanout": "k_oneshot.cu",
     "oneshot_pull": "k_oneshot.cu", "oneshot_fanout_bulk": "k_oneshot_bulk.cu",
     "twophase": "k_twophase.cu",
@@ -427,8 +424,7 @@ def run_ours(args):
     extra = {}
     if not args.no_extra:
         for v in ("oneshot_fanout", "oneshot_fanout_bulk", "oneshot_pull", "twophase",
-                  "fused_ll8", "fused_ll8_staged", "packet_3op", "fused_ll8_ring",
-                  "fused_ll8_cluster"):
+                  "fused_ll8", "fused_ll8_staged", "packet_3op", "fused_ll8_ring"):
             if v == args.variant:
                 continue
             t, pv, _, _ = time_variant(ar, sets, N, v, min(args.steps, 2000), 20, stream,
@@ -485,7 +481,7 @@ def run_ours(args):
         torch.cuda.empty_cache()
         tsets = make_sets(wt.R, wt.count, wt.fill, 2, dev)
         art = AllReduce(wt.R, wt.count, device=dev)
-        for v in ("fused_ll8", "fused_ll8_cluster", "oneshot_fanout"):
+        for v in ("fused_ll8", "oneshot_fanout"):
             t, pv, _, _ = time_variant(art, tsets, wt.count, v, min(args.steps, 2000), 20, stream,
                                        args.timing)
             ab_t = alg_bytes(v, wt.R, wt.count)
@@ -575,8 +571,7 @@ def run_reference(args):
 # sweep mode: every variant over the benchmark message sizes
 
 SWEEP_VARIANTS = ["oneshot_pull", "oneshot_fanout", "oneshot_fanout_bulk", "twophase",
-                  "fused_ll8", "fused_ll8_ring", "fused_ll8_cluster", "fused_ll8_staged",
-                  "packet_3op"]
+                  "fused_ll8", "fused_ll8_ring", "fused_ll8_staged", "packet_3op"]
 
 
 def sweep_counts():
@@ -638,7 +633,7 @@ def parse_args(argv=None):
     p.add_argument("--variant", default="fused_ll8",
                    choices=["oneshot_pull", "oneshot_fanout", "twophase", "fused_ll8",
                             "oneshot_fanout_bulk", "fused_ll8_staged", "packet_3op",
-                            "fused_ll8_ring", "fused_ll8_cluster"])
+                            "fused_ll8_ring"])
     p.add_argument("--timing", choices=["graph", "stream"], default="graph",
                    help="graph: calls replayed from CUDA graphs; stream: plain launches")
     p.add_argument("--e2e-steps", type=int, default=200)

@@ -43,13 +43,6 @@
  *     whole message: producers take credits from the owners' progress words
  *     before reusing a slot, and the flag advances once per round, so the
  *     packet footprint stays small enough to live in L2;
- *   - AR_FUSED_LL8_CLUSTER is AR_FUSED_LL8 with each owner's packet slots
- *     in the owner CTA's shared memory: the R virtual ranks of a chunk are
- *     the R CTAs of one thread-block cluster, producers store LL8 packets
- *     into the owners' shared memory over the cluster's distributed shared
- *     memory, owners poll the flags there, and a cluster barrier per round
- *     orders slot reuse; no packet reaches L2 or HBM, and clusters do not
- *     wait on one another;
  *   - AR_FUSED_LL8 is the single fused scatter -> reduce -> broadcast kernel
  *     synchronised by LL packet flags of "Add monolithic fused packet
  *     allreduce kernel and Model::all_reduce_packet API" (microsoft/ark #254,
@@ -107,11 +100,10 @@ typedef enum {
   AR_ONESHOT_FANOUT_BULK = 5, /* fan-out with tiles moved by bulk (TMA) copies through shared memory */
   AR_FUSED_LL8_STAGED = 6,    /* fused LL8 without write mode: result packets back to every rank */
   AR_PACKET_3OP = 7,          /* the same three packet phases as three separate launches */
-  AR_FUSED_LL8_RING = 8,      /* AR_FUSED_LL8 with packets in a small per-CTA ring (credits) */
-  AR_FUSED_LL8_CLUSTER = 9    /* AR_FUSED_LL8 with packets in the owners' shared memory (clusters) */
+  AR_FUSED_LL8_RING = 8       /* AR_FUSED_LL8 with packets in a small per-CTA ring (credits) */
 } ar_variant_t;
 
-#define AR_NUM_VARIANTS 10
+#define AR_NUM_VARIANTS 9
 
 /* Static description of a handle (filled by ar_query). */
 typedef struct {
@@ -220,9 +212,8 @@ ar_status_t ar_select(ar_handle_t h, size_t count, int* variant);
  * (0 = automatic).  ctas is the total grid for AR_FUSED_LL8 (rounded down to
  * a multiple of R, clamped to the co-resident limit and raised to at least
  * R), and the grid-stride CTA count for the others.  threads must be a
- * multiple of 32 in [64, 512] (AR_FUSED_LL8 and the fan-out accept
- * 128..512, AR_FUSED_LL8_CLUSTER 64..256, whose ctas, rounded down to whole
- * clusters of R, is clamped to one wave of co-resident clusters). */
+ * multiple of 32 in [64, 512] (the packet and fan-out kernels accept
+ * 128..512). */
 ar_status_t ar_set_launch(ar_handle_t h, int variant, int ctas, int threads);
 
 /* ar_set_spin_limit_ns -- the longest a fused-kernel packet wait may spin

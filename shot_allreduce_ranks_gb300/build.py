@@ -20,7 +20,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libar_gb300.so")
 
 SOURCES = ["ar_api.cu", "k_oneshot.cu", "k_oneshot_bulk.cu", "k_twophase.cu", "k_fused_ll8.cu",
-           "k_fused_cluster.cu", "k_rs_ag.cu"]
+           "k_rs_ag.cu"]
 HEADERS = [os.path.join(CSRC, "ar_internal.cuh"), os.path.join(INCLUDE, "ar.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -83,9 +83,7 @@ struct ar_ctx {
   int occ_staged[33] = {};
   int occ_ring[33] = {};
   int occ_fanout[33] = {};
-  int bulk_ctas_per_sm = 0;
-  int cluster_threads = 256;   // cluster variant's default CTA size
-  int occ_cluster[33] = {};    // co-resident clusters per threads/32 (-1: none fit)    // bulk fan-out (fixed 256 threads)
+  int bulk_ctas_per_sm = 0;    // bulk fan-out (fixed 256 threads)
 
   // host-buffer path
   char* staging = nullptr;        // 2 * R buffers of max_count elements
@@ -99,7 +97,7 @@ ar_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? AR_OK : AR_ER
 
 bool is_packet_variant(int v) {
   return v == AR_FUSED_LL8 || v == AR_FUSED_LL8_STAGED || v == AR_PACKET_3OP ||
-         v == AR_FUSED_LL8_RING || v == AR_FUSED_LL8_CLUSTER;
+         v == AR_FUSED_LL8_RING;
 }
 
 size_t ceil_div(size_t a, size_t b) { return (a + b - 1) / b; }
@@ -157,17 +155,6 @@ int choose(const ar_ctx* h, size_t count, const TuneRow** row) {
   const TuneRow* t = lookup(h, count);
   *row = t;
   return t ? t->variant : AR_ONESHOT_FANOUT;
-}
-
-// Co-resident clusters of the cluster variant at `threads` threads (cached).
-int cluster_active(ar_ctx* h, int threads) {
-  const int k = threads / 32;
-  if (k < 1 || k > 32) return 0;
-  if (h->occ_cluster[k] == 0) {
-    const int n = ar::cluster_max_active(h->R, h->dtype, threads);
-    h->occ_cluster[k] = n > 0 ? n : -1;
-  }
-  return h->occ_cluster[k] > 0 ? h->occ_cluster[k] : 0;
 }
 
 int occupancy(ar_ctx* h, int variant, int threads) {
@@ -252,18 +239,6 @@ LaunchCfg shape(ar_ctx* h, int variant, const TuneRow* row, size_t groups, size_
       c.ctas = (int)(per_rank * (size_t)R);
       break;
     }
-    case AR_FUSED_LL8_CLUSTER: {
-      // One cluster of R CTAs per chunk of threads groups per shard; clusters
-      // are independent, so the grid is one wave of co-resident clusters.
-      if (c.threads <= 0) c.threads = h->cluster_threads;
-      const int active = cluster_active(h, c.threads);
-      if (active <= 0) return {0, 0};
-      size_t clusters = std::max<size_t>(1, ceil_div(shard_groups, (size_t)c.threads));
-      if (c.ctas > 0) clusters = std::max<size_t>(1, (size_t)c.ctas / (size_t)R);
-      clusters = std::min(clusters, (size_t)active);
-      c.ctas = (int)(clusters * (size_t)R);
-      break;
-    }
     case AR_FUSED_LL8:
     case AR_FUSED_LL8_STAGED: {
       if (c.threads <= 0) c.threads = h->fused_threads;
@@ -331,20 +306,6 @@ ar_status_t launch(ar_ctx* h, int variant, const TuneRow* row, const void* const
       e = ar::launch_fused_ll8_ring(h->R, h->dtype, a, f, cfg, s);
       break;
     }
-    case AR_FUSED_LL8_CLUSTER: {
-      FusedArgs f;
-      f.scratch = nullptr;
-      f.rscratch = nullptr;
-      f.slot_groups = 0;
-      f.state = h->state;
-      f.spin_limit_ns = h->spin_limit_ns;
-      f.skip_producer = h->skip_producer;
-      f.ring_depth = 0;
-      f.progress = nullptr;
-      h->skip_producer = -1;
-      e = ar::launch_fused_ll8_cluster(h->R, h->dtype, a, f, cfg, s);
-      break;
-    }
     case AR_FUSED_LL8:
     case AR_FUSED_LL8_STAGED:
     case AR_PACKET_3OP: {
@@ -397,7 +358,6 @@ const char* ar_variant_name(int variant) {
     case AR_FUSED_LL8_STAGED: return "fused_ll8_staged";
     case AR_PACKET_3OP: return "packet_3op";
     case AR_FUSED_LL8_RING: return "fused_ll8_ring";
-    case AR_FUSED_LL8_CLUSTER: return "fused_ll8_cluster";
     default: return "?";
   }
 }
@@ -462,7 +422,6 @@ ar_status_t ar_create(int R, size_t max_count, int dtype, ar_handle_t* out) {
   }
   h->ring_bytes = (size_t)R * (size_t)(R - 1) * ar::kMaxRingDepth * h->ring_threads * 32;
   if (ar::bulk_prepare(R, dtype) == cudaSuccess) h->bulk_ctas_per_sm = ar::bulk_ctas_per_sm(R, dtype);
-  if (packets) ar::cluster_prepare(R, dtype);
   cudaGetLastError();
 
   ar_status_t st = AR_OK;
@@ -539,7 +498,6 @@ ar_status_t ar_set_launch(ar_handle_t h, int variant, int ctas, int threads) {
   if ((variant == AR_FUSED_LL8 || variant == AR_ONESHOT_FANOUT) && threads &&
       (threads < 128 || threads > 512))
     return AR_ERR_INVALID_ARG;
-  if (variant == AR_FUSED_LL8_CLUSTER && threads > 256) return AR_ERR_INVALID_ARG;
   h->override_cfg[variant] = {ctas, threads};
   return AR_OK;
 }

@@ -335,14 +335,6 @@ cudaError_t launch_packet_3op(int R, int dtype, const CallArgs& a, const FusedAr
                               LaunchCfg cfg, cudaStream_t s);
 cudaError_t launch_fused_ll8_ring(int R, int dtype, const CallArgs& a, const FusedArgs& f,
                                   LaunchCfg cfg, cudaStream_t s);
-// Fused LL8 with packets in the owners' shared memory (k_fused_cluster.cu):
-// cfg.ctas is a multiple of R (one cluster of R CTAs per chunk), cfg.threads
-// at most 256.  cluster_prepare sets the kernel's shared-memory limit once;
-// cluster_max_active is the number of co-resident clusters (0 if none fit).
-cudaError_t launch_fused_ll8_cluster(int R, int dtype, const CallArgs& a, const FusedArgs& f,
-                                     LaunchCfg cfg, cudaStream_t s);
-cudaError_t cluster_prepare(int R, int dtype);
-int cluster_max_active(int R, int dtype, int threads);
 // Reduce-scatter / all-gather (k_rs_ag.cu): a.count is the block length;
 // the grid is (cfg.ctas, R).
 cudaError_t launch_reduce_scatter(int R, int dtype, const CallArgs& a, LaunchCfg cfg,

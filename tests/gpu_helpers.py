@@ -10,8 +10,7 @@ from shot_allreduce_ranks_gb300 import AllReduce, build, inputs
 
 DEV = "cuda"
 PARITY_VARIANTS = ["oneshot_pull", "oneshot_fanout", "twophase", "fused_ll8",
-                   "oneshot_fanout_bulk", "fused_ll8_staged", "packet_3op", "fused_ll8_ring",
-                   "fused_ll8_cluster"]
+                   "oneshot_fanout_bulk", "fused_ll8_staged", "packet_3op", "fused_ll8_ring"]
 
 _handles = {}
 

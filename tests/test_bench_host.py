@@ -16,7 +16,6 @@ def test_alg_bytes_match_the_roofline_table():
     N = 512 * 8192
     assert bench.alg_bytes("oneshot_fanout", 8, N) == 134_217_728
     assert bench.alg_bytes("fused_ll8", 8, N) == 369_098_752
-    assert bench.alg_bytes("fused_ll8_cluster", 8, N) == 134_217_728
     assert bench.alg_bytes("twophase", 8, N) == 134_217_728 + 2 * N
     assert bench.alg_bytes("oneshot_pull", 8, N) == 2 * 64 * N + 2 * 8 * N
     # R = 4 and R = 8 at 64 MiB per rank

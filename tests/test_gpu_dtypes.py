@@ -11,7 +11,7 @@ from shot_allreduce_ranks_gb300._lib import AR_ERR_UNSUPPORTED
 pytestmark = pytest.mark.gpu
 
 ONE_SHOT = ["oneshot_pull", "oneshot_fanout", "oneshot_fanout_bulk", "twophase"]
-PACKET = ["fused_ll8", "fused_ll8_staged", "packet_3op", "fused_ll8_ring", "fused_ll8_cluster"]
+PACKET = ["fused_ll8", "fused_ll8_staged", "packet_3op", "fused_ll8_ring"]
 COUNTS = [1, 7, 9, 4097, 3 * 65536 + 5]
 
 _handles = {}

@@ -22,8 +22,7 @@ def ar():
     G.release_handles()
 
 
-PACKET_VARIANTS = ["fused_ll8", "fused_ll8_staged", "packet_3op", "fused_ll8_ring",
-                   "fused_ll8_cluster"]
+PACKET_VARIANTS = ["fused_ll8", "fused_ll8_staged", "packet_3op", "fused_ll8_ring"]
 
 
 def _bufs(xs):
@@ -62,7 +61,7 @@ def test_epoch_wraps_to_one_skipping_zero(ar, variant):
     ar.set_variant("fused_ll8")
 
 
-@pytest.mark.parametrize("variant", PACKET_VARIANTS[:4])
+@pytest.mark.parametrize("variant", PACKET_VARIANTS)
 def test_epoch_advances_once_per_call_every_packet_variant(ar, variant):
     xs = inputs.make_inputs(R, COUNT, 11)
     bufs, outs = _bufs(xs)
@@ -119,12 +118,10 @@ def test_stale_packets_are_rejected(ar):
     G.check_all_outputs(outs, G.oracle_expect(xb), "after stale-packet timeout")
 
 
-@pytest.mark.parametrize("variant", ["fused_ll8", "fused_ll8_cluster"])
-def test_graph_replay_with_changing_inputs(ar, variant):
+def test_graph_replay_with_changing_inputs(ar):
     """Capture one fused call into a CUDA graph, then replay it with inputs
     that change between replays.  The epoch lives on the device, so every
     replay rotates it (a by-value epoch would be baked into the graph)."""
-    ar.set_variant(variant)
     bufs = [torch.empty(COUNT, dtype=torch.bfloat16, device=G.DEV) for _ in range(R)]
     outs = [torch.empty_like(b) for b in bufs]
     in_tbl, out_tbl = ar.tables(bufs, outs)
@@ -146,10 +143,8 @@ def test_graph_replay_with_changing_inputs(ar, variant):
         g.replay()
         torch.cuda.synchronize()
         G.check_all_outputs(outs, G.oracle_expect(xs), "replay %d" % rep)
-    per_call = (ar.debug_get_epoch() - e0) // 6
-    assert per_call >= 1 and ar.debug_get_epoch() == e0 + 6 * per_call
+    assert ar.debug_get_epoch() == e0 + 6
     assert ar.device_status() == AR_OK
-    ar.set_variant("fused_ll8")
 
 
 @pytest.mark.parametrize("depth_calls", [(0, 2), (3 * R, 5)])
@@ -178,53 +173,3 @@ def test_ring_many_rounds(depth_calls):
     for call, (snap, want) in enumerate(zip(snaps, wants)):
         G.check_all_outputs(snap, want, "ring call %d" % call)
     h.set_launch("fused_ll8_ring", 0, 0)
-
-
-# The cluster variant: one cluster of R CTAs per chunk, packets in the owners'
-# shared memory.  With one cluster of 64 threads the call runs
-# ceil(shard groups / 64) rounds, each reusing the same ring slots.
-def _cdiv(a, b):
-    return -(-a // b)
-
-
-CLUSTER_ROUNDS = _cdiv(_cdiv(_cdiv(COUNT, 8), R), 64)
-
-
-def test_cluster_many_rounds_epoch_and_wrap(ar):
-    """One cluster of 64-thread CTAs: CLUSTER_ROUNDS rounds per call, so
-    every ring slot is reused round after round, the epoch moves on by the
-    number of rounds per call, and the flag sequence crosses 2^32 - 1 -> 1
-    inside a call."""
-    ar.set_variant("fused_ll8_cluster")
-    ar.set_launch("fused_ll8_cluster", R, 64)
-    xs = inputs.make_inputs(R, COUNT, 21)
-    want = G.oracle_expect(xs)
-    bufs, outs = _bufs(xs)
-    e0 = ar.debug_get_epoch()
-    ar(bufs, outs)
-    assert ar.debug_get_epoch() == e0 + CLUSTER_ROUNDS
-    G.check_all_outputs(outs, want, "cluster, %d rounds" % CLUSTER_ROUNDS)
-    start = 0xFFFFFFFF - CLUSTER_ROUNDS // 2
-    ar.debug_set_epoch(start)
-    for o in outs:
-        o.zero_()
-    ar(bufs, outs)
-    assert ar.debug_get_epoch() == (start - 1 + CLUSTER_ROUNDS) % 0xFFFFFFFF + 1
-    G.check_all_outputs(outs, want, "cluster, flags across the wrap")
-    assert ar.device_status() == AR_OK
-    ar.set_launch("fused_ll8_cluster", 0, 0)
-    ar.set_variant("fused_ll8")
-
-
-@pytest.mark.parametrize("threads", [64, 128, 256])
-@pytest.mark.parametrize("clusters", [1, 3, 0])
-def test_cluster_launch_shapes(ar, threads, clusters):
-    ar.set_variant("fused_ll8_cluster")
-    ar.set_launch("fused_ll8_cluster", clusters * R, threads)
-    xs = inputs.make_inputs(R, COUNT, 22)
-    bufs, outs = _bufs(xs)
-    ar(bufs, outs)
-    G.check_all_outputs(outs, G.oracle_expect(xs), "cluster x%d threads=%d" % (clusters, threads))
-    assert ar.device_status() == AR_OK
-    ar.set_launch("fused_ll8_cluster", 0, 0)
-    ar.set_variant("fused_ll8")
