@@ -40,36 +40,51 @@ def test_epoch_advances_once_per_call(ar):
     G.check_all_outputs(outs, G.oracle_expect(xs), "after 5 calls")
 
 
+def _flag_after(e, k):
+    """The k-th epoch after e in the sequence 1 .. 2^32-1 that skips 0."""
+    return (e - 1 + k) % 0xFFFFFFFF + 1
+
+
 @pytest.mark.parametrize("variant", ["fused_ll8", "fused_ll8_ring", "packet_3op"])
 def test_epoch_wraps_to_one_skipping_zero(ar, variant):
-    """One call moves the epoch by one step here (the ring kernel moves it by
-    its number of rounds, which is 1 at this size)."""
+    """A call moves the epoch by its number of flag values (one for the
+    full-scratch kernels, one per round for the ring).  Started just below
+    2^32, three calls carry the flags across the wrap, skipping 0, and every
+    one is correct."""
     ar.set_variant(variant)
     xs = inputs.make_inputs(R, COUNT, 2)
     want = G.oracle_expect(xs)
     bufs, outs = _bufs(xs)
-    ar.debug_set_epoch(0xFFFFFFFE)
+    e0 = ar.debug_get_epoch()
     ar(bufs, outs)
-    assert ar.debug_get_epoch() == 0xFFFFFFFF
-    G.check_all_outputs(outs, want, "epoch 2^32-2")
-    ar(bufs, outs)
-    assert ar.debug_get_epoch() == 1
-    G.check_all_outputs(outs, want, "epoch 2^32-1")
-    ar(bufs, outs)
-    assert ar.debug_get_epoch() == 2
-    G.check_all_outputs(outs, want, "epoch 1 after wrap")
+    step = ar.debug_get_epoch() - e0
+    assert 1 <= step <= 8
+    e = 0xFFFFFFFF - step
+    ar.debug_set_epoch(e)
+    for call in range(3):
+        for o in outs:
+            o.zero_()
+        ar(bufs, outs)
+        e = _flag_after(e, step)
+        assert ar.debug_get_epoch() == e
+        G.check_all_outputs(outs, want, "%s call %d near the wrap" % (variant, call))
+    assert ar.device_status() == AR_OK
     ar.set_variant("fused_ll8")
 
 
 @pytest.mark.parametrize("variant", PACKET_VARIANTS)
 def test_epoch_advances_once_per_call_every_packet_variant(ar, variant):
+    """By one per call (the ring: by its rounds per call, the same every call)."""
     xs = inputs.make_inputs(R, COUNT, 11)
     bufs, outs = _bufs(xs)
     ar.set_variant(variant)
     e0 = ar.debug_get_epoch()
-    for _ in range(3):
+    ar(bufs, outs)
+    step = ar.debug_get_epoch() - e0
+    assert step == 1 or (variant == "fused_ll8_ring" and 1 <= step <= 8)
+    for _ in range(2):
         ar(bufs, outs)
-    assert ar.debug_get_epoch() == e0 + 3
+    assert ar.debug_get_epoch() == e0 + 3 * step
     G.check_all_outputs(outs, G.oracle_expect(xs), variant)
     ar.set_variant("fused_ll8")
 
