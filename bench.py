@@ -339,6 +339,37 @@ def time_variant(ar, sets, N, variant, steps, warmup, stream, mode="graph", per_
     return total, per, w0, w1
 
 
+def time_flushed(ar, sets, N, variant, steps, stream, flush):
+    """Per-call device time with L2 flushed before every call: `flush` (a
+    buffer larger than L2) is rewritten on `stream`, then the call runs
+    between two events.  Returns the per-call durations in s."""
+    import torch
+    ar.set_variant(variant)
+    tables = [ar.tables(xin, xout) for _, xin, xout in sets]
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            it, ot = tables[i % len(tables)]
+            ar.allreduce_tables(it, ot, N, stream)
+        for i, (e0, e1) in enumerate(evs):
+            flush.zero_()
+            it, ot = tables[i % len(tables)]
+            e0.record(stream)
+            ar.allreduce_tables(it, ot, N, stream)
+            e1.record(stream)
+    torch.cuda.synchronize()
+    return [e0.elapsed_time(e1) * 1e-3 for e0, e1 in evs]
+
+
+def spread(durations_s):
+    """Median, min, 90th percentile and max of per-call durations, in us."""
+    xs = sorted(d * 1e6 for d in durations_s)
+    pick = lambda q: xs[min(len(xs) - 1, int(q * (len(xs) - 1) + 0.5))]
+    return {"median": round(pick(0.5), 3), "min": round(xs[0], 3), "p90": round(pick(0.9), 3),
+            "max": round(xs[-1], 3), "calls": len(xs)}
+
+
 def time_e2e(ar, R, N, steps, warmup, stream, host_in, host_out):
     import torch
     ar.reserve_host_staging()
@@ -469,6 +500,14 @@ def run_ours(args):
                                    other)
         extra["%s_%s_timing" % (args.variant, other)] = {
             "us_per_call": round(t * 1e6 / min(args.steps, 2000), 3)}
+        # per-call events (an event pair around every launch on the stream):
+        # the spread of single calls, warm and with L2 flushed before each
+        _, per_stream, _, _ = time_variant(ar, sets, N, args.variant, 200, 20, stream, "stream")
+        extra["%s_per_call_stream_us" % args.variant] = spread(per_stream)
+        flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+        extra["%s_per_call_l2_flushed_us" % args.variant] = spread(
+            time_flushed(ar, sets, N, args.variant, 200, stream, flush))
+        del flush
         ar.set_variant("auto")
         extra["auto_selects"] = ar.select(N)
 

@@ -98,3 +98,8 @@ def test_reference_arm_other_ranks_stay_silent(capsys, monkeypatch):
 def test_warmup_floor():
     with pytest.raises(SystemExit):
         bench.parse_args(["--warmup", "2"])
+
+
+def test_spread_of_per_call_times():
+    s = bench.spread([t * 1e-6 for t in (5.0, 1.0, 3.0, 2.0, 4.0)])
+    assert s == {"median": 3.0, "min": 1.0, "p90": 5.0, "max": 5.0, "calls": 5}
