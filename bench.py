@@ -145,6 +145,7 @@ KERNEL_SOURCES = {
     "oneshot_fanout": "k_oneshot.cu",
     "oneshot_pull": "k_oneshot.cu", "oneshot_fanout_bulk": "k_oneshot_bulk.cu",
     "twophase": "k_twophase.cu",
+    "reduce_scatter": "k_rs_ag.cu", "all_gather": "k_rs_ag.cu",
 }
 
 
@@ -687,6 +688,8 @@ def run_sweep(args):
             xin = [torch.randn(N, device=dev).to(dtype) for _ in range(R)]
             sets.append((None, xin, [torch.empty_like(x) for x in xin]))
         steps = max(100, min(2000, int(2e5 / (per / 1e6 + 5))))
+        ar.set_variant("auto")
+        auto_choice = ar.select(N)
         for v in variants:
             t, _, _, _ = time_variant(ar, sets, N, v, steps, 20, stream, "graph")
             us = t * 1e6 / steps
@@ -695,11 +698,77 @@ def run_sweep(args):
                               "us_per_call": round(us, 3),
                               "alg_GBps": round(alg / (us * 1e3), 1),
                               "frac_of_measured": round(alg / (us * 1e3) / peak, 4),
-                              "auto_selects": ar.select(N)}), flush=True)
+                              "auto_selects": auto_choice}), flush=True)
         del sets
         torch.cuda.empty_cache()
     if ar.device_status() != 0:
         raise RuntimeError("device error word set during the sweep")
+    ar.close()
+
+
+def run_collective(args):
+    """Reduce-scatter or all-gather of the workload's message, one JSON line:
+    graph-replay us/call and algorithmic GB/s.  reduce_scatter: every rank
+    holds N elements (R blocks of N/R) and receives its block of the sum;
+    all_gather: every rank holds N/R elements and receives all N."""
+    import torch
+    from shot_allreduce_ranks_gb300 import AllReduce, inputs
+    from shot_allreduce_ranks_gb300 import build as lib_build
+    lib_build.build()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(device=dev)
+    dtype = {"bf16": torch.bfloat16, "fp16": torch.float16, "fp32": torch.float32}[args.dtype]
+    ebytes = 4 if args.dtype == "fp32" else 2
+    w = inputs.WORKLOADS[args.workload]
+    R, N = w.R, w.count
+    b = N // R
+    rs = args.collective == "reduce_scatter"
+    n_in, n_out = (R * b, b) if rs else (b, R * b)
+    alg = ebytes * R * (n_in + n_out)  # every input read once, every output written once
+    nsets = min(16, max(2, math.ceil(3 * L2_BYTES / alg)))
+    sets = [([torch.randn(n_in, device=dev).to(dtype) for _ in range(R)],
+             [torch.empty(n_out, dtype=dtype, device=dev) for _ in range(R)])
+            for _ in range(nsets)]
+    ar = AllReduce(R, R * b, device=dev, dtype=dtype)
+
+    def call(i):
+        xin, xout = sets[i % nsets]
+        if rs:
+            ar.reduce_scatter(xin, xout, recvcount=b, stream=stream)
+        else:
+            ar.all_gather(xin, xout, sendcount=b, stream=stream)
+
+    with torch.cuda.stream(stream):  # also builds every set's pointer tables before capture
+        for i in range(max(3, nsets, args.warmup)):
+            call(i)
+    torch.cuda.synchronize()
+    per_graph = 50
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(per_graph):
+            call(i)
+    reps = max(1, args.steps // per_graph)
+    with torch.cuda.stream(stream):
+        g.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / (reps * per_graph)
+    peak, peak_kind = measured_peaks()
+    if ar.device_status() != 0:
+        raise RuntimeError("device error word set")
+    print(json.dumps({"collective": args.collective, "workload": args.workload, "R": R,
+                      "block": b, "dtype": args.dtype, "calls": reps * per_graph,
+                      "us_per_call": round(us, 3), "alg_bytes_per_call": alg,
+                      "alg_GBps": round(alg / (us * 1e3), 1),
+                      "frac_of_measured": round(alg / (us * 1e3) / peak, 4),
+                      "peak_kind": peak_kind, "gpu_launches": reps * per_graph}), flush=True)
     ar.close()
 
 
@@ -723,7 +792,9 @@ def parse_args(argv=None):
                    help="time every variant over the benchmark message sizes (JSON lines)")
     p.add_argument("--sweep-r", type=int, default=8)
     p.add_argument("--dtype", choices=["bf16", "fp16", "fp32"], default="bf16",
-                   help="element type of --sweep")
+                   help="element type of --sweep and --collective")
+    p.add_argument("--collective", choices=["reduce_scatter", "all_gather"], default=None,
+                   help="time ar_reduce_scatter / ar_all_gather on the workload (JSON line)")
     p.add_argument("--no-clocks", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     a = p.parse_args(argv)
@@ -736,6 +807,8 @@ def main(argv=None):
     args = parse_args(argv)
     if args.sweep:
         run_sweep(args)
+    elif args.collective:
+        run_collective(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

@@ -37,18 +37,27 @@ struct TuneRow {
   int threads;
 };
 
-// Measured on GB300 (bf16, CUDA-graph replay, inputs larger than L2 between
+// Measured on GB300 (CUDA-graph replay, inputs larger than L2 between
 // reuses): one-shot pull is fastest for small messages and fan-out with
-// 128-thread CTAs above.  The curves cross near 115 Ki elements per rank at
-// R = 8 (pull 2.95 us vs 3.25 at 64 Ki; 3.44 vs 3.36 at 128 Ki) and near
-// 230 Ki at R = 4 (2.54 vs 2.68 at 128 Ki; 2.79 vs 2.76 at 256 Ki): pull
-// reads R^2 N bytes through L2, so the crossover scales as 1/R, about
-// 0.92 Mi / R elements.  Rows are generated per R from that rule.
-constexpr size_t kPullCrossoverTimesR = 917504;
+// 128-thread CTAs above.  For bf16 the curves cross near 115 Ki elements per
+// rank at R = 8 (pull 3.03 us vs 3.28 at 64 Ki; 3.52 vs 3.36 at 128 Ki) and
+// near 230 Ki at R = 4 (2.58 vs 2.67 at 128 Ki; 2.83 vs 2.75 at 256 Ki):
+// pull reads R^2 N bytes through L2, so the crossover scales as 1/R.  It is
+// a number of bytes per rank: fp16 crosses where bf16 does, fp32 at half
+// the element count (R = 8: pull 2.91 vs 2.99 us at 32 Ki; 3.36 vs 3.10 at
+// 64 Ki), about 1.75 MiB / R per rank.  At R = 16 (bf16) the bulk-copy
+// fan-out beats the register fan-out from 64 Ki to 128 Ki elements (4.63 vs
+// 5.27 us, 5.18 vs 5.72) and not above (6.46 vs 6.40 at 256 Ki, 14.79 vs
+// 13.37 at 1 Mi).  Rows are generated per (R, element size) from these rules.
+constexpr size_t kPullCrossoverBytesTimesR = 917504 * 2;
+constexpr size_t kBulkMaxBytesR16 = 131072 * 2;
 
-std::vector<TuneRow> builtin_table(int R) {
-  const size_t pull_max = kPullCrossoverTimesR / (size_t)R / 64 * 64;
-  return {{R, pull_max, AR_ONESHOT_PULL, 0, 256}, {R, (size_t)-1, AR_ONESHOT_FANOUT, 0, 128}};
+std::vector<TuneRow> builtin_table(int R, size_t elem_bytes) {
+  const size_t pull_max = kPullCrossoverBytesTimesR / elem_bytes / (size_t)R / 64 * 64;
+  std::vector<TuneRow> t = {{R, pull_max, AR_ONESHOT_PULL, 0, 256}};
+  if (R >= 16) t.push_back({R, kBulkMaxBytesR16 / elem_bytes, AR_ONESHOT_FANOUT_BULK, 0, 0});
+  t.push_back({R, (size_t)-1, AR_ONESHOT_FANOUT, 0, 128});
+  return t;
 }
 
 struct ar_ctx {
@@ -384,7 +393,7 @@ ar_status_t ar_create(int R, size_t max_count, int dtype, ar_handle_t* out) {
   h->max_count = max_count;
   h->device = dev;
   h->num_sms = sms;
-  h->table = builtin_table(R);
+  h->table = builtin_table(R, dtype == AR_FP32 ? 4 : 2);
   const char* env = getenv("AR_TUNING_FILE");
   if (env && *env && !load_table_file(env, &h->table)) {
     fprintf(stderr, "[ar] cannot use AR_TUNING_FILE=%s; keeping the built-in table\n", env);

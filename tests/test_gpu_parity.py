@@ -273,16 +273,25 @@ def test_host_buffer_path():
             G.assert_bitexact(inputs.bits(hout[r]), want, "host path %s rank %d" % (variant, r))
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16, torch.float32],
+                         ids=["bf16", "fp16", "fp32"])
 @pytest.mark.parametrize("R", [2, 4, 8, 16])
-def test_selector_boundaries_bracket_the_measured_crossover(R):
-    """Pull below the crossover (about 0.92 Mi / R elements), fan-out above."""
+def test_selector_boundaries_bracket_the_measured_crossover(R, dtype):
+    """Pull up to about 1.75 MiB / R per rank (fp32: half the elements of
+    bf16/fp16), then fan-out; at R = 16 the bulk-copy fan-out up to 256 KiB
+    per rank first."""
     from shot_allreduce_ranks_gb300 import AllReduce
-    edge = 917504 // R // 64 * 64
-    with AllReduce(R, edge + 4096) as ar:
+    eb = 4 if dtype == torch.float32 else 2
+    edge = 917504 * 2 // eb // R // 64 * 64
+    bulk_edge = 262144 // eb if R >= 16 else edge
+    with AllReduce(R, max(edge, bulk_edge) + 4096, dtype=dtype) as ar:
         assert ar.select(1) == "oneshot_pull"
         assert ar.select(edge) == "oneshot_pull"
-        assert ar.select(edge + 1) == "oneshot_fanout"
-        assert ar.select(edge + 4096) == "oneshot_fanout"
+        if R >= 16:
+            assert ar.select(edge + 1) == "oneshot_fanout_bulk"
+            assert ar.select(bulk_edge) == "oneshot_fanout_bulk"
+        assert ar.select(bulk_edge + 1) == "oneshot_fanout"
+        assert ar.select(bulk_edge + 4096) == "oneshot_fanout"
         ar.set_variant("fused_ll8" if R <= 8 else "twophase")
         assert ar.select(5) == ("fused_ll8" if R <= 8 else "twophase")
 
