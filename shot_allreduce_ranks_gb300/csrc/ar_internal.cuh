@@ -319,7 +319,36 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 struct LaunchCfg {
   int ctas;
   int threads;
+  bool pdl = false;  // launch with programmatic dependent launch (plain kernels only)
 };
+
+// Programmatic dependent launch.  A kernel launched with cfg.pdl may be
+// scheduled while the previous kernel in its stream is still running; its
+// first statement waits until that kernel has completed and its memory
+// operations are visible (griddepcontrol.wait), then lets the next kernel
+// be scheduled (griddepcontrol.launch_dependents).  No kernel touches global
+// memory before that wait, so results are those of plain stream order; what
+// is saved is the launch gap between back-to-back calls.  Launched without
+// the attribute, both instructions have nothing to wait for or release.
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launch configuration of a plain (non-cooperative) kernel.
+inline cudaLaunchConfig_t plain_config(const LaunchCfg& cfg, dim3 grid, size_t smem,
+                                       cudaStream_t s, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = grid;
+  lc.blockDim = dim3((unsigned)cfg.threads);
+  lc.dynamicSmemBytes = smem;
+  lc.stream = s;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = cfg.pdl ? 1 : 0;
+  return lc;
+}
 
 // Launchers (defined in the kernel translation units).  `dtype` is an
 // ar_dtype_t; each returns the CUDA error of its launch(es).
@@ -354,7 +383,7 @@ constexpr int kBulkThreads = 256;
 size_t bulk_smem_bytes(int R);
 int bulk_ctas_per_sm(int R, int dtype);
 cudaError_t bulk_prepare(int R, int dtype);
-cudaError_t launch_oneshot_fanout_bulk(int R, int dtype, const CallArgs& a, int ctas,
+cudaError_t launch_oneshot_fanout_bulk(int R, int dtype, const CallArgs& a, LaunchCfg cfg,
                                        cudaStream_t s);
 
 // Elements per 16-byte group of an ar_dtype_t (0 for an unknown one).

@@ -39,6 +39,7 @@ __device__ __forceinline__ uint4 reduce_group(const char* const* s_in, size_t g,
 // before any store; one group per iteration above 8 ranks (registers).
 template <int R, class E>
 __global__ void __launch_bounds__(512) k_oneshot_fanout(CallArgs a) {
+  pdl_enter();
   __shared__ const char* s_in[R];
   __shared__ char* s_out[R];
   const bool vec = load_tables<R>(a, s_in, s_out);
@@ -85,6 +86,7 @@ __global__ void __launch_bounds__(512) k_oneshot_fanout(CallArgs a) {
 // chunk write every output instead (the fan-out order, alias-safe).
 template <int R, class E>
 __global__ void __launch_bounds__(512) k_oneshot_pull(CallArgs a) {
+  pdl_enter();
   __shared__ const char* s_in[R];
   __shared__ char* s_out[R];
   __shared__ int s_alias;
@@ -130,18 +132,22 @@ int fanout_ctas_per_sm(int R, int dtype, int threads) {
 
 cudaError_t launch_oneshot_fanout(int R, int dtype, const CallArgs& a, LaunchCfg cfg,
                                   cudaStream_t s) {
-#define L(RR, EE) k_oneshot_fanout<RR, EE><<<cfg.ctas, cfg.threads, 0, s>>>(a)
+  cudaLaunchAttribute attr[1];
+  const cudaLaunchConfig_t lc = plain_config(cfg, dim3((unsigned)cfg.ctas), 0, s, attr);
+#define L(RR, EE) return cudaLaunchKernelEx(&lc, k_oneshot_fanout<RR, EE>, a)
   AR_DISPATCH(dtype, R, L, AR_SWITCH_R16)
 #undef L
-  return cudaGetLastError();
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_oneshot_pull(int R, int dtype, const CallArgs& a, LaunchCfg cfg,
                                 cudaStream_t s) {
-#define L(RR, EE) k_oneshot_pull<RR, EE><<<cfg.ctas, cfg.threads, 0, s>>>(a)
+  cudaLaunchAttribute attr[1];
+  const cudaLaunchConfig_t lc = plain_config(cfg, dim3((unsigned)cfg.ctas), 0, s, attr);
+#define L(RR, EE) return cudaLaunchKernelEx(&lc, k_oneshot_pull<RR, EE>, a)
   AR_DISPATCH(dtype, R, L, AR_SWITCH_R16)
 #undef L
-  return cudaGetLastError();
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace ar

@@ -154,6 +154,7 @@ __device__ __forceinline__ void bulk_issue(uint8_t* in_tiles, const char* const*
 
 template <int R, class E>
 __global__ void __launch_bounds__(kBulkThreads) k_oneshot_fanout_bulk(CallArgs a) {
+  pdl_enter();
   constexpr int S = bulk_stages<R>();
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full[S];
@@ -294,12 +295,19 @@ int bulk_ctas_per_sm(int R, int dtype) {
   return bulk_occ(R, dtype, &n) == cudaSuccess ? n : 0;
 }
 
-cudaError_t launch_oneshot_fanout_bulk(int R, int dtype, const CallArgs& a, int ctas,
+cudaError_t launch_oneshot_fanout_bulk(int R, int dtype, const CallArgs& a, LaunchCfg cfg,
                                        cudaStream_t s) {
-#define L(RR, EE) k_oneshot_fanout_bulk<RR, EE><<<ctas, kBulkThreads, bulk_smem<RR>(), s>>>(a)
+  cudaLaunchAttribute attr[1];
+  cfg.threads = kBulkThreads;
+#define L(RR, EE)                                                                             \
+  {                                                                                           \
+    const cudaLaunchConfig_t lc = plain_config(cfg, dim3((unsigned)cfg.ctas), bulk_smem<RR>(), s, \
+                                               attr);                                         \
+    return cudaLaunchKernelEx(&lc, k_oneshot_fanout_bulk<RR, EE>, a);                         \
+  }
   AR_DISPATCH(dtype, R, L, AR_SWITCH_R16)
 #undef L
-  return cudaGetLastError();
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace ar

@@ -25,6 +25,7 @@ namespace {
 
 template <int R, class E>
 __global__ void __launch_bounds__(512) k_reduce_scatter(CallArgs a) {
+  pdl_enter();
   __shared__ const char* s_in[R];
   __shared__ char* s_out[R];
   const bool vec = load_tables<R>(a, s_in, s_out) && (a.count % E::kGroup == 0);
@@ -46,6 +47,7 @@ __global__ void __launch_bounds__(512) k_reduce_scatter(CallArgs a) {
 
 template <int R, class E>
 __global__ void __launch_bounds__(512) k_all_gather(CallArgs a) {
+  pdl_enter();
   __shared__ const char* s_in[R];
   __shared__ char* s_out[R];
   const bool vec = load_tables<R>(a, s_in, s_out) && (a.count % E::kGroup == 0);
@@ -64,19 +66,21 @@ __global__ void __launch_bounds__(512) k_all_gather(CallArgs a) {
 
 cudaError_t launch_reduce_scatter(int R, int dtype, const CallArgs& a, LaunchCfg cfg,
                                   cudaStream_t s) {
-  const dim3 grid((unsigned)cfg.ctas, (unsigned)R);
-#define L(RR, EE) k_reduce_scatter<RR, EE><<<grid, cfg.threads, 0, s>>>(a)
+  cudaLaunchAttribute attr[1];
+  const cudaLaunchConfig_t lc = plain_config(cfg, dim3((unsigned)cfg.ctas, (unsigned)R), 0, s, attr);
+#define L(RR, EE) return cudaLaunchKernelEx(&lc, k_reduce_scatter<RR, EE>, a)
   AR_DISPATCH(dtype, R, L, AR_SWITCH_R16)
 #undef L
-  return cudaGetLastError();
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_all_gather(int R, int dtype, const CallArgs& a, LaunchCfg cfg, cudaStream_t s) {
-  const dim3 grid((unsigned)cfg.ctas, (unsigned)R);
-#define L(RR, EE) k_all_gather<RR, EE><<<grid, cfg.threads, 0, s>>>(a)
+  cudaLaunchAttribute attr[1];
+  const cudaLaunchConfig_t lc = plain_config(cfg, dim3((unsigned)cfg.ctas, (unsigned)R), 0, s, attr);
+#define L(RR, EE) return cudaLaunchKernelEx(&lc, k_all_gather<RR, EE>, a)
   AR_DISPATCH(dtype, R, L, AR_SWITCH_R16)
 #undef L
-  return cudaGetLastError();
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace ar

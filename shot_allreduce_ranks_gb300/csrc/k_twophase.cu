@@ -21,6 +21,7 @@ namespace {
 // CTA b works for owner b % R on chunk b / R (gridDim.x is a multiple of R).
 template <int R, class E>
 __global__ void __launch_bounds__(512) k_twophase_reduce(CallArgs a) {
+  pdl_enter();
   __shared__ const char* s_in[R];
   __shared__ char* s_out[R];
   const bool vec = load_tables<R>(a, s_in, s_out);
@@ -45,6 +46,7 @@ __global__ void __launch_bounds__(512) k_twophase_reduce(CallArgs a) {
 
 template <int R, class E>
 __global__ void __launch_bounds__(512) k_twophase_broadcast(CallArgs a) {
+  pdl_enter();
   __shared__ const char* s_in[R];
   __shared__ char* s_out[R];
   const bool vec = load_tables<R>(a, s_in, s_out);
@@ -66,15 +68,17 @@ __global__ void __launch_bounds__(512) k_twophase_broadcast(CallArgs a) {
 }  // namespace
 
 cudaError_t launch_twophase(int R, int dtype, const CallArgs& a, LaunchCfg cfg, cudaStream_t s) {
-#define L(RR, EE) k_twophase_reduce<RR, EE><<<cfg.ctas, cfg.threads, 0, s>>>(a)
+  cudaLaunchAttribute attr[1];
+  const cudaLaunchConfig_t lc = plain_config(cfg, dim3((unsigned)cfg.ctas), 0, s, attr);
+  cudaError_t e = cudaErrorInvalidValue;
+#define L(RR, EE) e = cudaLaunchKernelEx(&lc, k_twophase_reduce<RR, EE>, a)
   AR_DISPATCH(dtype, R, L, AR_SWITCH_R16)
 #undef L
-  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || R == 1) return e;
-#define L(RR, EE) k_twophase_broadcast<RR, EE><<<cfg.ctas, cfg.threads, 0, s>>>(a)
+#define L(RR, EE) e = cudaLaunchKernelEx(&lc, k_twophase_broadcast<RR, EE>, a)
   AR_DISPATCH(dtype, R, L, AR_SWITCH_R16)
 #undef L
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace ar

@@ -311,3 +311,51 @@ def test_tuning_file_and_forced_variant_env(tmp_path, monkeypatch):
     monkeypatch.setenv("AR_VARIANT", "twophase")
     with AllReduce(4, 100) as ar:
         assert ar.select(10) == "twophase"
+
+
+@pytest.mark.parametrize("pdl", ["1", "0"], ids=["pdl", "no_pdl"])
+@pytest.mark.parametrize("variant", ["oneshot_pull", "oneshot_fanout", "twophase",
+                                     "oneshot_fanout_bulk"])
+def test_chained_calls_see_the_previous_result(variant, pdl, monkeypatch):
+    """Each call reads the previous call's outputs, with no host
+    synchronisation in between, eagerly and replayed from a CUDA graph.
+    With programmatic dependent launch a call is scheduled before the
+    previous one has finished; it must still read that call's results."""
+    import oracle
+    from shot_allreduce_ranks_gb300 import AllReduce
+    monkeypatch.setenv("AR_PDL", pdl)
+    R, count, calls = 8, 30_001, 6
+    xs = inputs.make_inputs(R, count, seed=5, fill="ints")
+    cur = [inputs.bits(x) for x in xs]
+    for _ in range(calls):
+        cur = oracle.allreduce_bf16(cur)
+    want = cur[0]
+    with AllReduce(R, count) as ar:
+        ar.set_variant(variant)
+        a = G.to_device(xs)
+        b = [torch.empty_like(t) for t in a]
+        tabs = [ar.tables(a, b), ar.tables(b, a)]
+
+        def chain():
+            for k in range(calls):
+                ar.allreduce_tables(*tabs[k % 2], count)
+
+        chain()
+        torch.cuda.synchronize()
+        G.check_all_outputs(a if calls % 2 == 0 else b, want, "%s eager" % variant)
+        for t, x in zip(a, xs):
+            t.copy_(x)
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                chain()
+        torch.cuda.synchronize()
+        for t, x in zip(a, xs):
+            t.copy_(x)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        G.check_all_outputs(a if calls % 2 == 0 else b, want, "%s graph" % variant)
+        assert ar.device_status() == 0
