@@ -11,6 +11,8 @@
 #include <new>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "ar_internal.cuh"
 
 using ar::CallArgs;
@@ -110,6 +112,29 @@ struct ar_ctx {
 namespace {
 
 ar_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? AR_OK : AR_ERR_CUDA; }
+
+// An NVTX range around the host side of one call (what a profiler's timeline
+// shows as the call's enqueue).  Without a tool attached it costs a check.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+
+const char* range_name(int variant) {
+  switch (variant) {
+    case AR_ONESHOT_PULL: return "ar oneshot_pull";
+    case AR_ONESHOT_FANOUT: return "ar oneshot_fanout";
+    case AR_TWOPHASE: return "ar twophase";
+    case AR_FUSED_LL8: return "ar fused_ll8";
+    case AR_ONESHOT_FANOUT_BULK: return "ar oneshot_fanout_bulk";
+    case AR_FUSED_LL8_STAGED: return "ar fused_ll8_staged";
+    case AR_PACKET_3OP: return "ar packet_3op";
+    case AR_FUSED_LL8_RING: return "ar fused_ll8_ring";
+    default: return "ar ?";
+  }
+}
 
 bool is_packet_variant(int v) {
   return v == AR_FUSED_LL8 || v == AR_FUSED_LL8_STAGED || v == AR_PACKET_3OP ||
@@ -280,6 +305,7 @@ ar_status_t check_device(const ar_ctx* h) {
 
 ar_status_t launch(ar_ctx* h, int variant, const TuneRow* row, const void* const* d_in,
                    void* const* d_out, size_t count, cudaStream_t s) {
+  NvtxRange range(range_name(variant));
   CallArgs a;
   if (is_packet_variant(variant) && h->R > AR_MAX_PACKET_RANKS) return AR_ERR_UNSUPPORTED;
   a.in_tbl = reinterpret_cast<const char* const*>(d_in);
@@ -558,6 +584,7 @@ static ar_status_t launch_block_collective(ar_handle_t h, bool rs, const void* c
   if (!h || !d_in || !d_out) return AR_ERR_INVALID_ARG;
   if (block == 0) return AR_OK;
   if (block > h->max_count / (size_t)h->R) return AR_ERR_INVALID_ARG;
+  NvtxRange range(rs ? "ar reduce_scatter" : "ar all_gather");
   ar_status_t st = check_device(h);
   if (st != AR_OK) return st;
   CallArgs a;
@@ -649,6 +676,7 @@ ar_status_t ar_allreduce_host(ar_handle_t h, const void* const* h_in, void* cons
   if (count == 0) return AR_OK;
   ar_status_t st = check_device(h);
   if (st != AR_OK) return st;
+  NvtxRange range("ar allreduce_host");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   for (int r = 0; r < h->R; ++r)
     if (!h_in[r] || !h_out[r]) return AR_ERR_INVALID_ARG;
