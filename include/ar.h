@@ -59,9 +59,9 @@
  * #3850, region-lifetime commit) has the same precondition.)
  *
  * Launch overlap: the one-shot, two-phase, bulk fan-out, reduce-scatter and
- * all-gather kernels of a call that moves at most 16 MiB are launched with
- * programmatic dependent launch, so they may be scheduled while the previous
- * kernel in the stream is still running; each waits for that kernel to
+ * all-gather kernels of a call that moves at most 16 MiB (two-phase: 8 MiB)
+ * are launched with programmatic dependent launch, so they may be scheduled
+ * while the previous kernel in the stream is still running; each waits for that kernel to
  * complete (and its writes to be visible) before touching global memory, so
  * results are those of plain stream order.  The environment variable
  * AR_PDL=0, read by ar_create, turns this off.  The cooperative fused

@@ -99,9 +99,12 @@ struct ar_ctx {
   // calls that move at most pdl_max_bytes (AR_PDL=0: never).  Measured at
   // R = 8, bf16, back-to-back graph-replayed calls: pull 2.34 vs 2.52 us at
   // 4 Ki elements, 2.78 vs 3.15 at 64 Ki; fan-out 3.39 vs 3.77 at 256 Ki;
-  // but two-phase 11.2 vs 9.7 us at 1 Mi (32 MiB moved), hence 16 MiB.
+  // but two-phase 11.2 vs 9.7 us at 1 Mi (32 MiB moved), hence 16 MiB; and
+  // two-phase at R = 16 was slower with it already at 16 MiB (11.1 vs 7.1 us
+  // at 256 Ki) while faster at R = 8 up to 8 MiB, hence 8 MiB for it.
   bool pdl = true;
   size_t pdl_max_bytes = (size_t)16 << 20;
+  size_t pdl_max_bytes_twophase = (size_t)8 << 20;
 
   // host-buffer path
   char* staging = nullptr;        // 2 * R buffers of max_count elements
@@ -316,7 +319,8 @@ ar_status_t launch(ar_ctx* h, int variant, const TuneRow* row, const void* const
   a.state = h->state;
   a.spin_limit_ns = h->spin_limit_ns;
   LaunchCfg cfg = shape(h, variant, row, a.groups, a.shard_groups);
-  cfg.pdl = h->pdl && 2 * (size_t)h->R * count * h->elem_bytes <= h->pdl_max_bytes;
+  cfg.pdl = h->pdl && 2 * (size_t)h->R * count * h->elem_bytes <=
+                         (variant == AR_TWOPHASE ? h->pdl_max_bytes_twophase : h->pdl_max_bytes);
   if (h->log)
     fprintf(stderr, "[ar] R=%d count=%zu variant=%s ctas=%d threads=%d pdl=%d\n", h->R, count,
             ar_variant_name(variant), cfg.ctas, cfg.threads, (int)cfg.pdl);
