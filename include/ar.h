@@ -167,7 +167,7 @@ ar_status_t ar_create(int R, size_t max_count, int dtype, ar_handle_t* out);
  * detects exact aliasing on the device and then writes every output from
  * one CTA per chunk.  Partially overlapping buffers are undefined.
  * Alignment: buffers 16-byte aligned take 16-byte vector loads and stores;
- * any misaligned pointer switches that call to 2-byte element accesses
+ * any misaligned pointer switches that call to element-sized accesses
  * (same result, slower), decided on the device.
  * Allocates nothing, synchronises nothing, so it can be captured into a CUDA
  * graph; the fused kernel's epoch lives on the device and rotates on every
@@ -195,7 +195,8 @@ ar_status_t ar_allreduce(ar_handle_t h, const void* const* d_in_tbl,
  * outputs R*sendcount; R*sendcount <= max_count.
  * Both: device pointer tables as in ar_allreduce; outputs must not overlap
  * inputs; 16-byte vectors when every pointer is 16-byte aligned and the
- * block length is a multiple of 8, else 2-byte accesses; one launch, no
+ * block length is a multiple of the 16-byte group (8 elements of 2 bytes,
+ * 4 of fp32), else element-sized accesses; one launch, no
  * allocation, no synchronisation.  Errors: AR_ERR_INVALID_ARG (NULL handle
  * or table, block too large), AR_ERR_CUDA (launch).  A block of 0 returns
  * AR_OK without a launch.
