@@ -161,3 +161,27 @@ def test_packet_variants_need_at_most_8_ranks():
     ar.set_variant("auto")
     ar(xs)
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("R", [4, 16])
+@pytest.mark.parametrize("dtype", [torch.float16, torch.float32], ids=["fp16", "fp32"])
+def test_host_buffer_paths(dtype, R):
+    """ar_allreduce_host for the other element types and for R > 8: page-locked
+    buffers (kernel on the host memory in place) and pageable ones (staging)."""
+    count = 70_001
+    ar = handle(R, count, dtype)
+    ar.reserve_host_staging()
+    xs = inputs.make_inputs(R, count, 17, "normal", dtype)
+    want = expect(xs, dtype)
+    pinned_in = [x.pin_memory() for x in xs]
+    pinned_out = [torch.empty(count, dtype=dtype).pin_memory() for _ in range(R)]
+    pageable_out = [torch.empty(count, dtype=dtype) for _ in range(R)]
+    variants = ["auto", "oneshot_fanout", "twophase"] + (["fused_ll8"] if R <= 8 else [])
+    for v in variants:
+        ar.set_variant(v)
+        ar.allreduce_host(pinned_in, pinned_out)
+        ar.allreduce_host(xs, pageable_out)
+        torch.cuda.synchronize()
+        check(pinned_out, want, dtype, "host page-locked %s R=%d" % (v, R))
+        check(pageable_out, want, dtype, "host pageable %s R=%d" % (v, R))
+    ar.set_variant("auto")
