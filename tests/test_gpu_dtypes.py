@@ -185,3 +185,26 @@ def test_host_buffer_paths(dtype, R):
         check(pinned_out, want, dtype, "host page-locked %s R=%d" % (v, R))
         check(pageable_out, want, dtype, "host pageable %s R=%d" % (v, R))
     ar.set_variant("auto")
+
+
+@pytest.mark.parametrize("block", [4096 + 24, 1001], ids=["vector", "element"])
+@pytest.mark.parametrize("R", [4, 8])
+@pytest.mark.parametrize("dtype", [torch.float16, torch.float32], ids=["fp16", "fp32"])
+def test_reduce_scatter_and_all_gather_types(dtype, R, block):
+    """fp16/fp32 reduce-scatter and all-gather on both access paths: a block
+    that is a whole number of 16-byte groups (vector path) and one that is
+    not (element path).  Reduce-scatter block r must equal block r of the
+    oracle's allreduce; all-gather must be the plain concatenation."""
+    ar = handle(R, R * block, dtype)
+    big = inputs.make_inputs(R, R * block, seed=3, dtype=dtype)
+    rs = ar.reduce_scatter([x.cuda() for x in big], recvcount=block)
+    ag = ar.all_gather([x[:block].cuda() for x in big], sendcount=block)
+    torch.cuda.synchronize()
+    full = expect(big, dtype)
+    cat = np.concatenate([inputs.bits(x[:block]) for x in big])
+    for r in range(R):
+        got = inputs.bits(rs[r].cpu())
+        want = full[r * block:(r + 1) * block]
+        keep = ~(nan_mask(got, dtype) & nan_mask(want, dtype))
+        assert np.array_equal(got[keep], want[keep]), "reduce-scatter rank %d" % r
+        assert np.array_equal(inputs.bits(ag[r].cpu()), cat), "all-gather rank %d" % r

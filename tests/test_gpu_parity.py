@@ -359,3 +359,29 @@ def test_chained_calls_see_the_previous_result(variant, pdl, monkeypatch):
         torch.cuda.synchronize()
         G.check_all_outputs(a if calls % 2 == 0 else b, want, "%s graph" % variant)
         assert ar.device_status() == 0
+
+
+@pytest.mark.parametrize("variant", ["oneshot_fanout", "oneshot_pull", "twophase"])
+def test_two_handles_on_two_streams(variant):
+    """One handle per concurrent stream (the threading rule of ar.h): two
+    handles run calls on two streams at the same time, inputs changing every
+    call, and every call of each stream is exact."""
+    import oracle
+    from shot_allreduce_ranks_gb300 import AllReduce
+    R, count, calls = 8, 200_003, 4
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    with AllReduce(R, count) as h1, AllReduce(R, count) as h2:
+        h1.set_variant(variant)
+        h2.set_variant(variant)
+        runs = []
+        for k in range(calls):
+            for h, s, seed in ((h1, s1, 300 + k), (h2, s2, 400 + k)):
+                xs = inputs.make_inputs(R, count, seed=seed)
+                with torch.cuda.stream(s):
+                    xd = [x.to(G.DEV, non_blocking=False) for x in xs]
+                    outs = h(xd, stream=s)
+                runs.append((xs, outs))
+        torch.cuda.synchronize()
+        for k, (xs, outs) in enumerate(runs):
+            want = oracle.allreduce_bf16([inputs.bits(x) for x in xs])[0]
+            G.check_all_outputs(outs, want, "%s stream %d call %d" % (variant, k % 2, k // 2))
