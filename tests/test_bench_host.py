@@ -10,6 +10,8 @@ import torch.multiprocessing as mp
 
 import bench
 
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
 
 def test_alg_bytes_match_the_roofline_table():
     # R = 8, 512x8192 bf16 per rank
@@ -103,3 +105,23 @@ def test_warmup_floor():
 def test_spread_of_per_call_times():
     s = bench.spread([t * 1e-6 for t in (5.0, 1.0, 3.0, 2.0, 4.0)])
     assert s == {"median": 3.0, "min": 1.0, "p90": 5.0, "max": 5.0, "calls": 5}
+
+
+def test_reference_arm_prints_one_contract_line():
+    """bench.py --impl reference times the oracle on the host (no GPU) and
+    prints one JSON line carrying the contract's keys."""
+    import json
+    import subprocess
+    import sys
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "3", "--warmup", "3", "--workload", "r8_4096"],
+                       capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "us/call" and d["value"] > 0
+    assert d["higher_is_better"] is False and d["metric"] == bench.METRIC
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    assert d["config"]["workload"] == "r8_4096"
