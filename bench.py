@@ -571,6 +571,8 @@ def run_ours(args):
                 "us_per_call": round(t * 1e6 / min(args.steps, 2000), 3),
                 "alg_GBps": round(g, 1), "frac_of_measured": round(g / peak, 4),
                 "frac_of_nominal_8tbs": round(g / NOMINAL_HBM_GBS, 4)}
+        if art.device_status(stream) != 0:
+            raise RuntimeError("device error word set during the 512x8192 extras")
         art.close()
 
     line = {
@@ -593,6 +595,12 @@ def run_ours(args):
         "clocks": clocks,
         "extra": extra,
     }
+    # Every call of the run must have completed without a device-side timeout:
+    # a packet wait that gave up leaves undefined outputs, so fail loudly.
+    status = ar.device_status(stream)
+    if status != 0:
+        raise RuntimeError("device error word set during the run (status %d)" % status)
+    line["device_status"] = "ok"
     ar.close()
     if rank == 0:
         print(json.dumps(line), flush=True)
