@@ -208,3 +208,18 @@ def test_reduce_scatter_and_all_gather_types(dtype, R, block):
         keep = ~(nan_mask(got, dtype) & nan_mask(want, dtype))
         assert np.array_equal(got[keep], want[keep]), "reduce-scatter rank %d" % r
         assert np.array_equal(inputs.bits(ag[r].cpu()), cat), "all-gather rank %d" % r
+
+
+@pytest.mark.parametrize("count", [(1 << 20) - 4, 1 << 20, (1 << 20) + 4 + 1],
+                         ids=["below", "at", "odd_and_partial"])
+def test_fp32_fanout_wide_requests(count):
+    """fp32 fan-out around the 32-byte path's threshold (2^18 groups of 4)."""
+    R = 8
+    ar = handle(R, (1 << 20) + 64, torch.float32)
+    xs = inputs.make_inputs(R, count, 23, "normal", torch.float32)
+    want = expect(xs, torch.float32)
+    ar.set_variant("oneshot_fanout")
+    outs = ar([x.cuda() for x in xs])
+    torch.cuda.synchronize()
+    check(outs, want, torch.float32, "fp32 fanout count=%d" % count)
+    ar.set_variant("auto")

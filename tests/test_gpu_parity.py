@@ -385,3 +385,35 @@ def test_two_handles_on_two_streams(variant):
         for k, (xs, outs) in enumerate(runs):
             want = oracle.allreduce_bf16([inputs.bits(x) for x in xs])[0]
             G.check_all_outputs(outs, want, "%s stream %d call %d" % (variant, k % 2, k // 2))
+
+
+WIDE = 1 << 21  # bf16 elements in 2^18 groups: where the fan-out starts 32-byte requests
+
+
+@pytest.mark.parametrize("count", [WIDE - 8, WIDE, WIDE + 8, WIDE + 8 + 3],
+                         ids=["below", "at", "odd_groups", "odd_and_partial"])
+def test_fanout_wide_requests_edges(count):
+    """The fan-out's 32-byte path for large calls: at and around its size
+    threshold, with an odd number of whole groups and with a partial last
+    group; and pointers that are 16- but not 32-byte aligned, which must take
+    the 16-byte path.  All bit-exact against the oracle."""
+    R = 8
+    ar = G.handle(R, WIDE + 64)
+    xs = inputs.make_inputs(R, count, seed=count % 11)
+    want = G.oracle_expect(xs)
+    ar.set_variant("oneshot_fanout")
+    outs = ar(G.to_device(xs))
+    torch.cuda.synchronize()
+    G.check_all_outputs(outs, want, "fanout count=%d" % count)
+    # 16-byte aligned, not 32-byte aligned: views 8 elements into bigger buffers
+    base_in = [torch.zeros(count + 8, dtype=torch.bfloat16, device=G.DEV) for _ in range(R)]
+    base_out = [torch.zeros(count + 8, dtype=torch.bfloat16, device=G.DEV) for _ in range(R)]
+    vin = [b[8:] for b in base_in]
+    vout = [b[8:] for b in base_out]
+    assert all(v.data_ptr() % 32 == 16 for v in vin + vout)
+    for v, x in zip(vin, xs):
+        v.copy_(x)
+    ar(vin, vout)
+    torch.cuda.synchronize()
+    G.check_all_outputs(vout, want, "fanout 16B-aligned count=%d" % count)
+    ar.set_variant("auto")
