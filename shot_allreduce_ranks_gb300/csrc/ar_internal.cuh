@@ -211,6 +211,34 @@ struct Acc<F32> {
   }
 };
 
+// 32-byte global accesses (two adjacent groups), L1 not allocated.  Both
+// addresses must be 32-byte aligned.
+__device__ __forceinline__ void ld_wide(const char* p, uint4& lo, uint4& hi) {
+  uint64_t w0, w1, w2, w3;
+  asm volatile("ld.global.L1::no_allocate.v4.b64 {%0,%1,%2,%3}, [%4];"
+               : "=l"(w0), "=l"(w1), "=l"(w2), "=l"(w3)
+               : "l"(p));
+  lo = make_uint4((uint32_t)w0, (uint32_t)(w0 >> 32), (uint32_t)w1, (uint32_t)(w1 >> 32));
+  hi = make_uint4((uint32_t)w2, (uint32_t)(w2 >> 32), (uint32_t)w3, (uint32_t)(w3 >> 32));
+}
+
+__device__ __forceinline__ void st_wide(char* p, uint4 lo, uint4 hi) {
+  const uint64_t w0 = lo.x | ((uint64_t)lo.y << 32), w1 = lo.z | ((uint64_t)lo.w << 32);
+  const uint64_t w2 = hi.x | ((uint64_t)hi.y << 32), w3 = hi.z | ((uint64_t)hi.w << 32);
+  asm volatile("st.global.L1::no_allocate.v4.b64 [%0], {%1,%2,%3,%4};" ::"l"(p), "l"(w0), "l"(w1),
+               "l"(w2), "l"(w3)
+               : "memory");
+}
+
+// Calls with at least this many 16-byte groups per rank (4 MiB) use 32-byte
+// requests where the kernels allow them: measured faster from ~2 Mi bf16
+// elements per rank up and slower below (R = 8, GB300).
+constexpr size_t kWideMinGroups = (size_t)1 << 18;
+
+__device__ __forceinline__ bool aligned32(const void* p) {
+  return (reinterpret_cast<uintptr_t>(p) & 31u) == 0;
+}
+
 // One element's bits (2 or 4 bytes) at p.
 template <int kBytes>
 __device__ __forceinline__ uint32_t ld_elem(const char* p) {

@@ -43,26 +43,6 @@ __device__ __forceinline__ uint4 reduce_group(const char* const* s_in, size_t g,
 // Grid-stride over groups, two groups (g, g + stride) per iteration for
 // R <= 8 so that 2R independent 16-byte loads are in flight per thread
 // before any store; one group per iteration above 8 ranks (registers).
-constexpr size_t kWideMinGroups = (size_t)1 << 18;  // 4 MiB per rank
-
-// 32-byte global accesses (two adjacent groups), L1 not allocated.
-__device__ __forceinline__ void ld_wide(const char* p, uint4& lo, uint4& hi) {
-  uint64_t w0, w1, w2, w3;
-  asm volatile("ld.global.L1::no_allocate.v4.b64 {%0,%1,%2,%3}, [%4];"
-               : "=l"(w0), "=l"(w1), "=l"(w2), "=l"(w3)
-               : "l"(p));
-  lo = make_uint4((uint32_t)w0, (uint32_t)(w0 >> 32), (uint32_t)w1, (uint32_t)(w1 >> 32));
-  hi = make_uint4((uint32_t)w2, (uint32_t)(w2 >> 32), (uint32_t)w3, (uint32_t)(w3 >> 32));
-}
-
-__device__ __forceinline__ void st_wide(char* p, uint4 lo, uint4 hi) {
-  const uint64_t w0 = lo.x | ((uint64_t)lo.y << 32), w1 = lo.z | ((uint64_t)lo.w << 32);
-  const uint64_t w2 = hi.x | ((uint64_t)hi.y << 32), w3 = hi.z | ((uint64_t)hi.w << 32);
-  asm volatile("st.global.L1::no_allocate.v4.b64 [%0], {%1,%2,%3,%4};" ::"l"(p), "l"(w0), "l"(w1),
-               "l"(w2), "l"(w3)
-               : "memory");
-}
-
 // Fan-out with 32-byte requests: pair p = groups 2p and 2p+1 of every rank;
 // the last whole group (if the count of whole groups is odd) and a partial
 // group go one group at a time.  Every pointer is 32-byte aligned.
@@ -104,12 +84,10 @@ __global__ void __launch_bounds__(512) k_oneshot_fanout(CallArgs a) {
   const bool vec = load_tables<R>(a, s_in, s_out);
   if constexpr (R <= 8) {
     if (vec && a.groups >= kWideMinGroups) {
-      bool aligned32 = true;
+      bool all32 = true;
 #pragma unroll
-      for (int s = 0; s < R; ++s)
-        aligned32 = aligned32 && ((reinterpret_cast<uintptr_t>(s_in[s]) |
-                                   reinterpret_cast<uintptr_t>(s_out[s])) & 31u) == 0;
-      if (aligned32) {
+      for (int s = 0; s < R; ++s) all32 = all32 && aligned32(s_in[s]) && aligned32(s_out[s]);
+      if (all32) {
         fanout_wide<R, E>(a, s_in, s_out);
         return;
       }

@@ -83,3 +83,44 @@ def test_block_bounds():
     assert all(o.numel() == 25 for o in outs)
     np.testing.assert_array_equal(G.device_bits(outs[0]),
                                   oracle.reduce_scatter_bf16([inputs.bits(x.cpu()) for x in xs])[0])
+
+
+@pytest.mark.parametrize("R,block", [(8, 281_600), (8, 281_608), (16, 131_072)],
+                         ids=["r8_even_groups", "r8_odd_groups", "r16"])
+def test_large_blocks_and_32_byte_requests(R, block):
+    """Large blocks (the benchmark message split R ways, even and odd group
+    counts, R = 8 and 16) and pointers that are 16- but not 32-byte aligned;
+    reduce-scatter (R <= 8) and all-gather."""
+    ar = G.handle(R, R * block + 64)
+    xs = inputs.make_inputs(R, R * block, seed=block % 7, fill="normal")
+    ins = G.to_device(xs)
+    checks = []
+    if R <= 8:
+        want_rs = oracle.reduce_scatter_bf16([inputs.bits(x) for x in xs])
+        checks.append(("RS", ar.reduce_scatter(ins, recvcount=block), want_rs))
+    small = [x[:block] for x in xs]
+    want_ag = oracle.all_gather_bf16([inputs.bits(x) for x in small])
+    checks.append(("AG", ar.all_gather([t[:block].contiguous() for t in ins], sendcount=block),
+                   want_ag))
+    torch.cuda.synchronize()
+    for what, outs, want in checks:
+        for r in range(R):
+            G.assert_bitexact(G.device_bits(outs[r]), want[r], "%s R=%d block=%d rank %d" % (
+                what, R, block, r))
+    # 16-byte aligned, not 32-byte aligned: views 8 elements into larger buffers
+    def offset_copy(ts):
+        out = []
+        for t in ts:
+            b = torch.zeros(t.numel() + 8, dtype=t.dtype, device=G.DEV)
+            v = b[8:]
+            v.copy_(t)
+            out.append(v)
+        return out
+    vins = offset_copy([t[:block] for t in ins])
+    vouts = offset_copy([torch.zeros(R * block, dtype=torch.bfloat16, device=G.DEV)
+                         for _ in range(R)])
+    assert all(v.data_ptr() % 32 == 16 for v in vins + vouts)
+    outs = ar.all_gather(vins, vouts, sendcount=block)
+    torch.cuda.synchronize()
+    for r in range(R):
+        G.assert_bitexact(G.device_bits(outs[r]), want_ag[r], "AG 16B-aligned rank %d" % r)
