@@ -166,9 +166,11 @@ ar_status_t ar_create(int R, size_t max_count, int dtype, ar_handle_t* out);
  * output may alias any input exactly in AR_ONESHOT_FANOUT.  AR_ONESHOT_PULL
  * detects exact aliasing on the device and then writes every output from
  * one CTA per chunk.  Partially overlapping buffers are undefined.
- * Alignment: buffers 16-byte aligned take 16-byte vector loads and stores;
- * any misaligned pointer switches that call to element-sized accesses
- * (same result, slower), decided on the device.
+ * Alignment: buffers 16-byte aligned take 16-byte vector loads and stores
+ * (AR_ONESHOT_FANOUT: 32-byte ones for calls of at least 4 MiB per rank
+ * when every pointer is 32-byte aligned and R <= 8); any misaligned pointer
+ * switches that call to element-sized accesses (same result, slower),
+ * decided on the device.
  * Allocates nothing, synchronises nothing, so it can be captured into a CUDA
  * graph; the fused kernel's epoch lives on the device and rotates on every
  * execution, including graph replays.
