@@ -290,6 +290,19 @@ ar_status_t ar_allreduce_host(ar_handle_t h, const void* const* h_in,
  * call or per ring round, and a stale match needs a full 2^32 wrap).
  */
 ar_status_t ar_debug_skip_producer(ar_handle_t h, int rank);
+
+/* ar_debug_delay_producer -- for every later AR_FUSED_LL8 call (until
+ * cleared with rank -1 or ns 0), the CTAs of virtual rank `rank` wait `ns`
+ * nanoseconds of the device's global timer before their first packet store,
+ * so every owner polls for that rank's packets longer than the others'.
+ * This is the skewed producer of "Add HIP-graph capture coverage for the
+ * sharded-relay collectives" (meta-pytorch/torchcomms #3850, summary:
+ * replays with some ranks delayed so that a stale flag or stale staging
+ * fails deterministically), made on one GPU.  The value is taken at launch,
+ * so a captured call keeps it on every replay.  The wait is bounded (ns <=
+ * 10 ms, AR_ERR_INVALID_ARG above) and shorter than any spin limit a test
+ * sets, so no wait runs out because of it. */
+ar_status_t ar_debug_delay_producer(ar_handle_t h, int rank, uint64_t ns);
 ar_status_t ar_debug_set_epoch(ar_handle_t h, uint32_t epoch);
 ar_status_t ar_debug_get_epoch(ar_handle_t h, uint32_t* epoch);
 

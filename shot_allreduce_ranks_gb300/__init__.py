@@ -206,6 +206,10 @@ class AllReduce:
     def debug_skip_producer(self, rank: int) -> None:
         check(self._lib.ar_debug_skip_producer(self._h, int(rank)), "ar_debug_skip_producer")
 
+    def debug_delay_producer(self, rank: int, ns: int) -> None:
+        check(self._lib.ar_debug_delay_producer(self._h, int(rank), int(ns)),
+              "ar_debug_delay_producer")
+
     def debug_set_epoch(self, epoch: int) -> None:
         check(self._lib.ar_debug_set_epoch(self._h, int(epoch)), "ar_debug_set_epoch")
 

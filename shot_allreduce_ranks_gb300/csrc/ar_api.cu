@@ -87,6 +87,10 @@ struct ar_ctx {
   size_t slot_groups = 0;
   uint64_t spin_limit_ns = 100ull * 1000ull * 1000ull;
   int skip_producer = -1;
+  int delay_rank = -1;         // skewed-producer test hook (persists until cleared)
+  uint64_t delay_ns = 0;
+  int fused_lead = 2;          // tiles the fused kernel scatters ahead of its reduce
+  bool fused_discard = true;   // drop consumed packet lines from L2 (no write-back)
   int fused_threads = 256;
   int fused_ctas_per_sm = 0;   // occupancy at fused_threads
   // Occupancy cache (CTAs per SM) indexed by threads / 32; 0 = not queried.
@@ -283,7 +287,17 @@ LaunchCfg shape(ar_ctx* h, int variant, const TuneRow* row, size_t groups, size_
       c.ctas = (int)(per_rank * (size_t)R);
       break;
     }
-    case AR_FUSED_LL8:
+    case AR_FUSED_LL8: {
+      // One clique per CTA: R warp groups of Tr threads; a persistent grid of
+      // at most the co-resident CTAs, at most one per tile of Tr groups.
+      const int tr = ar::fused_rank_threads(R, c.threads > 0 ? c.threads : h->fused_threads);
+      c.threads = R * tr;
+      const size_t limit =
+          std::max<size_t>(1, (size_t)occupancy(h, variant, c.threads) * (size_t)h->num_sms);
+      size_t ctas = c.ctas > 0 ? (size_t)c.ctas : ceil_div(shard_groups, (size_t)tr);
+      c.ctas = (int)std::max<size_t>(1, std::min(ctas, limit));
+      break;
+    }
     case AR_FUSED_LL8_STAGED: {
       if (c.threads <= 0) c.threads = h->fused_threads;
       const int per_sm = occupancy(h, variant, c.threads);
@@ -298,6 +312,25 @@ LaunchCfg shape(ar_ctx* h, int variant, const TuneRow* row, size_t groups, size_
       break;
   }
   return c;
+}
+
+// Writes a temporary buffer of twice the L2 size on the current device and
+// waits, so that every dirty line L2 held before (the packet scratch just
+// zeroed) has been written back to memory.  The fused kernel drops consumed
+// packet lines from L2 without writing them back, after which they read back
+// as their memory contents: this makes those contents zeros or packets of
+// earlier calls (older flags), never whatever the memory held before.
+cudaError_t write_back_l2(int dev) {
+  int l2 = 0;
+  cudaError_t e = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
+  if (e != cudaSuccess) return e;
+  const size_t bytes = 2 * (size_t)(l2 > 0 ? l2 : (128 << 20));
+  void* tmp = nullptr;
+  if ((e = cudaMalloc(&tmp, bytes)) != cudaSuccess) return e;
+  e = cudaMemset(tmp, 0xA5, bytes);
+  const cudaError_t e2 = cudaDeviceSynchronize();
+  const cudaError_t e3 = cudaFree(tmp);
+  return e != cudaSuccess ? e : e2 != cudaSuccess ? e2 : e3;
 }
 
 ar_status_t check_device(const ar_ctx* h) {
@@ -347,6 +380,11 @@ ar_status_t launch(ar_ctx* h, int variant, const TuneRow* row, const void* const
       f.state = h->state;
       f.spin_limit_ns = h->spin_limit_ns;
       f.skip_producer = h->skip_producer;
+      f.lead = 1;
+      f.discard = 0;
+      f.fast32 = 0;
+      f.delay_rank = -1;
+      f.delay_ns = 0;
       f.ring_depth = h->ring_depth;
       f.progress = h->progress;
       h->skip_producer = -1;
@@ -363,6 +401,11 @@ ar_status_t launch(ar_ctx* h, int variant, const TuneRow* row, const void* const
       f.state = h->state;
       f.spin_limit_ns = h->spin_limit_ns;
       f.skip_producer = h->skip_producer;
+      f.lead = h->fused_lead;
+      f.discard = h->fused_discard ? 1 : 0;
+      f.fast32 = ar::fused_fits_32bit(h->R, a.shard_groups, h->slot_groups);
+      f.delay_rank = h->delay_rank;
+      f.delay_ns = h->delay_ns;
       f.ring_depth = h->ring_depth;
       f.progress = h->progress;
       h->skip_producer = -1;
@@ -450,6 +493,13 @@ ar_status_t ar_create(int R, size_t max_count, int dtype, ar_handle_t* out) {
   h->log = env && env[0] == '1';
   env = getenv("AR_PDL");
   if (env && env[0] == '0') h->pdl = false;
+  env = getenv("AR_FUSED_LEAD");
+  if (env && *env) {
+    const long v = strtol(env, nullptr, 10);
+    if (v >= 1 && v <= 4) h->fused_lead = (int)v;
+  }
+  env = getenv("AR_FUSED_DISCARD");
+  if (env && env[0] == '0') h->fused_discard = false;
 
   const size_t groups = ceil_div(max_count, (size_t)ar::group_elems(dtype));
   // Rounded up to 4 groups so that every slot starts on a 128-byte line.
@@ -458,7 +508,8 @@ ar_status_t ar_create(int R, size_t max_count, int dtype, ar_handle_t* out) {
   h->slot_groups = (ceil_div(groups, (size_t)R) + 3) / 4 * 4;
   h->scratch_bytes =
       packets ? (size_t)R * (size_t)(R - 1) * h->slot_groups * 4 * sizeof(uint64_t) : 0;
-  h->fused_ctas_per_sm = packets ? occupancy(h, AR_FUSED_LL8, h->fused_threads) : 0;
+  h->fused_ctas_per_sm =
+      packets ? occupancy(h, AR_FUSED_LL8, R * ar::fused_rank_threads(R, h->fused_threads)) : 0;
   env = getenv("AR_RING_DEPTH");
   if (env && *env) {
     const long d = strtol(env, nullptr, 10);
@@ -498,6 +549,8 @@ ar_status_t ar_create(int R, size_t max_count, int dtype, ar_handle_t* out) {
                       (h->ring_bytes && cudaMemset(h->ring, 0, h->ring_bytes) != cudaSuccess)))
     st = AR_ERR_CUDA;
   if (st == AR_OK && cudaDeviceSynchronize() != cudaSuccess) st = AR_ERR_CUDA;
+  if (st == AR_OK && h->scratch_bytes && h->fused_discard && write_back_l2(dev) != cudaSuccess)
+    st = AR_ERR_OOM;
   if (st != AR_OK) {
     cudaGetLastError();
     ar_destroy(h);
@@ -565,7 +618,7 @@ ar_status_t ar_query(ar_handle_t h, ar_info_t* info) {
   info->scratch_bytes = 2 * h->scratch_bytes + h->ring_bytes;
   info->num_sms = h->num_sms;
   info->fused_max_ctas = h->fused_ctas_per_sm * h->num_sms;
-  info->fused_threads = h->fused_threads;
+  info->fused_threads = h->R * ar::fused_rank_threads(h->R, h->fused_threads);
   info->device = h->device;
   return AR_OK;
 }
@@ -747,6 +800,13 @@ ar_status_t ar_debug_skip_producer(ar_handle_t h, int rank) {
   return AR_OK;
 }
 
+ar_status_t ar_debug_delay_producer(ar_handle_t h, int rank, uint64_t ns) {
+  if (!h || rank < -1 || rank >= h->R || ns > 10ull * 1000ull * 1000ull) return AR_ERR_INVALID_ARG;
+  h->delay_rank = ns ? rank : -1;
+  h->delay_ns = rank >= 0 ? ns : 0;
+  return AR_OK;
+}
+
 ar_status_t ar_debug_set_epoch(ar_handle_t h, uint32_t epoch) {
   if (!h || epoch == 0) return AR_ERR_INVALID_ARG;
   if (cudaDeviceSynchronize() != cudaSuccess) return AR_ERR_CUDA;
@@ -758,6 +818,8 @@ ar_status_t ar_debug_set_epoch(ar_handle_t h, uint32_t epoch) {
       cudaMemset(h->progress, 0, (size_t)h->R * ar::kRingProgressWords * sizeof(uint32_t)) !=
           cudaSuccess ||
       cudaDeviceSynchronize() != cudaSuccess)
+    return AR_ERR_CUDA;
+  if (h->scratch_bytes && h->fused_discard && write_back_l2(h->device) != cudaSuccess)
     return AR_ERR_CUDA;
   return cuda_status(cudaMemcpy(&h->state->epoch, &epoch, sizeof epoch, cudaMemcpyHostToDevice));
 }

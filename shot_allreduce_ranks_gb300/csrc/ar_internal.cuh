@@ -50,6 +50,17 @@ struct FusedArgs {
   DevState* state;
   uint64_t spin_limit_ns;
   int skip_producer;      // test hook: rank whose packet stores are skipped, or -1
+  // Write-mode fused kernel only.  lead: tiles a CTA scatters ahead of the
+  // tile it reduces (>= 1).  discard: drop consumed packet lines from L2
+  // without writing them back (set only where the scratch's memory contents
+  // are known to hold zeros or older packets, see ar_create).
+  int lead;
+  int discard;
+  int fast32;   // every slot and input group offset of the call fits in 32 bits
+  // Test hook: CTAs of virtual rank delay_rank (or none if -1) wait delay_ns
+  // of %globaltimer before their first packet store (a skewed producer).
+  int delay_rank;
+  uint64_t delay_ns;
   // Ring variant only: packets live in `scratch` as a ring of ring_depth
   // rounds per (owner, source, CTA); progress[(owner, c, warp)] is the flag
   // of the last round that warp of CTA c of `owner` finished reading.
@@ -208,6 +219,75 @@ struct Acc<F32> {
   __device__ __forceinline__ uint4 round() const {
     return make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]),
                       __float_as_uint(v[3]));
+  }
+};
+
+// Packed pairs of fp32 values (low element in the low 32 bits) and their
+// IEEE round-to-nearest-even addition, one instruction for both lanes.  Each
+// lane is exactly a plain fp32 add (no flush of subnormals), so a sum built
+// from these is bit-identical to one built from scalar adds in the same order.
+__device__ __forceinline__ uint64_t f32x2_make(uint32_t lo_bits, uint32_t hi_bits) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo_bits), "r"(hi_bits));
+  return d;
+}
+__device__ __forceinline__ uint64_t f32x2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ void f32x2_split(uint64_t p, float& lo, float& hi) {
+  uint32_t a, b;
+  asm("mov.b64 {%0, %1}, %2;" : "=r"(a), "=r"(b) : "l"(p));
+  lo = __uint_as_float(a);
+  hi = __uint_as_float(b);
+}
+
+// The rank-order accumulator of one group kept as packed pairs: same
+// results as Acc<E>, half the add instructions.
+template <class E>
+struct Acc2 {  // bf16 / fp16: word k of a group holds elements 2k (low) and 2k+1
+  uint64_t v[4];
+  __device__ __forceinline__ static uint64_t widen(uint32_t w) {
+    return f32x2_make(__float_as_uint(E::lo(w)), __float_as_uint(E::hi(w)));
+  }
+  __device__ __forceinline__ void set(uint4 x) {
+    v[0] = widen(x.x);
+    v[1] = widen(x.y);
+    v[2] = widen(x.z);
+    v[3] = widen(x.w);
+  }
+  __device__ __forceinline__ void add(uint4 x) {
+    v[0] = f32x2_add(v[0], widen(x.x));
+    v[1] = f32x2_add(v[1], widen(x.y));
+    v[2] = f32x2_add(v[2], widen(x.z));
+    v[3] = f32x2_add(v[3], widen(x.w));
+  }
+  __device__ __forceinline__ uint4 round() const {
+    float a[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) f32x2_split(v[k], a[2 * k], a[2 * k + 1]);
+    return make_uint4(E::pack(a[0], a[1]), E::pack(a[2], a[3]), E::pack(a[4], a[5]),
+                      E::pack(a[6], a[7]));
+  }
+};
+
+template <>
+struct Acc2<F32> {  // four fp32 elements: two pairs
+  uint64_t v[2];
+  __device__ __forceinline__ void set(uint4 x) {
+    v[0] = f32x2_make(x.x, x.y);
+    v[1] = f32x2_make(x.z, x.w);
+  }
+  __device__ __forceinline__ void add(uint4 x) {
+    v[0] = f32x2_add(v[0], f32x2_make(x.x, x.y));
+    v[1] = f32x2_add(v[1], f32x2_make(x.z, x.w));
+  }
+  __device__ __forceinline__ uint4 round() const {
+    uint32_t a, b, c, d;
+    asm("mov.b64 {%0, %1}, %2;" : "=r"(a), "=r"(b) : "l"(v[0]));
+    asm("mov.b64 {%0, %1}, %2;" : "=r"(c), "=r"(d) : "l"(v[1]));
+    return make_uint4(a, b, c, d);
   }
 };
 
@@ -413,6 +493,23 @@ int bulk_ctas_per_sm(int R, int dtype);
 cudaError_t bulk_prepare(int R, int dtype);
 cudaError_t launch_oneshot_fanout_bulk(int R, int dtype, const CallArgs& a, LaunchCfg cfg,
                                        cudaStream_t s);
+
+// Whether every input group offset (R * shard_groups) and packet slot offset
+// (R * R * slot_groups) of a fused call fits in 32 bits.
+inline int fused_fits_32bit(int R, size_t shard_groups, size_t slot_groups) {
+  const unsigned long long lim = 0xFFFFFFFFull;
+  return (unsigned long long)R * shard_groups < lim &&
+         (unsigned long long)R * (unsigned long long)R * slot_groups < lim;
+}
+
+// The write-mode fused kernel runs one clique per CTA: R warp groups of Tr
+// threads each (Tr a multiple of 32), group r standing for virtual rank r.
+// Tr for a requested CTA size of `threads`: threads / R rounded down to a
+// multiple of 32, at least 32.
+inline int fused_rank_threads(int R, int threads) {
+  const int tr = threads / R / 32 * 32;
+  return tr < 32 ? 32 : tr;
+}
 
 // Elements per 16-byte group of an ar_dtype_t (0 for an unknown one).
 inline int group_elems(int dtype) {

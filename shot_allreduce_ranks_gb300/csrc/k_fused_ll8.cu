@@ -163,12 +163,15 @@ __device__ __forceinline__ Lane packet_prologue(const CallArgs& a, const FusedAr
 // advance; every iteration is at least one L2 round trip) it records a
 // timeout and returns false; it also returns false as soon as another
 // waiter of the same call (identified by its base epoch) has given up.
-template <int R, class Ptr>
-__device__ __forceinline__ bool wait_packets_at(const FusedArgs& f, Packets4 (&pk)[R],
+// With skip >= 0, bit/entry i stands for source i < skip ? i : i + 1 (the
+// array holds only the other ranks' packets); otherwise entry s is source s.
+template <int N, class Ptr>
+__device__ __forceinline__ bool wait_packets_at(const FusedArgs& f, Packets4 (&pk)[N],
                                                 uint32_t pending, uint32_t flag,
-                                                uint32_t call_epoch, int who, Ptr ptr) {
+                                                uint32_t call_epoch, int who, Ptr ptr,
+                                                int skip = -1) {
 #pragma unroll
-  for (int s = 0; s < R; ++s)
+  for (int s = 0; s < N; ++s)
     if ((pending & (1u << s)) && pk[s].arrived(flag)) pending &= ~(1u << s);
   if (!pending) return true;
   uint64_t t_first = 0;
@@ -176,7 +179,7 @@ __device__ __forceinline__ bool wait_packets_at(const FusedArgs& f, Packets4 (&p
   while (pending) {
     __nanosleep(32);
 #pragma unroll
-    for (int s = 0; s < R; ++s) {
+    for (int s = 0; s < N; ++s) {
       if (pending & (1u << s)) {
         pk[s].load(ptr(s));
         if (pk[s].arrived(flag)) pending &= ~(1u << s);
@@ -186,6 +189,8 @@ __device__ __forceinline__ bool wait_packets_at(const FusedArgs& f, Packets4 (&p
       const uint64_t now = global_timer_ns();
       if (spins == 16u) t_first = now;
       if (spins > kMaxSpins || (spins > 16u && now - t_first > f.spin_limit_ns)) {
+        if (skip >= 0)
+          pending = (pending & ((1u << skip) - 1u)) | ((pending >> skip) << (skip + 1));
         report_timeout(f, who, pending, call_epoch);
         return false;
       }
@@ -337,15 +342,237 @@ __device__ __forceinline__ void epoch_advance(const FusedArgs& f, uint32_t epoch
   epoch_advance_to(f, flag_at(epoch, 1));
 }
 
-// Write mode: scatter -> reduce -> broadcast straight into all R outputs.
+// Drops one 128-byte line from L2 without writing it back; its memory
+// contents keep whatever was last written back (an older packet or zeros).
+__device__ __forceinline__ void discard_l2_line(const uint64_t* p) {
+  asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
+// After every lane of a warp has read its packets of the tile starting at
+// group jt: drop the warp's lines (4 groups of 32 bytes each, 8 lines per
+// source for 32 lanes) that hold some group < n of owner r's slots.
+template <int R>
+__device__ __forceinline__ void discard_round(const FusedArgs& f, int r, size_t jt, size_t t,
+                                              size_t n) {
+  const size_t wb = jt + (t & ~(size_t)31);  // the warp's first group
+  for (int i = (int)(t & 31); i < 8 * (R - 1); i += 32) {
+    const size_t line_g = wb + (size_t)(i & 7) * 4;
+    if (line_g < n)
+      discard_l2_line(f.scratch + ((size_t)(r * (R - 1) + (i >> 3)) * f.slot_groups + line_g) * 4);
+  }
+}
+
+// Test hook: a bounded wait of `ns` of %globaltimer (a late producer).
+__device__ __noinline__ void producer_delay(uint64_t ns) {
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 0; i < kMaxSpins && global_timer_ns() - t0 < ns; ++i) __nanosleep(256);
+}
+
+// Write mode: scatter -> reduce -> broadcast straight into all R outputs,
+// pipelined over tiles.
+//
+// A CTA is a clique: R warp groups of Tr threads (Tr a multiple of 32), group
+// r standing for virtual rank r, so producers and owners that exchange
+// packets always sit on the same SM and no CTA ever waits on another.  A
+// tile is Tr consecutive groups of every shard (one group per thread); CTA c
+// works on tiles c, c + C, c + 2C, ... (its rounds).  Iteration k of a warp
+// group scatters its rank's slices of round k (one group per other owner
+// per thread) and reduces its own shard's group of round k - lead, whose
+// packets the clique stored `lead` iterations earlier, so polls mostly
+// succeed at once.  The input slices of round k + 1 are loaded right after
+// round k's packet stores (when their registers are free), so their latency
+// overlaps the reduce.
+//
+// Packets written but not yet read stay within about lead + 1 rounds of the
+// grid (R(R-1) * 32 bytes per tile group), a few tens of MB, so they live in
+// L2 whatever the message size.  With f.discard, after a warp has read its
+// 32 groups of a round (eight 128-byte lines per source) it drops those
+// lines from L2, so consumed packets are never written back to HBM.
+//
+// Two bodies: iterations whose tiles lie wholly inside every shard (whole
+// 16-byte groups, aligned buffers, offsets within 32 bits: nearly all of
+// them) run without per-group checks; the others (the ragged end of the
+// message, misaligned buffers) take the checked body.  Whole tiles come
+// first, so each body is a loop of its own.  Both use the same packet layout
+// and produce the same bits.
+//
+// Deadlock freedom: iteration i of a warp waits only on scatters of round
+// i - lead by warps of its own CTA, done in their iteration i - lead; by
+// induction on i every wait is eventually satisfied.  The waits are bounded
+// all the same.
 template <int R, class E>
 __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, FusedArgs f) {
+  constexpr int RO = R > 1 ? R - 1 : 1;  // entries for the other ranks
   __shared__ const char* s_in[R];
   __shared__ char* s_out[R];
-  const Lane l = packet_prologue<R>(a, f, s_in, s_out);
-  phase_scatter<R, E>(a, f, l, s_in[l.r]);
-  phase_reduce<R, E, true>(a, f, l, s_in[l.r], s_out);
-  epoch_advance(f, l.epoch);
+  __shared__ uint32_t s_epoch;
+  const bool vec = load_tables<R>(a, s_in, s_out);
+  if (threadIdx.x == 0) s_epoch = ld_relaxed_u32(&f.state->epoch);
+  // CTA c is clique c; its warp group r (Tr threads, a multiple of 32)
+  // stands for virtual rank r.
+  const size_t Tr = blockDim.x / R;
+  const int r = (int)(threadIdx.x / Tr);
+  const size_t t = threadIdx.x % Tr;
+  const size_t C = gridDim.x, c = blockIdx.x;
+  const size_t Vs = a.shard_groups;
+  const uint64_t pol_in = l2_policy_evict_first();
+  const size_t g0 = (size_t)r * Vs;  // first group of my shard
+  const size_t my_n = g0 < a.groups ? min(Vs, a.groups - g0) : 0;
+  const size_t tiles = (Vs + Tr - 1) / Tr;
+  const size_t K = c < tiles ? (tiles - c + C - 1) / C : 0;  // rounds of this clique
+  const size_t L = (size_t)(f.lead > 0 ? f.lead : 1);
+  const bool scatter_on = R > 1 && r != f.skip_producer;
+
+  // Fast body: tiles [jt, jt + Tr) with jt + Tr <= fast_vs are whole groups
+  // in every shard (the last shard is the shortest).
+  const size_t whole = a.count / E::kGroup;
+  const size_t fast_vs =
+      (vec && f.fast32 && whole > (size_t)(R - 1) * Vs) ? min(Vs, whole - (size_t)(R - 1) * Vs)
+                                                        : 0;
+  const uint32_t Vs32 = (uint32_t)Vs, SG32 = (uint32_t)f.slot_groups;
+  // Per-rank offsets for q = 1..R-1 (owner o = (r + q) % R), in shared memory
+  // to leave the registers to the data in flight: start of o's shard in
+  // rank r's input, and start of the slot (owner o, source r).
+  __shared__ uint32_t s_in_off[R][RO], s_dst_off[R][RO];
+  if (t > 0 && t < (size_t)R) {
+    const int q = (int)t, o = r + q < R ? r + q : r + q - R;
+    s_in_off[r][q - 1] = (uint32_t)o * Vs32;
+    s_dst_off[r][q - 1] = (uint32_t)(o * (R - 1) + (r < o ? r : r - 1)) * SG32;
+  }
+  __syncthreads();
+  const uint32_t epoch = s_epoch;
+  const char* my_in = s_in[r];
+  // Slot of (owner r, i-th other source in rank order): r * (R - 1) + i.
+  const uint32_t src_row = (uint32_t)(r * (R - 1)) * SG32;
+  const uint32_t own_off = (uint32_t)r * Vs32;
+  // Iterations whose tiles are all whole form a prefix [0, k_fast): tile
+  // c + kC is whole for k < kf.
+  const size_t nf = fast_vs / Tr;
+  const size_t kf = nf > c ? (nf - c + C - 1) / C : 0;
+  const size_t k_fast = kf >= K ? K + L : (scatter_on ? kf : kf + L);
+
+  if (r == f.delay_rank && f.delay_ns) producer_delay(f.delay_ns);
+
+  bool ok = true;
+  size_t k = 0;
+  // The input slices of round k are loaded during iteration k - 1, right
+  // after that iteration's packet stores (when their registers are free), so
+  // their HBM latency overlaps the reduce of iteration k - 1.
+  uint4 x[RO];
+  auto load_slices = [&](size_t kk) {
+    const uint32_t js = (uint32_t)((c + kk * C) * Tr + t);
+#pragma unroll
+    for (int q = 0; q < R - 1; ++q)
+      x[q] = ld_v4_stream<true>(my_in + (size_t)(s_in_off[r][q] + js) * kGroupBytes, pol_in);
+  };
+  if (scatter_on && k_fast > 0 && K > 0) load_slices(0);
+  for (; k < k_fast; ++k) {
+    // ---------------- whole tiles: 32-bit offsets, no per-group checks
+    const size_t jts = (c + k * C) * Tr;                       // scatter tile (round k)
+    const bool rd_round = k >= L;
+    const size_t jtr = rd_round ? (c + (k - L) * C) * Tr : 0;  // reduced tile (round k - L)
+    {
+      const bool sc = scatter_on && k < K;
+      const uint32_t js = (uint32_t)(jts + t), jr = (uint32_t)(jtr + t);
+      Packets4 pk[RO];
+      uint4 own = make_uint4(0, 0, 0, 0);
+      if (rd_round) {
+        own = ld_v4_stream<true>(my_in + (size_t)(own_off + jr) * kGroupBytes, pol_in);
+#pragma unroll
+        for (int i = 0; i < R - 1; ++i)
+          pk[i].load(f.scratch + (size_t)(src_row + (uint32_t)i * SG32 + jr) * 4);
+      }
+      if (sc) {
+#pragma unroll
+        for (int q = 0; q < R - 1; ++q)
+          st_packets(f.scratch + (size_t)(s_dst_off[r][q] + js) * 4, x[q], epoch);
+      }
+      if (scatter_on && k + 1 < K && k + 1 < k_fast) load_slices(k + 1);
+      if (rd_round) {
+        ok = wait_packets_at<RO>(
+            f, pk, R > 1 ? (1u << (R - 1)) - 1u : 0u, epoch, epoch, r,
+            [&](int i) { return f.scratch + (size_t)(src_row + (uint32_t)i * SG32 + jr) * 4; },
+            r);
+        if (ok) {
+          // rank order 0..R-1; entry i of pk is source i (< r) or i + 1 (> r)
+          Acc2<E> acc;
+#pragma unroll
+          for (int s = 0; s < R; ++s) {
+            uint4 v = own;
+            if (s < R - 1 && s < r) v = pk[s < R - 1 ? s : 0].data();
+            else if (s > 0 && s > r) v = pk[s > 0 ? s - 1 : 0].data();
+            if (s == 0) acc.set(v);
+            else acc.add(v);
+          }
+          const uint4 y = acc.round();
+          const size_t goff = (size_t)(own_off + jr) * kGroupBytes;
+#pragma unroll
+          for (int q = 0; q < R; ++q) st_v4_stream(s_out[q] + goff, y);
+        }
+      }
+    }
+    if (!__all_sync(0xFFFFFFFFu, ok)) break;
+    if (R > 1 && f.discard && rd_round) discard_round<R>(f, r, jtr, t, my_n);
+  }
+  for (; ok && k < K + L; ++k) {
+    // ---------------- checked body (ragged end, misaligned buffers)
+    const size_t jts = (c + k * C) * Tr;
+    const bool rd_round = k >= L;
+    const size_t jtr = rd_round ? (c + (k - L) * C) * Tr : 0;
+    {
+      const size_t js = jts + t;
+      const bool sc = scatter_on && k < K && js < Vs;
+      uint4 x[RO];
+      if (sc) {
+#pragma unroll
+        for (int q = 1; q < R; ++q) {
+          const size_t g = (size_t)((r + q) % R) * Vs + js;
+          if (g < a.groups)
+            x[q - 1] = load_group<E, true>(my_in, g, group_valid<E>(g, a.count), vec, pol_in);
+        }
+      }
+      const size_t jr = jtr + t;
+      const bool rd = rd_round && jr < my_n;
+      Packets4 pk[R];
+      uint4 own = make_uint4(0, 0, 0, 0);
+      uint32_t pending = 0;
+      if (rd) {
+        own = load_group<E, true>(my_in, g0 + jr, group_valid<E>(g0 + jr, a.count), vec,
+                                  pol_in);
+#pragma unroll
+        for (int s = 0; s < R; ++s)
+          if (s != r) {
+            pk[s].load(slot_ptr<R>(f.scratch, f.slot_groups, r, s) + jr * 4);
+            pending |= 1u << s;
+          }
+      }
+      if (sc) {
+#pragma unroll
+        for (int q = 1; q < R; ++q) {
+          const int o = (r + q) % R;
+          if ((size_t)o * Vs + js < a.groups)
+            st_packets(slot_ptr<R>(f.scratch, f.slot_groups, o, r) + js * 4, x[q - 1], epoch);
+        }
+      }
+      if (rd) {
+        ok = wait_packets<R>(f, f.scratch, r, jr, pk, pending, epoch);
+        if (ok) {
+          Acc2<E> acc;
+          acc.set(r == 0 ? own : pk[0].data());
+#pragma unroll
+          for (int s = 1; s < R; ++s) acc.add(s == r ? own : pk[s].data());
+          const uint4 y = acc.round();
+          const size_t g = g0 + jr;
+          const int valid = group_valid<E>(g, a.count);
+#pragma unroll
+          for (int q = 0; q < R; ++q) store_group<E>(s_out[q], g, y, valid, vec);
+        }
+      }
+    }
+    if (!__all_sync(0xFFFFFFFFu, ok)) break;
+    if (R > 1 && f.discard && rd_round) discard_round<R>(f, r, jtr, t, my_n);
+  }
+  epoch_advance(f, epoch);
 }
 
 // Without write mode (the packet broadcast of the ARK page): scatter ->
@@ -712,7 +939,9 @@ ar_status_t noalloc_setup(int dev, int R, NoAllocDevice* out) {
     d.sms = sms;
     d.ready = true;
   }
-  if (d.ctas_per_sm[R] == 0) d.ctas_per_sm[R] = ar::fused_ctas_per_sm(R, AR_BF16, kNoAllocThreads);
+  if (d.ctas_per_sm[R] == 0)
+    d.ctas_per_sm[R] =
+        ar::fused_ctas_per_sm(R, AR_BF16, R * ar::fused_rank_threads(R, kNoAllocThreads));
   *out = d;
   return AR_OK;
 }
@@ -748,12 +977,21 @@ extern "C" ar_status_t ar_allreduce_fused_noalloc(int R, const void* const* d_in
   f.state = d.state;
   f.spin_limit_ns = 100ull * 1000ull * 1000ull;
   f.skip_producer = -1;
+  // No discards: nothing guarantees that the fixed array's zeros have reached
+  // memory, so a dropped line could read back as whatever preceded them.
+  f.lead = 1;
+  f.discard = 0;
+  f.fast32 = ar::fused_fits_32bit(R, a.shard_groups, f.slot_groups);
+  f.delay_rank = -1;
+  f.delay_ns = 0;
   f.ring_depth = 0;
   f.progress = nullptr;
-  const size_t limit = (size_t)d.ctas_per_sm[R] * (size_t)d.sms / (size_t)R;
-  size_t per_rank = (a.shard_groups + kNoAllocThreads - 1) / kNoAllocThreads;
-  per_rank = std::max<size_t>(1, std::min(per_rank, limit));
-  ar::LaunchCfg cfg = {(int)(per_rank * (size_t)R), kNoAllocThreads};
+  // One clique of R warp groups per CTA, a persistent grid of co-resident CTAs.
+  const int tr = ar::fused_rank_threads(R, kNoAllocThreads);
+  const size_t limit = (size_t)d.ctas_per_sm[R] * (size_t)d.sms;
+  size_t ctas = (a.shard_groups + (size_t)tr - 1) / (size_t)tr;
+  ctas = std::max<size_t>(1, std::min(ctas, limit));
+  ar::LaunchCfg cfg = {(int)ctas, R * tr};
   return ar::launch_fused_ll8(R, AR_BF16, a, f, cfg, static_cast<cudaStream_t>(stream)) ==
                  cudaSuccess
              ? AR_OK
