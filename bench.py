@@ -62,7 +62,7 @@ def alg_bytes(variant: str, R: int, N: int) -> int:
         return 2 * R * R * N + 2 * R * N
     if variant == "twophase":
         return 4 * R * N + (2 * N if R > 1 else 0)
-    if variant in ("fused_ll8", "fused_ll8_ring"):
+    if variant == "fused_ll8":
         return 4 * R * N + 8 * (R - 1) * N
     if variant in ("fused_ll8_staged", "packet_3op"):
         # plus the reduced shards sent back as packets and read by every rank
@@ -141,7 +141,7 @@ def measured_peaks():
 
 KERNEL_SOURCES = {
     "fused_ll8": "k_fused_ll8.cu", "fused_ll8_staged": "k_fused_ll8.cu",
-    "packet_3op": "k_fused_ll8.cu", "fused_ll8_ring": "k_fused_ll8.cu",
+    "packet_3op": "k_fused_ll8.cu",
     "oneshot_fanout": "k_oneshot.cu",
     "oneshot_pull": "k_oneshot.cu", "oneshot_fanout_bulk": "k_oneshot_bulk.cu",
     "twophase": "k_twophase.cu",
@@ -487,7 +487,7 @@ def run_ours(args):
     extra = {}
     if not args.no_extra:
         for v in ("oneshot_fanout", "oneshot_fanout_bulk", "oneshot_pull", "twophase",
-                  "fused_ll8", "fused_ll8_staged", "packet_3op", "fused_ll8_ring"):
+                  "fused_ll8", "fused_ll8_staged", "packet_3op"):
             if v == args.variant:
                 continue
             t, pv, _, _ = time_variant(ar, sets, N, v, min(args.steps, 2000), 20, stream,
@@ -660,7 +660,7 @@ def run_reference(args):
 # sweep mode: every variant over the benchmark message sizes
 
 SWEEP_VARIANTS = ["oneshot_pull", "oneshot_fanout", "oneshot_fanout_bulk", "twophase",
-                  "fused_ll8", "fused_ll8_ring", "fused_ll8_staged", "packet_3op"]
+                  "fused_ll8", "fused_ll8_staged", "packet_3op"]
 
 
 def sweep_counts():
@@ -684,7 +684,7 @@ def run_sweep(args):
     R = args.sweep_r
     counts = sweep_counts()
     variants = [v for v in SWEEP_VARIANTS
-                if not (R > 8 and v in ("fused_ll8", "fused_ll8_ring", "fused_ll8_staged",
+                if not (R > 8 and v in ("fused_ll8", "fused_ll8_staged",
                                         "packet_3op"))]
     ar = AllReduce(R, max(counts), device=dev, dtype=dtype)
     peak, _ = measured_peaks()
@@ -789,8 +789,7 @@ def parse_args(argv=None):
     p.add_argument("--workload", default="r8_440x5120")
     p.add_argument("--variant", default="fused_ll8",
                    choices=["oneshot_pull", "oneshot_fanout", "twophase", "fused_ll8",
-                            "oneshot_fanout_bulk", "fused_ll8_staged", "packet_3op",
-                            "fused_ll8_ring"])
+                            "oneshot_fanout_bulk", "fused_ll8_staged", "packet_3op"])
     p.add_argument("--timing", choices=["graph", "stream"], default="graph",
                    help="graph: calls replayed from CUDA graphs; stream: plain launches")
     p.add_argument("--e2e-steps", type=int, default=200)

@@ -38,11 +38,6 @@
  *     as three launches (that page's send_packet -> recv_reduce_send_packet
  *     -> recv_packet decomposition).  Both exist to measure what write mode
  *     and fusion save;
- *   - AR_FUSED_LL8_RING is AR_FUSED_LL8 with its packets in a ring of a few
- *     rounds per (owner, source, CTA) instead of a region sized for the
- *     whole message: producers take credits from the owners' progress words
- *     before reusing a slot, and the flag advances once per round, so the
- *     packet footprint stays small enough to live in L2;
  *   - AR_FUSED_LL8 is the single fused scatter -> reduce -> broadcast kernel
  *     synchronised by LL packet flags of "Add monolithic fused packet
  *     allreduce kernel and Model::all_reduce_packet API" (microsoft/ark #254,
@@ -94,7 +89,8 @@ typedef enum {
 typedef enum {
   AR_OK = 0,
   AR_ERR_INVALID_ARG = 1, /* bad R, count, pointer, variant or handle */
-  AR_ERR_UNSUPPORTED = 2, /* unknown dtype, a packet variant with R > 8, or no sm_103 device */
+  AR_ERR_UNSUPPORTED = 2, /* unknown dtype, a packet variant with R > 8, no sm_103 device,
+                             or ar_allreduce_host under stream capture */
   AR_ERR_OOM = 3,         /* device allocation failed in ar_create */
   AR_ERR_CUDA = 4,        /* a CUDA runtime call failed (launch, copy, sync) */
   AR_ERR_TIMEOUT = 5      /* a packet wait inside the fused kernel gave up */
@@ -108,11 +104,10 @@ typedef enum {
   AR_FUSED_LL8 = 4,      /* one persistent kernel: LL8 packet scatter, poll+reduce, write mode */
   AR_ONESHOT_FANOUT_BULK = 5, /* fan-out with tiles moved by bulk (TMA) copies through shared memory */
   AR_FUSED_LL8_STAGED = 6,    /* fused LL8 without write mode: result packets back to every rank */
-  AR_PACKET_3OP = 7,          /* the same three packet phases as three separate launches */
-  AR_FUSED_LL8_RING = 8       /* AR_FUSED_LL8 with packets in a small per-CTA ring (credits) */
+  AR_PACKET_3OP = 7           /* the same three packet phases as three separate launches */
 } ar_variant_t;
 
-#define AR_NUM_VARIANTS 9
+#define AR_NUM_VARIANTS 8
 
 /* Static description of a handle (filled by ar_query). */
 typedef struct {
@@ -138,13 +133,21 @@ typedef struct {
  * packets and the staged variants' result packets), each
  * 32 * R * (R-1) * S bytes with S = ceil(ceil(max_count/G)/R) rounded up
  * to a multiple of 4, G = 8 elements per 16-byte group for bf16/fp16 and 4
- * for fp32 (about 4*(R-1)*max_count bytes for 2-byte types); the ring variant's packet ring (32 * R * (R-1) * 4 *
- * the co-resident threads per rank, independent of max_count) and its
- * progress words; all zeroed here so that no flag matches a live epoch; and
+ * for fp32 (about 4*(R-1)*max_count bytes for 2-byte types), zeroed here
+ * so that no flag matches a live epoch, then written back from L2 to memory
+ * (the fused kernel drops consumed packet lines from L2 without writing
+ * them back, so they read back as these zeros or as older packets); and
  * a small state block (epoch, done counter, error word).  Synchronous; not
  * for stream capture.
  * Errors: AR_ERR_INVALID_ARG (R, max_count, out), AR_ERR_UNSUPPORTED (dtype,
  * or the current device is not compute capability 10.3), AR_ERR_OOM, AR_ERR_CUDA.
+ * Source: the one-shot region of "Add HIP-graph capture coverage for the
+ * sharded-relay collectives" (meta-pytorch/torchcomms #3850, the commit that
+ * ties the region's lifetime to its communicator: created once with it, never
+ * re-created while it lives, so the epoch never resets); scratch and peer
+ * references set up once by Model::all_reduce_packet in "Add monolithic fused
+ * packet allreduce kernel and Model::all_reduce_packet API" (microsoft/ark
+ * #254, Changes).
  */
 ar_status_t ar_create(int R, size_t max_count, int dtype, ar_handle_t* out);
 
@@ -179,6 +182,12 @@ ar_status_t ar_create(int R, size_t max_count, int dtype, ar_handle_t* out);
  * (launch failure).  A packet wait that exceeds the spin limit
  * is reported later by ar_get_device_status (the outputs of that call are
  * then undefined).
+ * Source: the allreduce with every rank's output pointer available inside
+ * the kernel, broadcast once on the host in graph mode, of "optimize
+ * allreduce write mode by broadcast output ptr" (ROCm/aiter #1910,
+ * Motivation and Technical Details); the device array of peer pointers passed
+ * as a kernel argument in "One shot all reduce Example" (pytorch-labs/helion
+ * #245, review discussion); the fused kernel of microsoft/ark #254, Changes.
  */
 ar_status_t ar_allreduce(ar_handle_t h, const void* const* d_in_tbl,
                          void* const* d_out_tbl, size_t count, void* stream);
@@ -188,10 +197,11 @@ ar_status_t ar_allreduce(ar_handle_t h, const void* const* d_in_tbl,
  *   out_r[j] = rne(sum over s in rank order of in_s[r*recvcount + j]),
  * j < recvcount.  Same numerics as ar_allreduce.  Each input holds
  * R*recvcount elements, each output recvcount elements; R*recvcount <=
- * max_count.  It is the "srcStride = recvCount, ownOffset = slot *
- * recvCount" case of the one-shot push-reduce kernel of "Add HIP-graph
+ * max_count.  It is the one-shot push-reduce kernel of "Add HIP-graph
  * capture coverage for the sharded-relay collectives" (meta-pytorch/
- * torchcomms #3850), whose allreduce case is the stride-0 one.
+ * torchcomms #3850) with a per-peer source stride of one block and an owner
+ * offset of the rank's slot times one block; its allreduce case is the one
+ * with a stride of zero.
  * ar_all_gather -- every output is the concatenation of all inputs in rank
  * order: out_r[s*sendcount + j] = in_s[j]; inputs hold sendcount elements,
  * outputs R*sendcount; R*sendcount <= max_count.
@@ -209,11 +219,18 @@ ar_status_t ar_all_gather(ar_handle_t h, const void* const* d_in_tbl,
                           void* const* d_out_tbl, size_t sendcount, void* stream);
 
 /* ar_destroy -- synchronise the device and free everything the handle owns.
- * NULL is accepted.  Returns AR_ERR_CUDA if a free failed. */
+ * NULL is accepted.  Returns AR_ERR_CUDA if a free failed.
+ * Source: the region freed together with its communicator in the
+ * region-lifetime commit of meta-pytorch/torchcomms #3850 (never freeing
+ * leaked a region per communicator). */
 ar_status_t ar_destroy(ar_handle_t h);
 
 /* ar_set_variant -- force a variant for later calls on h (AR_AUTO restores
- * the selector).  AR_ERR_INVALID_ARG for an unknown value. */
+ * the selector).  AR_ERR_INVALID_ARG for an unknown value.
+ * Source: the per-size choice between schedules at measured crossovers of
+ * meta-pytorch/torchcomms #3850 (the commit re-measuring the relay/direct
+ * crossovers), and the fixed block size that cost helion #245's one-shot
+ * kernel at 1m (performance table note). */
 ar_status_t ar_set_variant(ar_handle_t h, int variant);
 
 /* ar_select -- the variant a call of `count` elements would run (the forced
@@ -237,13 +254,19 @@ ar_status_t ar_set_spin_limit_ns(ar_handle_t h, uint64_t ns);
  * `stream` to drain, then read and clear the handle's device error word.
  * AR_OK, AR_ERR_TIMEOUT if some fused call since the last check gave up
  * waiting for packets, AR_ERR_CUDA if the stream did not drain or a copy
- * failed. */
+ * failed.
+ * Source: the stream synchronise replaced by a bounded poll, so that a kernel
+ * that never retires is reported instead of hanging, in the summary of
+ * meta-pytorch/torchcomms #3850. */
 ar_status_t ar_get_device_status(ar_handle_t h, void* stream);
 
 /* ar_query -- fill *info. */
 ar_status_t ar_query(ar_handle_t h, ar_info_t* info);
 
-/* ar_status_string -- static, never NULL. */
+/* ar_status_string -- static, never NULL.
+ * Source: the pages define no such function; it names the status codes
+ * above, whose failure modes (a wait that never ends, reported rather than
+ * hung on) come from the summary of meta-pytorch/torchcomms #3850. */
 const char* ar_status_string(int status);
 
 /* ar_variant_name -- static name of a variant ("auto", "oneshot_pull", ...),
@@ -270,6 +293,11 @@ const char* ar_variant_name(int variant);
  * back into h_out[r].  Returns after enqueueing; the caller synchronises
  * `stream` before reading h_out.  AR_ERR_INVALID_ARG if the staging was not
  * reserved or count > max_count.
+ * Not capturable: a call on a stream that is being captured into a CUDA
+ * graph returns AR_ERR_UNSUPPORTED and enqueues nothing (the device pointer
+ * table is copied from memory that lives only for the duration of the call,
+ * and pageable copies cannot be captured).  Capture ar_allreduce on device
+ * buffers instead.
  */
 ar_status_t ar_reserve_host_staging(ar_handle_t h);
 ar_status_t ar_allreduce_host(ar_handle_t h, const void* const* h_in,
@@ -284,10 +312,10 @@ ar_status_t ar_allreduce_host(ar_handle_t h, const void* const* h_in,
  *
  * ar_debug_set_epoch / ar_debug_get_epoch -- synchronous write / read of
  * the device epoch (for testing the wrap from 2^32-1 to 1, which skips 0).
- * Setting it also zeroes every packet region and the ring progress words,
- * so that no packet or credit left from before the jump can match the new
+ * Setting it also zeroes every packet region (and writes the zeros back to
+ * memory), so that no packet left from before the jump can match the new
  * epoch's flags (in normal use the epoch only moves forward one step per
- * call or per ring round, and a stale match needs a full 2^32 wrap).
+ * call, and a stale match needs a full 2^32 wrap).
  */
 ar_status_t ar_debug_skip_producer(ar_handle_t h, int rank);
 
@@ -317,8 +345,9 @@ ar_status_t ar_debug_get_epoch(ar_handle_t h, uint32_t* epoch);
  *
  * ar_allreduce_fused_noalloc -- the AR_FUSED_LL8 allreduce of bf16 buffers
  * (R <= AR_MAX_PACKET_RANKS) without a handle.
- * Same arguments and result as ar_allreduce (R = rank count, 1..AR_MAX_RANKS;
- * device pointer tables; count elements per rank; stream), but the packet
+ * Same arguments and result as ar_allreduce (R = rank count,
+ * 1..AR_MAX_PACKET_RANKS; device pointer tables; count elements per rank;
+ * stream), but the packet
  * scratch and the epoch/counter/error block live in fixed arrays inside the
  * library's device image (AR_NOALLOC_SCRATCH_BYTES of scratch plus 64 bytes),
  * which every GPU that loads the library holds until the process exits.  It
@@ -337,8 +366,9 @@ ar_status_t ar_debug_get_epoch(ar_handle_t h, uint32_t* epoch);
  *   - A packet wait that gives up (100 ms) is recorded in the device-side
  *     error word, which no entry point reads back for this call; that call's
  *     outputs are then undefined.
- * Errors: AR_ERR_INVALID_ARG (R, NULL table, count too large),
- * AR_ERR_UNSUPPORTED (device ordinal >= 64), AR_ERR_CUDA (set-up or launch).
+ * Errors: AR_ERR_INVALID_ARG (R < 1 or R > AR_MAX_PACKET_RANKS, NULL table,
+ * count too large), AR_ERR_UNSUPPORTED (device ordinal >= 64), AR_ERR_CUDA
+ * (set-up or launch).
  */
 #define AR_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 #define AR_NOALLOC_MAX_COUNT(R)                                                   \

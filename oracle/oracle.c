@@ -6,8 +6,8 @@
  * baseline leg of the benchmark may load it; the library itself never does,
  * and this file shares no code, header or table with the CUDA sources.
  *
- * What is computed.  The pages describe allreduce as "every rank's buffer
- * summed into every rank's output":
+ * What is computed.  Allreduce leaves in every rank's output the element-wise
+ * sum of all ranks' input buffers; the pages show it this way:
  *   - "optimize allreduce write mode by broadcast output ptr" (ROCm/aiter
  *     #1910), Motivation: stage 2 writes the reduced data into every rank's
  *     output through their output pointers;
@@ -108,11 +108,12 @@ int oracle_allreduce_bf16(int R, size_t count, const uint16_t* const* in,
  * Reduce-scatter: the same summation, but rank r keeps only block r.  Rank
  * s's input holds R blocks of `recvcount` elements; rank r's output holds
  *   out[r][j] = bf16_rne(sum over s in rank order of in[s][r*recvcount + j]).
- * This is the "srcStride = recvCount, ownOffset = slot * recvCount" case of
- * the one-shot push-reduce kernel in "Add HIP-graph capture coverage for the
- * sharded-relay collectives" (meta-pytorch/torchcomms #3850, the commit that
- * generalises the one-shot kernel to allreduce), whose allreduce case is the
- * stride-0 one above.  Outputs must not overlap inputs.
+ * This is the one-shot push-reduce kernel of "Add HIP-graph capture coverage
+ * for the sharded-relay collectives" (meta-pytorch/torchcomms #3850, the
+ * commit that generalises the one-shot kernel to allreduce) with a per-peer
+ * source stride of one block and an owner offset of the rank's slot times one
+ * block; its allreduce case, a stride of zero, is the function above.  Outputs
+ * must not overlap inputs.
  */
 int oracle_reduce_scatter_bf16(int R, size_t recvcount, const uint16_t* const* in,
                                uint16_t* const* out) {

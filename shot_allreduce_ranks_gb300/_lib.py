@@ -17,7 +17,7 @@ HEADER = os.path.join(os.path.dirname(PKG), "include", "ar.h")
 AR_OK, AR_ERR_INVALID_ARG, AR_ERR_UNSUPPORTED, AR_ERR_OOM, AR_ERR_CUDA, AR_ERR_TIMEOUT = range(6)
 AR_BF16, AR_FP16, AR_FP32 = 0, 1, 2
 AR_AUTO, AR_ONESHOT_PULL, AR_ONESHOT_FANOUT, AR_TWOPHASE, AR_FUSED_LL8 = range(5)
-AR_ONESHOT_FANOUT_BULK, AR_FUSED_LL8_STAGED, AR_PACKET_3OP, AR_FUSED_LL8_RING = 5, 6, 7, 8
+AR_ONESHOT_FANOUT_BULK, AR_FUSED_LL8_STAGED, AR_PACKET_3OP = 5, 6, 7
 VARIANTS = {
     "auto": AR_AUTO,
     "oneshot_pull": AR_ONESHOT_PULL,
@@ -27,7 +27,6 @@ VARIANTS = {
     "oneshot_fanout_bulk": AR_ONESHOT_FANOUT_BULK,
     "fused_ll8_staged": AR_FUSED_LL8_STAGED,
     "packet_3op": AR_PACKET_3OP,
-    "fused_ll8_ring": AR_FUSED_LL8_RING,
 }
 AR_MAX_RANKS = 16
 AR_MAX_PACKET_RANKS = 8

@@ -78,12 +78,6 @@ struct ar_ctx {
   uint64_t* scratch = nullptr;   // scatter packets
   uint64_t* rscratch = nullptr;  // result packets (staged variants)
   size_t scratch_bytes = 0;      // bytes of each region
-  uint64_t* ring = nullptr;      // ring variant's packets
-  size_t ring_bytes = 0;
-  size_t ring_threads = 0;       // threads per rank the ring can hold (C * T)
-  uint32_t* progress = nullptr;  // ring variant's progress words [R][kMaxRingCtas][kMaxRingWarps]
-  int ring_depth = 4;            // measured best on GB300 (2..4 allowed)
-  int ring_threads_default = 128;
   size_t slot_groups = 0;
   uint64_t spin_limit_ns = 100ull * 1000ull * 1000ull;
   int skip_producer = -1;
@@ -91,12 +85,12 @@ struct ar_ctx {
   uint64_t delay_ns = 0;
   int fused_lead = 2;          // tiles the fused kernel scatters ahead of its reduce
   bool fused_discard = true;   // drop consumed packet lines from L2 (no write-back)
+  bool fused_pdl = true;       // programmatic dependent launch for the write-mode fused kernel
   int fused_threads = 256;
   int fused_ctas_per_sm = 0;   // occupancy at fused_threads
   // Occupancy cache (CTAs per SM) indexed by threads / 32; 0 = not queried.
   int occ_fused[33] = {};
   int occ_staged[33] = {};
-  int occ_ring[33] = {};
   int occ_fanout[33] = {};
   int bulk_ctas_per_sm = 0;    // bulk fan-out (fixed 256 threads)
   // Programmatic dependent launch for the plain (non-cooperative) kernels of
@@ -138,14 +132,12 @@ const char* range_name(int variant) {
     case AR_ONESHOT_FANOUT_BULK: return "ar oneshot_fanout_bulk";
     case AR_FUSED_LL8_STAGED: return "ar fused_ll8_staged";
     case AR_PACKET_3OP: return "ar packet_3op";
-    case AR_FUSED_LL8_RING: return "ar fused_ll8_ring";
     default: return "ar ?";
   }
 }
 
 bool is_packet_variant(int v) {
-  return v == AR_FUSED_LL8 || v == AR_FUSED_LL8_STAGED || v == AR_PACKET_3OP ||
-         v == AR_FUSED_LL8_RING;
+  return v == AR_FUSED_LL8 || v == AR_FUSED_LL8_STAGED || v == AR_PACKET_3OP;
 }
 
 size_t ceil_div(size_t a, size_t b) { return (a + b - 1) / b; }
@@ -208,7 +200,6 @@ int choose(const ar_ctx* h, size_t count, const TuneRow** row) {
 int occupancy(ar_ctx* h, int variant, int threads) {
   int* cache = variant == AR_FUSED_LL8          ? h->occ_fused
                : variant == AR_FUSED_LL8_STAGED ? h->occ_staged
-               : variant == AR_FUSED_LL8_RING   ? h->occ_ring
                                                 : h->occ_fanout;
   const int k = threads / 32;
   if (k < 0 || k > 32) return 0;
@@ -216,7 +207,6 @@ int occupancy(ar_ctx* h, int variant, int threads) {
     const int R = h->R, dt = h->dtype;
     const int n = variant == AR_FUSED_LL8          ? ar::fused_ctas_per_sm(R, dt, threads)
                   : variant == AR_FUSED_LL8_STAGED ? ar::fused_staged_ctas_per_sm(R, dt, threads)
-                  : variant == AR_FUSED_LL8_RING   ? ar::fused_ring_ctas_per_sm(R, dt, threads)
                                                    : ar::fanout_ctas_per_sm(R, dt, threads);
     cache[k] = n > 0 ? n : -1;
   }
@@ -271,19 +261,6 @@ LaunchCfg shape(ar_ctx* h, int variant, const TuneRow* row, size_t groups, size_
       size_t per_rank = std::max<size_t>(1, ceil_div(shard_groups, (size_t)c.threads));
       if (c.ctas > 0) per_rank = std::max<size_t>(1, (size_t)c.ctas / (size_t)R);
       per_rank = std::min(per_rank, std::max<size_t>(1, cap / (size_t)R));
-      c.ctas = (int)(per_rank * (size_t)R);
-      break;
-    }
-    case AR_FUSED_LL8_RING: {
-      // Co-resident, at most kMaxRingCtas per rank, and C * T within the ring.
-      if (c.threads <= 0) c.threads = h->ring_threads_default;
-      const int per_sm = occupancy(h, variant, c.threads);
-      size_t limit = (size_t)per_sm * (size_t)h->num_sms / (size_t)R;
-      limit = std::min(limit, (size_t)ar::kMaxRingCtas);
-      limit = std::min(limit, h->ring_threads / (size_t)c.threads);
-      size_t per_rank = std::max<size_t>(1, ceil_div(shard_groups, (size_t)c.threads));
-      if (c.ctas > 0) per_rank = std::max<size_t>(1, (size_t)c.ctas / (size_t)R);
-      per_rank = std::min(per_rank, limit);
       c.ctas = (int)(per_rank * (size_t)R);
       break;
     }
@@ -354,6 +331,7 @@ ar_status_t launch(ar_ctx* h, int variant, const TuneRow* row, const void* const
   LaunchCfg cfg = shape(h, variant, row, a.groups, a.shard_groups);
   cfg.pdl = h->pdl && 2 * (size_t)h->R * count * h->elem_bytes <=
                          (variant == AR_TWOPHASE ? h->pdl_max_bytes_twophase : h->pdl_max_bytes);
+  if (variant == AR_FUSED_LL8) cfg.pdl = h->pdl && h->fused_pdl;
   if (h->log)
     fprintf(stderr, "[ar] R=%d count=%zu variant=%s ctas=%d threads=%d pdl=%d\n", h->R, count,
             ar_variant_name(variant), cfg.ctas, cfg.threads, (int)cfg.pdl);
@@ -372,25 +350,6 @@ ar_status_t launch(ar_ctx* h, int variant, const TuneRow* row, const void* const
     case AR_ONESHOT_FANOUT_BULK:
       e = ar::launch_oneshot_fanout_bulk(h->R, h->dtype, a, cfg, s);
       break;
-    case AR_FUSED_LL8_RING: {
-      FusedArgs f;
-      f.scratch = h->ring;
-      f.rscratch = nullptr;
-      f.slot_groups = 0;
-      f.state = h->state;
-      f.spin_limit_ns = h->spin_limit_ns;
-      f.skip_producer = h->skip_producer;
-      f.lead = 1;
-      f.discard = 0;
-      f.fast32 = 0;
-      f.delay_rank = -1;
-      f.delay_ns = 0;
-      f.ring_depth = h->ring_depth;
-      f.progress = h->progress;
-      h->skip_producer = -1;
-      e = ar::launch_fused_ll8_ring(h->R, h->dtype, a, f, cfg, s);
-      break;
-    }
     case AR_FUSED_LL8:
     case AR_FUSED_LL8_STAGED:
     case AR_PACKET_3OP: {
@@ -406,8 +365,6 @@ ar_status_t launch(ar_ctx* h, int variant, const TuneRow* row, const void* const
       f.fast32 = ar::fused_fits_32bit(h->R, a.shard_groups, h->slot_groups);
       f.delay_rank = h->delay_rank;
       f.delay_ns = h->delay_ns;
-      f.ring_depth = h->ring_depth;
-      f.progress = h->progress;
       h->skip_producer = -1;
       const int dt = h->dtype;
       e = variant == AR_FUSED_LL8          ? ar::launch_fused_ll8(h->R, dt, a, f, cfg, s)
@@ -447,7 +404,6 @@ const char* ar_variant_name(int variant) {
     case AR_ONESHOT_FANOUT_BULK: return "oneshot_fanout_bulk";
     case AR_FUSED_LL8_STAGED: return "fused_ll8_staged";
     case AR_PACKET_3OP: return "packet_3op";
-    case AR_FUSED_LL8_RING: return "fused_ll8_ring";
     default: return "?";
   }
 }
@@ -498,6 +454,8 @@ ar_status_t ar_create(int R, size_t max_count, int dtype, ar_handle_t* out) {
     const long v = strtol(env, nullptr, 10);
     if (v >= 1 && v <= 4) h->fused_lead = (int)v;
   }
+  env = getenv("AR_FUSED_PDL");
+  if (env && env[0] == '0') h->fused_pdl = false;
   env = getenv("AR_FUSED_DISCARD");
   if (env && env[0] == '0') h->fused_discard = false;
 
@@ -510,17 +468,6 @@ ar_status_t ar_create(int R, size_t max_count, int dtype, ar_handle_t* out) {
       packets ? (size_t)R * (size_t)(R - 1) * h->slot_groups * 4 * sizeof(uint64_t) : 0;
   h->fused_ctas_per_sm =
       packets ? occupancy(h, AR_FUSED_LL8, R * ar::fused_rank_threads(R, h->fused_threads)) : 0;
-  env = getenv("AR_RING_DEPTH");
-  if (env && *env) {
-    const long d = strtol(env, nullptr, 10);
-    if (d >= 2 && d <= ar::kMaxRingDepth) h->ring_depth = (int)d;
-  }
-  for (int t = 128; packets && t <= 512; t *= 2) {
-    const size_t per_rank = std::min<size_t>(
-        (size_t)occupancy(h, AR_FUSED_LL8_RING, t) * (size_t)sms / (size_t)R, ar::kMaxRingCtas);
-    h->ring_threads = std::max(h->ring_threads, per_rank * (size_t)t);
-  }
-  h->ring_bytes = (size_t)R * (size_t)(R - 1) * ar::kMaxRingDepth * h->ring_threads * 32;
   if (ar::bulk_prepare(R, dtype) == cudaSuccess) h->bulk_ctas_per_sm = ar::bulk_ctas_per_sm(R, dtype);
   cudaGetLastError();
 
@@ -537,16 +484,9 @@ ar_status_t ar_create(int R, size_t max_count, int dtype, ar_handle_t* out) {
     if (cudaMemcpy(h->state, &init, sizeof init, cudaMemcpyHostToDevice) != cudaSuccess)
       st = AR_ERR_CUDA;
   }
-  const size_t progress_bytes = (size_t)R * ar::kRingProgressWords * sizeof(uint32_t);
-  if (st == AR_OK && cudaMalloc(&h->progress, progress_bytes) != cudaSuccess) st = AR_ERR_OOM;
-  if (st == AR_OK && h->ring_bytes && cudaMalloc(&h->ring, h->ring_bytes) != cudaSuccess)
-    st = AR_ERR_OOM;
   if (st == AR_OK && h->scratch_bytes &&
       (cudaMemset(h->scratch, 0, h->scratch_bytes) != cudaSuccess ||
        cudaMemset(h->rscratch, 0, h->scratch_bytes) != cudaSuccess))
-    st = AR_ERR_CUDA;
-  if (st == AR_OK && (cudaMemset(h->progress, 0, progress_bytes) != cudaSuccess ||
-                      (h->ring_bytes && cudaMemset(h->ring, 0, h->ring_bytes) != cudaSuccess)))
     st = AR_ERR_CUDA;
   if (st == AR_OK && cudaDeviceSynchronize() != cudaSuccess) st = AR_ERR_CUDA;
   if (st == AR_OK && h->scratch_bytes && h->fused_discard && write_back_l2(dev) != cudaSuccess)
@@ -569,8 +509,6 @@ ar_status_t ar_destroy(ar_handle_t h) {
   if (cudaDeviceSynchronize() != cudaSuccess) st = AR_ERR_CUDA;
   if (h->scratch && cudaFree(h->scratch) != cudaSuccess) st = AR_ERR_CUDA;
   if (h->rscratch && cudaFree(h->rscratch) != cudaSuccess) st = AR_ERR_CUDA;
-  if (h->ring && cudaFree(h->ring) != cudaSuccess) st = AR_ERR_CUDA;
-  if (h->progress && cudaFree(h->progress) != cudaSuccess) st = AR_ERR_CUDA;
   if (h->state && cudaFree(h->state) != cudaSuccess) st = AR_ERR_CUDA;
   if (h->staging && cudaFree(h->staging) != cudaSuccess) st = AR_ERR_CUDA;
   if (h->staging_tables && cudaFree(h->staging_tables) != cudaSuccess) st = AR_ERR_CUDA;
@@ -615,7 +553,7 @@ ar_status_t ar_query(ar_handle_t h, ar_info_t* info) {
   info->R = h->R;
   info->dtype = h->dtype;
   info->max_count = h->max_count;
-  info->scratch_bytes = 2 * h->scratch_bytes + h->ring_bytes;
+  info->scratch_bytes = 2 * h->scratch_bytes;
   info->num_sms = h->num_sms;
   info->fused_max_ctas = h->fused_ctas_per_sm * h->num_sms;
   info->fused_threads = h->R * ar::fused_rank_threads(h->R, h->fused_threads);
@@ -731,10 +669,19 @@ ar_status_t ar_allreduce_host(ar_handle_t h, const void* const* h_in, void* cons
   if (!h || !h_in || !h_out || !h->staging) return AR_ERR_INVALID_ARG;
   if (count > h->max_count) return AR_ERR_INVALID_ARG;
   if (count == 0) return AR_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // Not capturable: the direct path's pointer table is copied from this
+  // call's stack (a captured copy node would keep pointing at it), and the
+  // staging path copies from pageable memory.  Refuse before any other work.
+  cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &capture) != cudaSuccess) {
+    cudaGetLastError();
+    return AR_ERR_CUDA;
+  }
+  if (capture != cudaStreamCaptureStatusNone) return AR_ERR_UNSUPPORTED;
   ar_status_t st = check_device(h);
   if (st != AR_OK) return st;
   NvtxRange range("ar allreduce_host");
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   for (int r = 0; r < h->R; ++r)
     if (!h_in[r] || !h_out[r]) return AR_ERR_INVALID_ARG;
 
@@ -811,12 +758,9 @@ ar_status_t ar_debug_set_epoch(ar_handle_t h, uint32_t epoch) {
   if (!h || epoch == 0) return AR_ERR_INVALID_ARG;
   if (cudaDeviceSynchronize() != cudaSuccess) return AR_ERR_CUDA;
   // A jump of the epoch invalidates the "older flag = not arrived" ordering
-  // for everything written before it: clear every packet and credit.
+  // for everything written before it: clear every packet.
   if ((h->scratch_bytes && (cudaMemset(h->scratch, 0, h->scratch_bytes) != cudaSuccess ||
                             cudaMemset(h->rscratch, 0, h->scratch_bytes) != cudaSuccess)) ||
-      (h->ring_bytes && cudaMemset(h->ring, 0, h->ring_bytes) != cudaSuccess) ||
-      cudaMemset(h->progress, 0, (size_t)h->R * ar::kRingProgressWords * sizeof(uint32_t)) !=
-          cudaSuccess ||
       cudaDeviceSynchronize() != cudaSuccess)
     return AR_ERR_CUDA;
   if (h->scratch_bytes && h->fused_discard && write_back_l2(h->device) != cudaSuccess)

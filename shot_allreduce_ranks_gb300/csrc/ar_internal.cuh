@@ -61,18 +61,7 @@ struct FusedArgs {
   // of %globaltimer before their first packet store (a skewed producer).
   int delay_rank;
   uint64_t delay_ns;
-  // Ring variant only: packets live in `scratch` as a ring of ring_depth
-  // rounds per (owner, source, CTA); progress[(owner, c, warp)] is the flag
-  // of the last round that warp of CTA c of `owner` finished reading.
-  int ring_depth;
-  uint32_t* progress;
 };
-
-constexpr int kMaxRingCtas = 1024;  // CTAs per rank the ring progress array can hold
-constexpr int kMaxRingWarps = 16;   // warps per CTA (512 threads)
-constexpr int kMaxRingDepth = 4;
-// Progress words per rank: one per (CTA, warp).
-constexpr size_t kRingProgressWords = (size_t)kMaxRingCtas * kMaxRingWarps;
 
 // ---------------------------------------------------------------------------
 // Small device helpers.
@@ -470,8 +459,6 @@ cudaError_t launch_fused_ll8_staged(int R, int dtype, const CallArgs& a, const F
                                     LaunchCfg cfg, cudaStream_t s);
 cudaError_t launch_packet_3op(int R, int dtype, const CallArgs& a, const FusedArgs& f,
                               LaunchCfg cfg, cudaStream_t s);
-cudaError_t launch_fused_ll8_ring(int R, int dtype, const CallArgs& a, const FusedArgs& f,
-                                  LaunchCfg cfg, cudaStream_t s);
 // Reduce-scatter / all-gather (k_rs_ag.cu): a.count is the block length;
 // the grid is (cfg.ctas, R).
 cudaError_t launch_reduce_scatter(int R, int dtype, const CallArgs& a, LaunchCfg cfg,
@@ -482,7 +469,6 @@ cudaError_t launch_all_gather(int R, int dtype, const CallArgs& a, LaunchCfg cfg
 // `threads` threads per CTA.
 int fused_ctas_per_sm(int R, int dtype, int threads);
 int fused_staged_ctas_per_sm(int R, int dtype, int threads);
-int fused_ring_ctas_per_sm(int R, int dtype, int threads);
 int fanout_ctas_per_sm(int R, int dtype, int threads);
 
 // Bulk-copy fan-out (k_oneshot_bulk.cu): fixed 256 threads per CTA, dynamic

@@ -74,6 +74,12 @@ __device__ __forceinline__ void st_relaxed_u32(uint32_t* p, uint32_t v) {
   asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // Four packets of one group in one 32-byte access, flag in the high half of
 // every 64-bit word.  Stores ask L2 to keep the line (it is read back soon by
 // the owner); loads mark it evict-first once read.  As a vector access, the
@@ -330,12 +336,9 @@ __device__ __forceinline__ void epoch_advance_to(const FusedArgs& f, uint32_t ne
 }
 
 // The epoch sequence skips 0 (the value of zeroed scratch): the k-th value
-// after e, and the number of steps from b forward to a.
+// after e.
 __device__ __forceinline__ uint32_t flag_at(uint32_t e, uint64_t k) {
   return (uint32_t)(((uint64_t)e - 1u + k) % 0xFFFFFFFFull + 1u);
-}
-__device__ __forceinline__ uint64_t flag_dist(uint32_t a, uint32_t b) {
-  return ((uint64_t)a + 0xFFFFFFFFull - b) % 0xFFFFFFFFull;
 }
 
 __device__ __forceinline__ void epoch_advance(const FusedArgs& f, uint32_t epoch) {
@@ -406,8 +409,25 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, Fuse
   __shared__ const char* s_in[R];
   __shared__ char* s_out[R];
   __shared__ uint32_t s_epoch;
-  const bool vec = load_tables<R>(a, s_in, s_out);
-  if (threadIdx.x == 0) s_epoch = ld_relaxed_u32(&f.state->epoch);
+  __shared__ int s_misaligned;
+  // Launched with programmatic dependent launch: wait until the previous
+  // kernel in the stream has completed and its writes (the epoch among
+  // them) are visible, then let the next one be scheduled.
+  pdl_enter();
+  // Pointer tables and the call's epoch, read in one step.
+  if (threadIdx.x == 0) s_misaligned = 0;
+  __syncthreads();
+  if (threadIdx.x < R) {
+    const char* p = a.in_tbl[threadIdx.x];
+    s_in[threadIdx.x] = p;
+    if (reinterpret_cast<uintptr_t>(p) & 15u) atomicOr(&s_misaligned, 1);
+  } else if (threadIdx.x < 2 * R) {
+    char* p = a.out_tbl[threadIdx.x - R];
+    s_out[threadIdx.x - R] = p;
+    if (reinterpret_cast<uintptr_t>(p) & 15u) atomicOr(&s_misaligned, 1);
+  } else if (threadIdx.x == 2 * R) {
+    s_epoch = ld_acquire_u32(&f.state->epoch);
+  }
   // CTA c is clique c; its warp group r (Tr threads, a multiple of 32)
   // stands for virtual rank r.
   const size_t Tr = blockDim.x / R;
@@ -423,12 +443,6 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, Fuse
   const size_t L = (size_t)(f.lead > 0 ? f.lead : 1);
   const bool scatter_on = R > 1 && r != f.skip_producer;
 
-  // Fast body: tiles [jt, jt + Tr) with jt + Tr <= fast_vs are whole groups
-  // in every shard (the last shard is the shortest).
-  const size_t whole = a.count / E::kGroup;
-  const size_t fast_vs =
-      (vec && f.fast32 && whole > (size_t)(R - 1) * Vs) ? min(Vs, whole - (size_t)(R - 1) * Vs)
-                                                        : 0;
   const uint32_t Vs32 = (uint32_t)Vs, SG32 = (uint32_t)f.slot_groups;
   // Per-rank offsets for q = 1..R-1 (owner o = (r + q) % R), in shared memory
   // to leave the registers to the data in flight: start of o's shard in
@@ -440,7 +454,20 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, Fuse
     s_dst_off[r][q - 1] = (uint32_t)(o * (R - 1) + (r < o ? r : r - 1)) * SG32;
   }
   __syncthreads();
+  const bool vec = s_misaligned == 0;
   const uint32_t epoch = s_epoch;
+  // Fast body: tiles [jt, jt + Tr) with jt + Tr <= fast_vs are whole groups
+  // in every shard (the last shard is the shortest).
+  const size_t whole = a.count / E::kGroup;
+  const size_t fast_vs =
+      (vec && f.fast32 && whole > (size_t)(R - 1) * Vs) ? min(Vs, whole - (size_t)(R - 1) * Vs)
+                                                        : 0;
+  // Flag rotation at arrival: every CTA has read the epoch before it counts
+  // itself in, so the last CTA to arrive may install the next epoch (at its
+  // end, when the counter's answer has long come back); no CTA waits on
+  // another at exit.  The next call, ordered after this kernel, reads it.
+  uint32_t arrival = 0;
+  if (threadIdx.x == 0) arrival = atomicAdd(&f.state->done, 1u);
   const char* my_in = s_in[r];
   // Slot of (owner r, i-th other source in rank order): r * (R - 1) + i.
   const uint32_t src_row = (uint32_t)(r * (R - 1)) * SG32;
@@ -572,7 +599,10 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, Fuse
     if (!__all_sync(0xFFFFFFFFu, ok)) break;
     if (R > 1 && f.discard && rd_round) discard_round<R>(f, r, jtr, t, my_n);
   }
-  epoch_advance(f, epoch);
+  if (threadIdx.x == 0 && arrival == gridDim.x - 1) {
+    st_relaxed_u32(&f.state->done, 0u);
+    st_relaxed_u32(&f.state->epoch, flag_at(epoch, 1));
+  }
 }
 
 // Without write mode (the packet broadcast of the ARK page): scatter ->
@@ -615,172 +645,6 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_packet_recv(CallArgs a, Fu
   epoch_advance(f, l.epoch);
 }
 
-// ---------------------------------------------------------------------------
-// Ring variant of the write-mode kernel.
-//
-// The scratch above holds every packet of a call (about 4(R-1)N bytes), so
-// on a large call its dirty lines leave L2 and are written back to HBM after
-// being read once.  Here each (owner, source, CTA) pair owns a ring of D
-// round slots of T groups; round k of CTA c covers groups
-// j = k*C*T + c*T + t of every shard and uses ring slot k mod D, so the
-// packet footprint is R(R-1)*C*D*T*32 bytes whatever the message size, and
-// L2 keeps rewriting the same lines.
-//
-//   * Flags: round k of a call with epoch e carries flag_at(e, k); the call
-//     moves the epoch on by its number of rounds K, so a slot's previous
-//     contents (an earlier round or call) never carry the flag expected now.
-//   * Credits: warp w of owner CTA (o, c) publishes, with a release store
-//     after a warp barrier, progress[o][c][w] = flag of the last round it
-//     finished reading; before warp w of producer CTA (s, c) overwrites slot
-//     k mod D it waits (acquire) until every other owner's warp w has
-//     reached round k - D.  Producer thread t writes only slots that
-//     consumer thread t reads, so warps need no CTA-wide barrier.
-//   * Schedule of every warp, iteration k = 0..K: [credits for round k] ->
-//     scatter round k -> reduce round k-1 -> warp barrier -> publish k-1.
-//     With D >= 2 and a co-resident grid this cannot deadlock: by induction
-//     on k, iteration k needs only iterations <= k-1 of the other warps.
-//   * Every wait is bounded like the others; a timeout abandons the call.
-// Progress word of (owner, CTA c, warp w).
-__device__ __forceinline__ size_t ring_progress_index(int owner, int c, int w) {
-  return ((size_t)owner * kMaxRingCtas + c) * kMaxRingWarps + w;
-}
-
-template <int R>
-__device__ __forceinline__ uint64_t* ring_slot(const FusedArgs& f, int o, int s, int c, int C,
-                                               int p, int tid, int T) {
-  const int pair = o * (R - 1) + (s < o ? s : s - 1);
-  const size_t idx = (((size_t)pair * C + c) * f.ring_depth + p) * T + tid;
-  return f.scratch + idx * 4;
-}
-
-__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-// Bounded wait (one thread) until progress word *pp has reached `target`.
-__device__ __noinline__ bool wait_credit(const FusedArgs& f, const uint32_t* pp, uint32_t& pv,
-                                         uint32_t target, int who, uint32_t call_epoch) {
-  uint64_t t_first = 0;
-  uint32_t spins = 0;
-  // 0 is never a flag (zeroed memory): not yet published.
-  while (pv == 0u || flag_dist(pv, target) >= 0x80000000ull) {
-    __nanosleep(64);
-    pv = ld_acquire_u32(pp);
-    if ((++spins & 15u) == 0) {
-      const uint64_t now = global_timer_ns();
-      if (spins == 16u) t_first = now;
-      if (spins > kMaxSpins || (spins > 16u && now - t_first > f.spin_limit_ns)) {
-        report_timeout(f, who, 0u, call_epoch);
-        return false;
-      }
-      if (ld_relaxed_u32(&f.state->abort_epoch) == call_epoch) return false;
-    }
-  }
-  return true;
-}
-
-template <int R, class E>
-__global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8_ring(CallArgs a, FusedArgs f) {
-  __shared__ const char* s_in[R];
-  __shared__ char* s_out[R];
-  const Lane l = packet_prologue<R>(a, f, s_in, s_out);
-  const int T = blockDim.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int C = (int)(gridDim.x / R), c = (int)(blockIdx.x / R), r = l.r;
-  const int D = f.ring_depth;
-  const size_t Vs = l.Vs;
-  const size_t per_round = (size_t)C * T;
-  const size_t K = (Vs + per_round - 1) / per_round;  // rounds of this call
-  const char* my_in = s_in[r];
-  const size_t g0 = (size_t)r * Vs;  // first group of my shard
-  const size_t my_n = g0 < a.groups ? min(Vs, a.groups - g0) : 0;
-  // Thread t of producer CTA (s, c) writes exactly the ring slots that
-  // thread t of consumer CTA (o, c) reads, so credits are per warp: lanes
-  // 0..R-2 each watch one other owner's progress word for this warp.
-  const int watch = (R > 1 && lane < R - 1) ? (r + 1 + lane) % R : -1;
-  uint32_t* const my_progress = f.progress + ring_progress_index(r, c, warp);
-  const uint32_t* const watched =
-      watch >= 0 ? f.progress + ring_progress_index(watch, c, warp) : nullptr;
-  uint32_t pv = watch >= 0 ? ld_acquire_u32(watched) : 0u;
-
-  for (size_t k = 0; k <= K; ++k) {
-    // ---- credits for round k: every other owner's warp has read round k - D
-    if (R > 1 && k < K && k >= (size_t)D) {
-      const bool ok =
-          watch < 0 || wait_credit(f, watched, pv, flag_at(l.epoch, k - D), r, l.epoch);
-      __syncwarp();
-      if (!__all_sync(0xFFFFFFFFu, ok)) break;
-    }
-    const size_t jk = k * per_round + (size_t)c * T + tid;  // my group of round k
-    // ---- issue: input loads of round k, packet loads of round k-1 ----------
-    uint4 x[R > 1 ? R - 1 : 1];
-    const bool scatter = R > 1 && k < K && jk < Vs && r != f.skip_producer;
-    if (scatter) {
-#pragma unroll
-      for (int q = 1; q < R; ++q) {
-        const int o = (r + q) % R;
-        const size_t g = (size_t)o * Vs + jk;
-        if (g < a.groups) x[q - 1] = load_group<E, true>(my_in, g, group_valid<E>(g, a.count), l.vec, l.pol_in);
-      }
-    }
-    const size_t jp = jk - per_round;  // my group of round k-1 (valid when k >= 1)
-    const bool reduce = k >= 1 && jp < my_n;
-    const int pp = (int)((k + D - 1) % D);  // ring slot of round k-1
-    Packets4 pk[R];
-    uint4 own = make_uint4(0, 0, 0, 0);
-    uint32_t pending = 0;
-    if (reduce) {
-      own = load_group<E, true>(my_in, g0 + jp, group_valid<E>(g0 + jp, a.count), l.vec, l.pol_in);
-#pragma unroll
-      for (int s = 0; s < R; ++s)
-        if (s != r) {
-          pk[s].load(ring_slot<R>(f, r, s, c, C, pp, tid, T));
-          pending |= 1u << s;
-        }
-    }
-    // ---- scatter round k ----------------------------------------------------
-    if (scatter) {
-      const uint32_t flag = flag_at(l.epoch, k);
-      const int p = (int)(k % D);
-#pragma unroll
-      for (int q = 1; q < R; ++q) {
-        const int o = (r + q) % R;
-        if ((size_t)o * Vs + jk < a.groups)
-          st_packets(ring_slot<R>(f, o, r, c, C, p, tid, T), x[q - 1], flag);
-      }
-    }
-    // ---- reduce round k-1 + write-mode broadcast ----------------------------
-    bool ok = true;
-    if (reduce) {
-      const uint32_t flag = flag_at(l.epoch, k - 1);
-      ok = wait_packets_at<R>(f, pk, pending, flag, l.epoch, r, [&](int s) {
-        return ring_slot<R>(f, r, s, c, C, pp, tid, T);
-      });
-      if (ok) {
-        Acc<E> acc;
-        acc.set(r == 0 ? own : pk[0].data());
-#pragma unroll
-        for (int s = 1; s < R; ++s) acc.add(s == r ? own : pk[s].data());
-        const uint4 y = acc.round();
-        const size_t g = g0 + jp;
-        const int valid = group_valid<E>(g, a.count);
-#pragma unroll
-        for (int q = 0; q < R; ++q) store_group<E>(s_out[q], g, y, valid, l.vec);
-      }
-    }
-    // Every lane of the warp is done reading ring slot pp: publish it.
-    __syncwarp();
-    if (!__all_sync(0xFFFFFFFFu, ok)) break;
-    if (k >= 1 && lane == 0) st_release_u32(my_progress, flag_at(l.epoch, k - 1));
-  }
-  epoch_advance_to(f, flag_at(l.epoch, K));
-}
-
 }  // namespace
 
 namespace {
@@ -814,14 +678,6 @@ cudaError_t occ_staged(int R, int dtype, int threads, int* n) {
   return cudaErrorInvalidValue;
 }
 
-cudaError_t occ_ring(int R, int dtype, int threads, int* n) {
-#define Q(RR, EE) \
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, k_fused_ll8_ring<RR, EE>, threads, 0)
-  AR_DISPATCH(dtype, R, Q, AR_SWITCH_R8)
-#undef Q
-  return cudaErrorInvalidValue;
-}
-
 }  // namespace
 
 int fused_ctas_per_sm(int R, int dtype, int threads) {
@@ -834,15 +690,12 @@ int fused_staged_ctas_per_sm(int R, int dtype, int threads) {
   return occ_staged(R, dtype, threads, &n) == cudaSuccess ? n : 0;
 }
 
-int fused_ring_ctas_per_sm(int R, int dtype, int threads) {
-  int n = 0;
-  return occ_ring(R, dtype, threads, &n) == cudaSuccess ? n : 0;
-}
-
 cudaError_t launch_fused_ll8(int R, int dtype, const CallArgs& a, const FusedArgs& f,
                              LaunchCfg cfg, cudaStream_t s) {
+  // A plain launch: every packet wait stays inside one CTA, so co-residency
+  // is not needed for progress (the grid is still sized to fit at once).
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t lc = cooperative_config(cfg, s, attr);
+  const cudaLaunchConfig_t lc = plain_config(cfg, dim3((unsigned)cfg.ctas), 0, s, attr);
 #define L(RR, EE) return cudaLaunchKernelEx(&lc, k_fused_ll8<RR, EE>, a, f)
   AR_DISPATCH(dtype, R, L, AR_SWITCH_R8)
 #undef L
@@ -854,16 +707,6 @@ cudaError_t launch_fused_ll8_staged(int R, int dtype, const CallArgs& a, const F
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t lc = cooperative_config(cfg, s, attr);
 #define L(RR, EE) return cudaLaunchKernelEx(&lc, k_fused_ll8_staged<RR, EE>, a, f)
-  AR_DISPATCH(dtype, R, L, AR_SWITCH_R8)
-#undef L
-  return cudaErrorInvalidValue;
-}
-
-cudaError_t launch_fused_ll8_ring(int R, int dtype, const CallArgs& a, const FusedArgs& f,
-                                  LaunchCfg cfg, cudaStream_t s) {
-  cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t lc = cooperative_config(cfg, s, attr);
-#define L(RR, EE) return cudaLaunchKernelEx(&lc, k_fused_ll8_ring<RR, EE>, a, f)
   AR_DISPATCH(dtype, R, L, AR_SWITCH_R8)
 #undef L
   return cudaErrorInvalidValue;
@@ -984,8 +827,6 @@ extern "C" ar_status_t ar_allreduce_fused_noalloc(int R, const void* const* d_in
   f.fast32 = ar::fused_fits_32bit(R, a.shard_groups, f.slot_groups);
   f.delay_rank = -1;
   f.delay_ns = 0;
-  f.ring_depth = 0;
-  f.progress = nullptr;
   // One clique of R warp groups per CTA, a persistent grid of co-resident CTAs.
   const int tr = ar::fused_rank_threads(R, kNoAllocThreads);
   const size_t limit = (size_t)d.ctas_per_sm[R] * (size_t)d.sms;

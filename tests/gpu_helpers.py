@@ -10,7 +10,7 @@ from shot_allreduce_ranks_gb300 import AllReduce, build, inputs
 
 DEV = "cuda"
 PARITY_VARIANTS = ["oneshot_pull", "oneshot_fanout", "twophase", "fused_ll8",
-                   "oneshot_fanout_bulk", "fused_ll8_staged", "packet_3op", "fused_ll8_ring"]
+                   "oneshot_fanout_bulk", "fused_ll8_staged", "packet_3op"]
 
 _handles = {}
 

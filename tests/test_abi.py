@@ -79,3 +79,30 @@ def test_build_targets_sm103a_only():
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError, match="not built"):
         _lib.load(str(tmp_path / "libar_gb300.so"))
+
+
+def _prototype_comment(text, name):
+    """The comment block that ends right before `name`'s prototype."""
+    import re
+    for m in re.finditer(r"/\*(.*?)\*/", text, re.S):
+        after = text[m.end():m.end() + 1200]
+        # skip preprocessor lines (with their continuations) between the two
+        after = re.sub(r"\A(\s*#(?:[^\n]*\\\n)*[^\n]*\n)+", "", after)
+        decl = re.match(r"\s*[A-Za-z_][\w \t*]*?\b(\w+)\s*\(", after)
+        if decl and decl.group(1) == name:
+            return m.group(1)
+    return ""
+
+
+def test_core_entry_points_cite_their_source_passage():
+    """Every core call of the boundary names the page (and section) that
+    defines the operation, or says that the pages have none."""
+    text = open(_lib.HEADER).read()
+    cites = ("#1910", "#245", "#3850", "#254", "no counterpart", "define no such")
+    for name in ("ar_create", "ar_allreduce", "ar_destroy", "ar_set_variant",
+                 "ar_get_device_status", "ar_status_string",
+                 "ar_allreduce_fused_noalloc"):
+        comment = _prototype_comment(text, name)
+        assert comment, name
+        assert "Source:" in comment or "no counterpart" in comment, name
+        assert any(c in comment for c in cites), name

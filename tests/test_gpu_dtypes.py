@@ -11,7 +11,7 @@ from shot_allreduce_ranks_gb300._lib import AR_ERR_UNSUPPORTED
 pytestmark = pytest.mark.gpu
 
 ONE_SHOT = ["oneshot_pull", "oneshot_fanout", "oneshot_fanout_bulk", "twophase"]
-PACKET = ["fused_ll8", "fused_ll8_staged", "packet_3op", "fused_ll8_ring"]
+PACKET = ["fused_ll8", "fused_ll8_staged", "packet_3op"]
 COUNTS = [1, 7, 9, 4097, 3 * 65536 + 5]
 
 _handles = {}
@@ -185,6 +185,39 @@ def test_host_buffer_paths(dtype, R):
         check(pinned_out, want, dtype, "host page-locked %s R=%d" % (v, R))
         check(pageable_out, want, dtype, "host pageable %s R=%d" % (v, R))
     ar.set_variant("auto")
+
+
+def test_host_path_refuses_stream_capture():
+    """ar_allreduce_host copies its device pointer table from memory that
+    lives only for the call, so a captured graph would keep a dangling
+    source: under capture the call must refuse (AR_ERR_UNSUPPORTED) and
+    enqueue nothing, and work again once capture has ended."""
+    from shot_allreduce_ranks_gb300 import _lib
+    import ctypes
+    R, count = 4, 4097
+    ar = handle(R, count, torch.bfloat16)
+    ar.reserve_host_staging()
+    xs = inputs.make_inputs(R, count, seed=3, fill="normal")
+    pinned_in = [x.pin_memory() for x in xs]
+    pinned_out = [torch.empty(count, dtype=torch.bfloat16).pin_memory() for _ in range(R)]
+    ins = (ctypes.c_void_p * R)(*[t.data_ptr() for t in pinned_in])
+    outs = (ctypes.c_void_p * R)(*[t.data_ptr() for t in pinned_out])
+    lib = _lib.load()
+    side = torch.cuda.Stream()
+    dummy = torch.zeros(16, device="cuda")
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        dummy.add_(1.0)  # keep the captured graph non-empty
+        st = lib.ar_allreduce_host(ar._h, ctypes.cast(ins, ctypes.c_void_p),
+                                   ctypes.cast(outs, ctypes.c_void_p), count,
+                                   side.cuda_stream)
+    assert st == AR_ERR_UNSUPPORTED
+    g.replay()
+    torch.cuda.synchronize()
+    ar.set_variant("auto")
+    ar.allreduce_host(pinned_in, pinned_out)
+    torch.cuda.synchronize()
+    check(pinned_out, expect(xs, torch.bfloat16), torch.bfloat16, "host path after capture")
 
 
 @pytest.mark.parametrize("block", [4096 + 24, 1001], ids=["vector", "element"])

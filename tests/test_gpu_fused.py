@@ -22,7 +22,7 @@ def ar():
     G.release_handles()
 
 
-PACKET_VARIANTS = ["fused_ll8", "fused_ll8_staged", "packet_3op", "fused_ll8_ring"]
+PACKET_VARIANTS = ["fused_ll8", "fused_ll8_staged", "packet_3op"]
 
 
 def _bufs(xs):
@@ -45,12 +45,11 @@ def _flag_after(e, k):
     return (e - 1 + k) % 0xFFFFFFFF + 1
 
 
-@pytest.mark.parametrize("variant", ["fused_ll8", "fused_ll8_ring", "packet_3op"])
+@pytest.mark.parametrize("variant", ["fused_ll8", "packet_3op"])
 def test_epoch_wraps_to_one_skipping_zero(ar, variant):
-    """A call moves the epoch by its number of flag values (one for the
-    full-scratch kernels, one per round for the ring).  Started just below
-    2^32, three calls carry the flags across the wrap, skipping 0, and every
-    one is correct."""
+    """A call moves the epoch by one flag value.  Started just below 2^32,
+    three calls carry the flags across the wrap, skipping 0, and every one
+    is correct."""
     ar.set_variant(variant)
     xs = inputs.make_inputs(R, COUNT, 2)
     want = G.oracle_expect(xs)
@@ -58,7 +57,7 @@ def test_epoch_wraps_to_one_skipping_zero(ar, variant):
     e0 = ar.debug_get_epoch()
     ar(bufs, outs)
     step = ar.debug_get_epoch() - e0
-    assert 1 <= step <= 8
+    assert step == 1
     e = 0xFFFFFFFF - step
     ar.debug_set_epoch(e)
     for call in range(3):
@@ -74,14 +73,14 @@ def test_epoch_wraps_to_one_skipping_zero(ar, variant):
 
 @pytest.mark.parametrize("variant", PACKET_VARIANTS)
 def test_epoch_advances_once_per_call_every_packet_variant(ar, variant):
-    """By one per call (the ring: by its rounds per call, the same every call)."""
+    """By one per call."""
     xs = inputs.make_inputs(R, COUNT, 11)
     bufs, outs = _bufs(xs)
     ar.set_variant(variant)
     e0 = ar.debug_get_epoch()
     ar(bufs, outs)
     step = ar.debug_get_epoch() - e0
-    assert step == 1 or (variant == "fused_ll8_ring" and 1 <= step <= 8)
+    assert step == 1
     for _ in range(2):
         ar(bufs, outs)
     assert ar.debug_get_epoch() == e0 + 3 * step
@@ -162,29 +161,70 @@ def test_graph_replay_with_changing_inputs(ar):
     assert ar.device_status() == AR_OK
 
 
-@pytest.mark.parametrize("depth_calls", [(0, 2), (3 * R, 5)])
-def test_ring_many_rounds(depth_calls):
-    """The ring kernel over many rounds (a small grid forces K >> D), so that
-    every ring slot is reused and every credit wait is exercised; several
-    calls in a row with changing inputs."""
-    ctas, calls = depth_calls
-    h = G.handle(R, 3 * 65536 * 8 + 5)
-    h.set_variant("fused_ll8_ring")
-    h.set_launch("fused_ll8_ring", ctas if ctas else R, 128)
-    count = 3 * 65536 * 8 + 5
-    bufs = [torch.empty(count, dtype=torch.bfloat16, device=G.DEV) for _ in range(R)]
+def _replay_time_us(g):
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3
+
+
+@pytest.mark.parametrize("rank", [0, 5])
+def test_graph_replay_with_a_skewed_producer(ar, rank):
+    """The capture-and-replay check of "Add HIP-graph capture coverage for
+    the sharded-relay collectives" (torchcomms #3850, summary), with one
+    producer late: the warps of virtual rank `rank` wait 40 us of the device
+    timer before their first packet store on every replay (the delay is a
+    launch argument, so the captured call keeps it), and the inputs change
+    between replays.  Owners therefore poll for that rank's packets while
+    its slots still hold the previous replay's packets; a flag that did not
+    rotate per replay (a by-value or hardcoded epoch) would accept them and
+    return the previous replay's sums.  Every replay must equal the oracle,
+    the epoch must move by one per replay, and no wait may run out."""
+    delay_ns = 40_000
+    bufs = [torch.empty(COUNT, dtype=torch.bfloat16, device=G.DEV) for _ in range(R)]
     outs = [torch.empty_like(b) for b in bufs]
-    in_tbl, out_tbl = h.tables(bufs, outs)
-    snaps, wants = [], []
-    for call in range(calls):
-        xs = inputs.make_inputs(R, count, seed=200 + call)
-        wants.append(G.oracle_expect(xs))
+    in_tbl, out_tbl = ar.tables(bufs, outs)
+    ar.set_variant("fused_ll8")
+    ar.debug_delay_producer(rank, delay_ns)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        ar.allreduce_tables(in_tbl, out_tbl, COUNT)  # warm-up outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        ar.allreduce_tables(in_tbl, out_tbl, COUNT)
+    ar.debug_delay_producer(-1, 0)  # later launches run undelayed; the graph keeps its copy
+    torch.cuda.synchronize()
+    e0 = ar.debug_get_epoch()
+    reps = 8
+    for rep in range(reps):
+        xs = inputs.make_inputs(R, COUNT, 70 + rep)
         for b, x in zip(bufs, xs):
             b.copy_(x)
-        h.allreduce_tables(in_tbl, out_tbl, count)
-        snaps.append([o.clone() for o in outs])
+        torch.cuda.synchronize()
+        assert _replay_time_us(g) >= delay_ns / 1e3  # the producer really was late
+        G.check_all_outputs(outs, G.oracle_expect(xs), "skewed replay %d" % rep)
+    assert ar.debug_get_epoch() == e0 + reps
+    assert ar.device_status() == AR_OK
+    # and an undelayed eager call afterwards is correct too
+    xs = inputs.make_inputs(R, COUNT, 99)
+    for b, x in zip(bufs, xs):
+        b.copy_(x)
+    ar.allreduce_tables(in_tbl, out_tbl, COUNT)
     torch.cuda.synchronize()
-    assert h.device_status() == AR_OK
-    for call, (snap, want) in enumerate(zip(snaps, wants)):
-        G.check_all_outputs(snap, want, "ring call %d" % call)
-    h.set_launch("fused_ll8_ring", 0, 0)
+    G.check_all_outputs(outs, G.oracle_expect(xs), "eager after skewed replays")
+
+
+def test_delay_hook_bounds():
+    from shot_allreduce_ranks_gb300 import ArError
+    h = G.handle(R, COUNT)
+    with pytest.raises(ArError):
+        h.debug_delay_producer(R, 1000)
+    with pytest.raises(ArError):
+        h.debug_delay_producer(0, 20_000_000)  # above the 10 ms bound
+    h.debug_delay_producer(-1, 0)

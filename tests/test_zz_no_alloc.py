@@ -65,3 +65,42 @@ def test_noalloc_rejects_counts_beyond_its_fixed_scratch():
                                           stream) == _lib.AR_ERR_INVALID_ARG
     assert lib.ar_allreduce_fused_noalloc(R, None, tbl.data_ptr(), 8,
                                           stream) == _lib.AR_ERR_INVALID_ARG
+
+
+def test_noalloc_switching_counts_and_ranks_against_the_oracle():
+    """The fixed array is shared by every call on the device, and its packet
+    layout moves with each call's count and R: only the rotating flag keeps
+    a packet of an earlier call from being taken for a new one.  Alternate
+    the largest count the array holds with a small ragged one, switch R from
+    8 to 3 and back, and make an R = 1 call (the identity); every output of
+    every call must equal the oracle bit for bit and the handle path's."""
+    import oracle
+    build.build()
+    lib = _lib.load()
+    stream = torch.cuda.current_stream().cuda_stream
+    plan = [(8, _lib.noalloc_max_count(8)), (8, 4097), (8, _lib.noalloc_max_count(8)),
+            (3, 100_003), (8, 65_541), (1, 12_345), (8, 4097)]
+    for call, (R, count) in enumerate(plan):
+        xs = inputs.make_inputs(R, count, seed=60 + call)
+        want = oracle.allreduce_bf16([inputs.bits(x) for x in xs])[0]
+        bufs = [x.to("cuda") for x in xs]
+        outs = [torch.full_like(b, float("nan")) for b in bufs]
+        in_tbl = torch.tensor([b.data_ptr() for b in bufs], dtype=torch.int64, device="cuda")
+        out_tbl = torch.tensor([o.data_ptr() for o in outs], dtype=torch.int64, device="cuda")
+        st = lib.ar_allreduce_fused_noalloc(R, in_tbl.data_ptr(), out_tbl.data_ptr(), count,
+                                            stream)
+        assert st == _lib.AR_OK, (call, st)
+        torch.cuda.synchronize()
+        for r in range(R):
+            got = _bits(outs[r])
+            bad = np.nonzero(got != want)[0]
+            assert bad.size == 0, "call %d (R=%d, count=%d) rank %d: %d differ, first at %d" % (
+                call, R, count, r, bad.size, int(bad[0]))
+        if R == 1:
+            assert np.array_equal(_bits(outs[0]), inputs.bits(xs[0]))
+        with AllReduce(R, count) as ar:
+            ar.set_variant("fused_ll8")
+            ref = ar(bufs)
+            torch.cuda.synchronize()
+            assert np.array_equal(_bits(ref[0]), want)
+        del bufs, outs
