@@ -83,9 +83,22 @@ struct ar_ctx {
   int skip_producer = -1;
   int delay_rank = -1;         // skewed-producer test hook (persists until cleared)
   uint64_t delay_ns = 0;
-  int fused_lead = 2;          // tiles the fused kernel scatters ahead of its reduce
-  bool fused_discard = true;   // drop consumed packet lines from L2 (no write-back)
+  // Packet handling of the write-mode fused kernel, chosen per call from the
+  // bytes of packets P = 32 R (R-1) groups-per-shard (measured at R = 8 on
+  // GB300, graph replay): P <= L2/2: packets written into the message-sized
+  // scratch stay in L2 between calls, so they are left there (22.8 vs 23.5 us
+  // at 440x5120 with drops); L2/2 < P <= 3 L2: the scratch, with each
+  // consumed line dropped from L2 (38.5 vs 45.6 us at 512x8192 without
+  // drops); P > 3 L2: per-CTA rings of lead + 1 rounds with lead 1 (138.7 vs
+  // 145.5 us at 16 Mi elements, 269 vs 285 us at 32 Mi).  The AR_FUSED_RING,
+  // AR_FUSED_DISCARD and AR_FUSED_LEAD environment variables force a choice.
+  int fused_lead = 0;          // tiles scattered ahead of the reduce (0: automatic)
+  int fused_discard = -1;      // -1 automatic, 0 never, 1 always (scratch mode)
+  int l2_bytes = 0;
   bool fused_pdl = true;       // programmatic dependent launch for the write-mode fused kernel
+  int fused_ring = -1;         // -1 automatic, 0 never, 1 always
+  uint64_t* ring = nullptr;    // the rings of all CTAs
+  size_t ring_groups = 0;      // its size in 32-byte packet groups
   int fused_threads = 256;
   int fused_ctas_per_sm = 0;   // occupancy at fused_threads
   // Occupancy cache (CTAs per SM) indexed by threads / 32; 0 = not queried.
@@ -213,6 +226,33 @@ int occupancy(ar_ctx* h, int variant, int threads) {
   return cache[k] > 0 ? cache[k] : 0;
 }
 
+constexpr int kMaxRingRounds = 3;  // rings are sized for lead 2 (lead + 1 rounds)
+
+struct FusedMode {
+  int lead;         // tiles scattered ahead of the reduce
+  int discard;      // drop consumed scratch lines from L2
+  int ring_rounds;  // > 0: per-CTA rings of this many rounds instead of the scratch
+};
+
+// The write-mode fused kernel's packet handling for a call with
+// `shard_groups` groups per shard (the rules at ar_ctx::fused_lead).
+FusedMode fused_mode(const ar_ctx* h, size_t shard_groups) {
+  const double P = 32.0 * h->R * (h->R - 1) * (double)shard_groups;
+  const double l2 = h->l2_bytes > 0 ? (double)h->l2_bytes : 128.0 * (1 << 20);
+  const bool ring = h->ring && (h->fused_ring == 1 || (h->fused_ring < 0 && P > 3.0 * l2));
+  FusedMode m;
+  m.lead = h->fused_lead > 0 ? h->fused_lead : (ring ? 1 : 2);
+  m.ring_rounds = ring ? m.lead + 1 : 0;
+  m.discard = ring ? 0 : h->fused_discard >= 0 ? h->fused_discard : (P > 0.5 * l2 ? 1 : 0);
+  return m;
+}
+
+// 32-byte packet groups one CTA's ring needs: `rounds` rounds of R(R-1)
+// slots of Tr groups.
+size_t ring_groups_per_cta(int R, int rounds, int tr) {
+  return (size_t)rounds * (size_t)R * (size_t)(R - 1) * (size_t)tr;
+}
+
 // Launch shape of one call.  Threads default to 256.  Fan-out: a persistent
 // grid of co-resident CTAs (two groups per thread per iteration); pull and
 // two-phase: one group per thread, capped at 16 CTAs per SM, a multiple of
@@ -273,6 +313,11 @@ LaunchCfg shape(ar_ctx* h, int variant, const TuneRow* row, size_t groups, size_
           std::max<size_t>(1, (size_t)occupancy(h, variant, c.threads) * (size_t)h->num_sms);
       size_t ctas = c.ctas > 0 ? (size_t)c.ctas : ceil_div(shard_groups, (size_t)tr);
       c.ctas = (int)std::max<size_t>(1, std::min(ctas, limit));
+      const FusedMode m = fused_mode(h, shard_groups);
+      if (m.ring_rounds) {  // every CTA's ring must fit
+        const size_t per_cta = ring_groups_per_cta(R, m.ring_rounds, tr);
+        c.ctas = (int)std::max<size_t>(1, std::min((size_t)c.ctas, h->ring_groups / per_cta));
+      }
       break;
     }
     case AR_FUSED_LL8_STAGED: {
@@ -360,8 +405,11 @@ ar_status_t launch(ar_ctx* h, int variant, const TuneRow* row, const void* const
       f.state = h->state;
       f.spin_limit_ns = h->spin_limit_ns;
       f.skip_producer = h->skip_producer;
-      f.lead = h->fused_lead;
-      f.discard = h->fused_discard ? 1 : 0;
+      const FusedMode m = fused_mode(h, a.shard_groups);
+      f.lead = m.lead;
+      f.discard = m.discard;
+      f.ring = h->ring;
+      f.ring_rounds = variant == AR_FUSED_LL8 ? m.ring_rounds : 0;
       f.fast32 = ar::fused_fits_32bit(h->R, a.shard_groups, h->slot_groups);
       f.delay_rank = h->delay_rank;
       f.delay_ns = h->delay_ns;
@@ -430,6 +478,7 @@ ar_status_t ar_create(int R, size_t max_count, int dtype, ar_handle_t* out) {
   h->max_count = max_count;
   h->device = dev;
   h->num_sms = sms;
+  cudaDeviceGetAttribute(&h->l2_bytes, cudaDevAttrL2CacheSize, dev);
   h->table = builtin_table(R, dtype == AR_FP32 ? 4 : 2);
   const char* env = getenv("AR_TUNING_FILE");
   if (env && *env && !load_table_file(env, &h->table)) {
@@ -452,12 +501,14 @@ ar_status_t ar_create(int R, size_t max_count, int dtype, ar_handle_t* out) {
   env = getenv("AR_FUSED_LEAD");
   if (env && *env) {
     const long v = strtol(env, nullptr, 10);
-    if (v >= 1 && v <= 4) h->fused_lead = (int)v;
+    if (v >= 1 && v <= 2) h->fused_lead = (int)v;
   }
+  env = getenv("AR_FUSED_RING");
+  if (env && (env[0] == '0' || env[0] == '1')) h->fused_ring = env[0] - '0';
   env = getenv("AR_FUSED_PDL");
   if (env && env[0] == '0') h->fused_pdl = false;
   env = getenv("AR_FUSED_DISCARD");
-  if (env && env[0] == '0') h->fused_discard = false;
+  if (env && (env[0] == '0' || env[0] == '1')) h->fused_discard = env[0] - '0';
 
   const size_t groups = ceil_div(max_count, (size_t)ar::group_elems(dtype));
   // Rounded up to 4 groups so that every slot starts on a 128-byte line.
@@ -488,8 +539,23 @@ ar_status_t ar_create(int R, size_t max_count, int dtype, ar_handle_t* out) {
       (cudaMemset(h->scratch, 0, h->scratch_bytes) != cudaSuccess ||
        cudaMemset(h->rscratch, 0, h->scratch_bytes) != cudaSuccess))
     st = AR_ERR_CUDA;
+  // The fused kernel's rings: room for every co-resident CTA at the default
+  // and at the largest CTA size, no more than the message needs.
+  if (st == AR_OK && packets && R > 1) {
+    size_t cap = 0;
+    for (int threads : {h->fused_threads, 512}) {
+      const int tr = ar::fused_rank_threads(R, threads);
+      const size_t ctas = std::min((size_t)occupancy(h, AR_FUSED_LL8, R * tr) * (size_t)sms,
+                                   ceil_div(h->slot_groups, (size_t)tr));
+      cap = std::max(cap, ctas * ring_groups_per_cta(R, kMaxRingRounds, tr));
+    }
+    h->ring_groups = cap;
+    if (cap && (cudaMalloc(&h->ring, cap * 32) != cudaSuccess ||
+                cudaMemset(h->ring, 0, cap * 32) != cudaSuccess))
+      st = AR_ERR_OOM;
+  }
   if (st == AR_OK && cudaDeviceSynchronize() != cudaSuccess) st = AR_ERR_CUDA;
-  if (st == AR_OK && h->scratch_bytes && h->fused_discard && write_back_l2(dev) != cudaSuccess)
+  if (st == AR_OK && h->scratch_bytes && h->fused_discard != 0 && write_back_l2(dev) != cudaSuccess)
     st = AR_ERR_OOM;
   if (st != AR_OK) {
     cudaGetLastError();
@@ -508,6 +574,7 @@ ar_status_t ar_destroy(ar_handle_t h) {
   if (prev != h->device) cudaSetDevice(h->device);
   if (cudaDeviceSynchronize() != cudaSuccess) st = AR_ERR_CUDA;
   if (h->scratch && cudaFree(h->scratch) != cudaSuccess) st = AR_ERR_CUDA;
+  if (h->ring && cudaFree(h->ring) != cudaSuccess) st = AR_ERR_CUDA;
   if (h->rscratch && cudaFree(h->rscratch) != cudaSuccess) st = AR_ERR_CUDA;
   if (h->state && cudaFree(h->state) != cudaSuccess) st = AR_ERR_CUDA;
   if (h->staging && cudaFree(h->staging) != cudaSuccess) st = AR_ERR_CUDA;
@@ -553,7 +620,7 @@ ar_status_t ar_query(ar_handle_t h, ar_info_t* info) {
   info->R = h->R;
   info->dtype = h->dtype;
   info->max_count = h->max_count;
-  info->scratch_bytes = 2 * h->scratch_bytes;
+  info->scratch_bytes = 2 * h->scratch_bytes + h->ring_groups * 32;
   info->num_sms = h->num_sms;
   info->fused_max_ctas = h->fused_ctas_per_sm * h->num_sms;
   info->fused_threads = h->R * ar::fused_rank_threads(h->R, h->fused_threads);
@@ -761,9 +828,10 @@ ar_status_t ar_debug_set_epoch(ar_handle_t h, uint32_t epoch) {
   // for everything written before it: clear every packet.
   if ((h->scratch_bytes && (cudaMemset(h->scratch, 0, h->scratch_bytes) != cudaSuccess ||
                             cudaMemset(h->rscratch, 0, h->scratch_bytes) != cudaSuccess)) ||
+      (h->ring && cudaMemset(h->ring, 0, h->ring_groups * 32) != cudaSuccess) ||
       cudaDeviceSynchronize() != cudaSuccess)
     return AR_ERR_CUDA;
-  if (h->scratch_bytes && h->fused_discard && write_back_l2(h->device) != cudaSuccess)
+  if (h->scratch_bytes && h->fused_discard != 0 && write_back_l2(h->device) != cudaSuccess)
     return AR_ERR_CUDA;
   return cuda_status(cudaMemcpy(&h->state->epoch, &epoch, sizeof epoch, cudaMemcpyHostToDevice));
 }

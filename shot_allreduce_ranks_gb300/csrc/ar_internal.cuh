@@ -57,6 +57,12 @@ struct FusedArgs {
   int lead;
   int discard;
   int fast32;   // every slot and input group offset of the call fits in 32 bits
+  // Ring mode of the write-mode fused kernel (ring_rounds > 0): every CTA
+  // keeps its packets in a private ring of ring_rounds rounds in `ring`
+  // ([CTA][round slot][owner][source slot][Tr groups][4]) instead of the
+  // message-sized scratch, and reuses a slot after a CTA barrier.
+  uint64_t* ring;
+  int ring_rounds;
   // Test hook: CTAs of virtual rank delay_rank (or none if -1) wait delay_ns
   // of %globaltimer before their first packet store (a skewed producer).
   int delay_rank;

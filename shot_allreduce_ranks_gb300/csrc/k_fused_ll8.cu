@@ -448,10 +448,20 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, Fuse
   // to leave the registers to the data in flight: start of o's shard in
   // rank r's input, and start of the slot (owner o, source r).
   __shared__ uint32_t s_in_off[R][RO], s_dst_off[R][RO];
+  // Ring mode: packets of round k live in slot k % D of this CTA's ring,
+  // at the thread's index instead of its shard position, and carry the flag
+  // of their round (the call moves the epoch on by its rounds).
+  const bool ring = f.ring_rounds > 0;
+  const uint32_t D = ring ? (uint32_t)f.ring_rounds : 1u;
+  const uint32_t Tr32 = (uint32_t)Tr, t32 = (uint32_t)t;
+  const uint32_t sstride = ring ? Tr32 : SG32;  // groups per (owner, source) slot
+  const uint32_t RRT = (uint32_t)(R * (R - 1)) * Tr32;  // groups per ring round of a CTA
+  const uint32_t ring_cta = (uint32_t)c * D * RRT;
+  uint64_t* const pkt = ring ? f.ring : f.scratch;
   if (t > 0 && t < (size_t)R) {
     const int q = (int)t, o = r + q < R ? r + q : r + q - R;
     s_in_off[r][q - 1] = (uint32_t)o * Vs32;
-    s_dst_off[r][q - 1] = (uint32_t)(o * (R - 1) + (r < o ? r : r - 1)) * SG32;
+    s_dst_off[r][q - 1] = (uint32_t)(o * (R - 1) + (r < o ? r : r - 1)) * sstride;
   }
   __syncthreads();
   const bool vec = s_misaligned == 0;
@@ -470,13 +480,27 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, Fuse
   if (threadIdx.x == 0) arrival = atomicAdd(&f.state->done, 1u);
   const char* my_in = s_in[r];
   // Slot of (owner r, i-th other source in rank order): r * (R - 1) + i.
-  const uint32_t src_row = (uint32_t)(r * (R - 1)) * SG32;
+  const uint32_t src_row = (uint32_t)(r * (R - 1)) * sstride;
   const uint32_t own_off = (uint32_t)r * Vs32;
+  // Position of this thread's packets of round kk within a slot: its shard
+  // position, or (ring mode) its index in the round's slot of the ring.
+  auto ppos = [&](size_t kk, uint32_t jpos) -> uint32_t {
+    return ring ? ring_cta + (uint32_t)(kk % D) * RRT + t32 : jpos;
+  };
+  auto flag_of = [&](size_t kk) -> uint32_t { return ring ? flag_at(epoch, kk) : epoch; };
+  // Rounds of the call: the epoch moves on by this many flags (ring mode).
+  const size_t K_all = (tiles + C - 1) / C;
   // Iterations whose tiles are all whole form a prefix [0, k_fast): tile
-  // c + kC is whole for k < kf.
+  // c + kC is whole for k < kf (the same for every warp of the CTA).
   const size_t nf = fast_vs / Tr;
   const size_t kf = nf > c ? (nf - c + C - 1) / C : 0;
-  const size_t k_fast = kf >= K ? K + L : (scatter_on ? kf : kf + L);
+  const size_t k_fast = kf >= K ? K + L : kf;
+  // End of an iteration: in ring mode a CTA barrier (a ring slot is reused
+  // only after every warp of the CTA has read it; all threads leave the loop
+  // together), else a warp vote.
+  auto iteration_done = [&](bool good) -> bool {
+    return ring ? __syncthreads_and(good) != 0 : __all_sync(0xFFFFFFFFu, good);
+  };
 
   if (r == f.delay_rank && f.delay_ns) producer_delay(f.delay_ns);
 
@@ -501,25 +525,26 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, Fuse
     {
       const bool sc = scatter_on && k < K;
       const uint32_t js = (uint32_t)(jts + t), jr = (uint32_t)(jtr + t);
+      const uint32_t pr = rd_round ? ppos(k - L, jr) : 0u;
       Packets4 pk[RO];
       uint4 own = make_uint4(0, 0, 0, 0);
       if (rd_round) {
         own = ld_v4_stream<true>(my_in + (size_t)(own_off + jr) * kGroupBytes, pol_in);
 #pragma unroll
         for (int i = 0; i < R - 1; ++i)
-          pk[i].load(f.scratch + (size_t)(src_row + (uint32_t)i * SG32 + jr) * 4);
+          pk[i].load(pkt + (size_t)(src_row + (uint32_t)i * sstride + pr) * 4);
       }
       if (sc) {
+        const uint32_t ps = ppos(k, js), fl = flag_of(k);
 #pragma unroll
         for (int q = 0; q < R - 1; ++q)
-          st_packets(f.scratch + (size_t)(s_dst_off[r][q] + js) * 4, x[q], epoch);
+          st_packets(pkt + (size_t)(s_dst_off[r][q] + ps) * 4, x[q], fl);
       }
       if (scatter_on && k + 1 < K && k + 1 < k_fast) load_slices(k + 1);
       if (rd_round) {
         ok = wait_packets_at<RO>(
-            f, pk, R > 1 ? (1u << (R - 1)) - 1u : 0u, epoch, epoch, r,
-            [&](int i) { return f.scratch + (size_t)(src_row + (uint32_t)i * SG32 + jr) * 4; },
-            r);
+            f, pk, R > 1 ? (1u << (R - 1)) - 1u : 0u, flag_of(k - L), epoch, r,
+            [&](int i) { return pkt + (size_t)(src_row + (uint32_t)i * sstride + pr) * 4; }, r);
         if (ok) {
           // rank order 0..R-1; entry i of pk is source i (< r) or i + 1 (> r)
           Acc2<E> acc;
@@ -538,8 +563,11 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, Fuse
         }
       }
     }
-    if (!__all_sync(0xFFFFFFFFu, ok)) break;
-    if (R > 1 && f.discard && rd_round) discard_round<R>(f, r, jtr, t, my_n);
+    if (!iteration_done(ok)) {
+      ok = false;
+      break;
+    }
+    if (R > 1 && f.discard && !ring && rd_round) discard_round<R>(f, r, jtr, t, my_n);
   }
   for (; ok && k < K + L; ++k) {
     // ---------------- checked body (ragged end, misaligned buffers)
@@ -569,7 +597,7 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, Fuse
 #pragma unroll
         for (int s = 0; s < R; ++s)
           if (s != r) {
-            pk[s].load(slot_ptr<R>(f.scratch, f.slot_groups, r, s) + jr * 4);
+            pk[s].load(slot_ptr<R>(pkt, sstride, r, s) + (size_t)ppos(k - L, (uint32_t)jr) * 4);
             pending |= 1u << s;
           }
       }
@@ -578,11 +606,15 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, Fuse
         for (int q = 1; q < R; ++q) {
           const int o = (r + q) % R;
           if ((size_t)o * Vs + js < a.groups)
-            st_packets(slot_ptr<R>(f.scratch, f.slot_groups, o, r) + js * 4, x[q - 1], epoch);
+            st_packets(slot_ptr<R>(pkt, sstride, o, r) + (size_t)ppos(k, (uint32_t)js) * 4,
+                       x[q - 1], flag_of(k));
         }
       }
       if (rd) {
-        ok = wait_packets<R>(f, f.scratch, r, jr, pk, pending, epoch);
+        const size_t pr = ppos(k - L, (uint32_t)jr);
+        ok = wait_packets_at<R>(f, pk, pending, flag_of(k - L), epoch, r, [&](int s) {
+          return slot_ptr<R>(pkt, sstride, r, s) + pr * 4;
+        });
         if (ok) {
           Acc2<E> acc;
           acc.set(r == 0 ? own : pk[0].data());
@@ -596,12 +628,15 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, Fuse
         }
       }
     }
-    if (!__all_sync(0xFFFFFFFFu, ok)) break;
-    if (R > 1 && f.discard && rd_round) discard_round<R>(f, r, jtr, t, my_n);
+    if (!iteration_done(ok)) {
+      ok = false;
+      break;
+    }
+    if (R > 1 && f.discard && !ring && rd_round) discard_round<R>(f, r, jtr, t, my_n);
   }
   if (threadIdx.x == 0 && arrival == gridDim.x - 1) {
     st_relaxed_u32(&f.state->done, 0u);
-    st_relaxed_u32(&f.state->epoch, flag_at(epoch, 1));
+    st_relaxed_u32(&f.state->epoch, flag_at(epoch, ring ? K_all : 1));
   }
 }
 
@@ -825,6 +860,8 @@ extern "C" ar_status_t ar_allreduce_fused_noalloc(int R, const void* const* d_in
   f.lead = 1;
   f.discard = 0;
   f.fast32 = ar::fused_fits_32bit(R, a.shard_groups, f.slot_groups);
+  f.ring = nullptr;
+  f.ring_rounds = 0;
   f.delay_rank = -1;
   f.delay_ns = 0;
   // One clique of R warp groups per CTA, a persistent grid of co-resident CTAs.
