@@ -498,6 +498,11 @@ ar_status_t ar_create(int R, size_t max_count, int dtype, ar_handle_t* out) {
   h->log = env && env[0] == '1';
   env = getenv("AR_PDL");
   if (env && env[0] == '0') h->pdl = false;
+  env = getenv("AR_PDL_MAX_MB");
+  if (env && *env) {
+    const long mb = strtol(env, nullptr, 10);
+    if (mb >= 0) h->pdl_max_bytes = (size_t)mb << 20;
+  }
   env = getenv("AR_FUSED_LEAD");
   if (env && *env) {
     const long v = strtol(env, nullptr, 10);

@@ -256,3 +256,22 @@ def test_fp32_fanout_wide_requests(count):
     torch.cuda.synchronize()
     check(outs, want, torch.float32, "fp32 fanout count=%d" % count)
     ar.set_variant("auto")
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.float32], ids=["fp16", "fp32"])
+def test_fused_ring_mode_types(dtype, monkeypatch):
+    """The fused kernel's per-CTA packet rings (forced, on a grid of 3 CTAs
+    so that every slot is reused many times) for fp16 and fp32, ragged
+    count, two calls with different inputs."""
+    monkeypatch.setenv("AR_FUSED_RING", "1")
+    R, count = 8, 3 * 65536 * 4 + 3
+    build.build()
+    with AllReduce(R, count, dtype=dtype) as ar:
+        ar.set_variant("fused_ll8")
+        ar.set_launch("fused_ll8", 3, 0)
+        for call in range(2):
+            xs = inputs.make_inputs(R, count, seed=400 + call, fill="normal", dtype=dtype)
+            outs = ar([x.to("cuda") for x in xs])
+            torch.cuda.synchronize()
+            check(outs, expect(xs, dtype), dtype, "ring %s call %d" % (dtype, call))
+        assert ar.device_status() == 0

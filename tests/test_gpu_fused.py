@@ -228,3 +228,92 @@ def test_delay_hook_bounds():
     with pytest.raises(ArError):
         h.debug_delay_producer(0, 20_000_000)  # above the 10 ms bound
     h.debug_delay_producer(-1, 0)
+
+
+RING_COUNT = 3 * 65_536 * 8 + 5
+
+
+@pytest.fixture(params=[1, 2], ids=["lead1", "lead2"])
+def ring_handle(request, monkeypatch):
+    """A handle whose fused calls use the per-CTA packet rings (forced: the
+    automatic choice takes them only for messages of several L2 sizes), on a
+    grid of 3 CTAs, so that every ring slot is reused hundreds of times in a
+    call and the flag moves on once per round."""
+    from shot_allreduce_ranks_gb300 import AllReduce
+    monkeypatch.setenv("AR_FUSED_RING", "1")
+    monkeypatch.setenv("AR_FUSED_LEAD", str(request.param))
+    G.ensure_built()
+    h = AllReduce(R, RING_COUNT)
+    h.set_variant("fused_ll8")
+    h.set_launch("fused_ll8", 3, 0)
+    yield h
+    h.close()
+
+
+def _rounds_per_call(h, count):
+    tr = h.query().fused_threads // R
+    groups = (count + 7) // 8
+    tiles = ((groups + R - 1) // R + tr - 1) // tr
+    return (tiles + 3 - 1) // 3  # 3 CTAs
+
+
+def test_ring_mode_many_rounds_and_changing_inputs(ring_handle):
+    h = ring_handle
+    bufs = [torch.empty(RING_COUNT, dtype=torch.bfloat16, device=G.DEV) for _ in range(R)]
+    outs = [torch.empty_like(b) for b in bufs]
+    in_tbl, out_tbl = h.tables(bufs, outs)
+    steps = _rounds_per_call(h, RING_COUNT)
+    assert steps > 100
+    e0 = h.debug_get_epoch()
+    snaps, wants = [], []
+    for call in range(4):
+        xs = inputs.make_inputs(R, RING_COUNT, seed=300 + call)
+        wants.append(G.oracle_expect(xs))
+        for b, x in zip(bufs, xs):
+            b.copy_(x)
+        h.allreduce_tables(in_tbl, out_tbl, RING_COUNT)
+        snaps.append([o.clone() for o in outs])
+    torch.cuda.synchronize()
+    assert h.device_status() == AR_OK
+    assert h.debug_get_epoch() == _flag_after(e0, 4 * steps)  # one flag per round
+    for call, (snap, want) in enumerate(zip(snaps, wants)):
+        G.check_all_outputs(snap, want, "ring call %d" % call)
+
+
+def test_ring_mode_flags_wrap_inside_a_call(ring_handle):
+    """Started 100 flags below 2^32, a call's rounds carry the flag across
+    the wrap (skipping 0) partway through; the next call starts after it."""
+    h = ring_handle
+    xs = inputs.make_inputs(R, RING_COUNT, seed=310)
+    want = G.oracle_expect(xs)
+    bufs, outs = _bufs(xs)
+    steps = _rounds_per_call(h, RING_COUNT)
+    e = 0xFFFFFFFF - 100
+    h.debug_set_epoch(e)
+    for call in range(2):
+        for o in outs:
+            o.zero_()
+        h(bufs, outs)
+        e = _flag_after(e, steps)
+        assert h.debug_get_epoch() == e
+        G.check_all_outputs(outs, want, "ring call %d across the wrap" % call)
+    assert h.device_status() == AR_OK
+
+
+@pytest.mark.parametrize("skip", [0, R - 1])
+def test_ring_mode_missing_producer_times_out_and_recovers(ring_handle, skip):
+    """A rank that stores nothing: its owners' waits run out, every warp of
+    the CTA leaves the loop through the same barrier, the error word says
+    so, and the next call is correct."""
+    h = ring_handle
+    xs = inputs.make_inputs(R, RING_COUNT, seed=320)
+    want = G.oracle_expect(xs)
+    bufs, outs = _bufs(xs)
+    h.set_spin_limit_ns(2_000_000)
+    h.debug_skip_producer(skip)
+    h(bufs, outs)
+    assert h.device_status() == AR_ERR_TIMEOUT
+    h(bufs, outs)
+    assert h.device_status() == AR_OK
+    G.check_all_outputs(outs, want, "ring call after a timeout")
+    h.set_spin_limit_ns(100_000_000)
