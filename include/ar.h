@@ -42,9 +42,11 @@
  *     synchronised by LL packet flags of "Add monolithic fused packet
  *     allreduce kernel and Model::all_reduce_packet API" (microsoft/ark #254,
  *     Changes), with the flag rotated on every call (that page's Known
- *     limitations leave Flag = 1 hardcoded), the grid sized to co-resident
- *     CTAs (its NumProcs >= NPeers limitation), and the broadcast done in the
- *     aiter write mode.
+ *     limitations leave Flag = 1 hardcoded), and the broadcast done in the
+ *     aiter write mode.  Each CTA holds one warp group per virtual rank, so
+ *     packet exchanges stay within a CTA and no CTA waits on another (the
+ *     page's NumProcs >= NPeers limitation cannot arise); the kernel is
+ *     pipelined over rounds so that its packets stay in L2.
  *
  * Threading: a handle may be used from one host thread at a time.  Calls on
  * one handle must be ordered on one stream (one call in flight), because a
@@ -117,7 +119,7 @@ typedef struct {
   size_t scratch_bytes;     /* LL8 packet scratch owned by the handle (both regions) */
   int num_sms;              /* SMs of the device the handle lives on */
   int fused_max_ctas;       /* co-resident CTA limit used to size the fused grid */
-  int fused_threads;        /* threads per CTA of the fused kernel */
+  int fused_threads;        /* threads per CTA of the fused kernel (R warp groups) */
   int device;               /* CUDA device ordinal */
 } ar_info_t;
 
@@ -176,7 +178,9 @@ ar_status_t ar_create(int R, size_t max_count, int dtype, ar_handle_t* out);
  * decided on the device.
  * Allocates nothing, synchronises nothing, so it can be captured into a CUDA
  * graph; the fused kernel's epoch lives on the device and rotates on every
- * execution, including graph replays.
+ * execution, including graph replays (by one per call, or, when the kernel
+ * keeps its packets in per-CTA rings -- messages of several L2 sizes -- by
+ * its number of rounds, one flag per round).
  * Errors: AR_ERR_INVALID_ARG (NULL handle or table, count > max_count),
  * AR_ERR_UNSUPPORTED (a packet variant forced with R > 8), AR_ERR_CUDA
  * (launch failure).  A packet wait that exceeds the spin limit
@@ -238,11 +242,13 @@ ar_status_t ar_set_variant(ar_handle_t h, int variant);
 ar_status_t ar_select(ar_handle_t h, size_t count, int* variant);
 
 /* ar_set_launch -- override the CTA count and threads per CTA of a variant
- * (0 = automatic).  ctas is the total grid for AR_FUSED_LL8 (rounded down to
- * a multiple of R, clamped to the co-resident limit and raised to at least
- * R), and the grid-stride CTA count for the others.  threads must be a
- * multiple of 32 in [64, 512] (the packet and fan-out kernels accept
- * 128..512). */
+ * (0 = automatic).  For AR_FUSED_LL8 ctas is the number of CTAs (each one
+ * clique of R warp groups), clamped to the co-resident limit and to the
+ * packet rings' room, and threads is rounded to R warp groups of a multiple
+ * of 32 threads each (at least 32); for the other variants ctas is the grid
+ * (the grid-stride CTA count; a multiple of R for the pull, two-phase and
+ * staged packet kernels).  threads must be a multiple of 32 in [64, 512]
+ * (the packet and fan-out kernels accept 128..512). */
 ar_status_t ar_set_launch(ar_handle_t h, int variant, int ctas, int threads);
 
 /* ar_set_spin_limit_ns -- the longest a fused-kernel packet wait may spin
