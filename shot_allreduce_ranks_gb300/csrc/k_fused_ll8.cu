@@ -1,56 +1,56 @@
-// Fused LL8 packet allreduce with write-mode broadcast: one persistent kernel.
+// Fused LL8 packet allreduce: the write-mode kernel and its comparison forms.
 //
 // This is the monolithic fused packet allreduce of "Add monolithic fused
 // packet allreduce kernel and Model::all_reduce_packet API" (microsoft/ark
 // #254, Changes): scatter -> reduce -> broadcast in one kernel, synchronised
 // by low-latency (LL) packet flags instead of cross-block barriers.  The R
 // virtual ranks live on one GPU, so "remote" scratch is a region of this
-// GPU's memory and the CTAs standing for a rank touch only what that rank's
-// GPU would touch: its own input, the packet slots it owns or sends to, and
-// (write mode) every rank's output.
+// GPU's memory, and the threads standing for a rank touch only what that
+// rank's GPU would touch: its own input, the packet slots it owns or sends
+// to, and (write mode) every rank's output.
 //
-// Work split.  The 8-element groups are split into R shards of
-// ceil(groups / R); rank o owns shard o.  The grid has G = R * C CTAs, all
-// co-resident (cooperative launch; the page's NumProcs >= NPeers limit,
-// Known limitations); CTA b stands for rank r = b % R with local index
-// c = b / R, and its threads cover groups j = c*T + t, c*T + t + C*T, ... of
-// a shard (T threads per CTA).
-//
+// The 16-byte groups are split into R shards of ceil(groups / R); rank o
+// owns shard o.
 //   scatter (packet stores): rank r reads group j of every other owner o's
 //     shard from its own input and stores it, as four LL8 packets, into
 //     owner o's slot for source r.
 //   reduce (packet polls): owner r loads, for every other source s, the four
-//     packets of group j from its slot for s until all four carry this
-//     call's flag, takes its own input for position r, and sums the R
+//     packets of group j from its slot for s until all four carry the
+//     expected flag, takes its own input for position r, and sums the R
 //     contributions in rank order 0..R-1 in fp32.
-//   broadcast (write mode): owner r rounds once to bf16 and stores the group
-//     into all R outputs through the output-pointer table, as in "optimize
+//   broadcast (write mode): owner r rounds once and stores the group into
+//     all R outputs through the output-pointer table, as in "optimize
 //     allreduce write mode by broadcast output ptr" (ROCm/aiter #1910,
 //     Motivation); completion is the kernel boundary, so no packets flow
 //     back.
 //
-// LL8 packet: one 64-bit word, low 32 bits = two bf16 (lower-indexed element
-// in the low half), high 32 bits = flag.  Stores and loads are 64-bit strong
-// (relaxed, gpu scope) accesses, issued two packets per 16-byte vector
-// instruction; the memory model treats each 64-bit element as single-copy
-// atomic, so a packet whose flag matches carries that call's data.
+// k_fused_ll8 (AR_FUSED_LL8) runs the three steps pipelined over rounds,
+// with one clique of R warp groups per CTA (its comment below).  The
+// comparison forms -- k_fused_ll8_staged (the result broadcast as packets,
+// the ARK page's form) and the three-launch decomposition -- run each phase
+// over the whole message with a CTA per virtual rank (b % R), all CTAs
+// co-resident (cooperative launch), every CTA storing all of its packets
+// before it polls.
+//
+// LL8 packet: one 64-bit word, low 32 bits = one 32-bit word of a group (two
+// bf16/fp16, lower-indexed element in the low half, or one fp32), high 32
+// bits = flag.  Stores and loads are 64-bit strong (relaxed, gpu scope)
+// accesses, four packets per 32-byte vector instruction; the memory model
+// treats each 64-bit element as single-copy atomic, so a packet whose flag
+// matches carries that call's data.
 //
 // Flag rotation.  The ARK page leaves Flag = 1 hardcoded (Known limitations);
-// here the flag is a device-resident epoch in [1, 2^32-1].  Every CTA reads
-// it at start; the last CTA to finish (done counter) advances it, skipping 0,
-// and resets the counter.  Because the epoch never comes from the host, a
+// here the flag is a device-resident epoch in [1, 2^32-1] that skips 0 (the
+// value of zeroed scratch).  Because the epoch never comes from the host, a
 // CUDA-graph replay rotates it too (the by-value epoch hazard G2 of "Add
 // HIP-graph capture coverage for the sharded-relay collectives",
 // meta-pytorch/torchcomms #3850), and it never rewinds while the handle
-// lives (that page's region-lifetime commit).  Scratch is zeroed at handle
-// creation, and a packet left from an earlier call carries an older epoch,
-// so it reads as not yet arrived.
+// lives (that page's region-lifetime commit).  A packet left from an earlier
+// call carries an older flag, so it reads as not yet arrived.
 //
-// Deadlock freedom.  Every CTA finishes all of its packet stores before it
-// polls, and all CTAs are co-resident, so every poll is eventually
-// satisfied.  Every wait is still bounded: after the spin limit the thread
-// records a timeout in the device error word and abandons the call; other
-// waiters see the error word and stop too.
+// Every wait is bounded: after the spin limit the thread records a timeout
+// in the device error word and abandons the call; other waiters see the
+// abandoned epoch and stop too.
 #include <string.h>
 
 #include <algorithm>
@@ -72,6 +72,16 @@ __device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {
 
 __device__ __forceinline__ void st_relaxed_u32(uint32_t* p, uint32_t v) {
   asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t atom_add_release_u32(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.release.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
 }
 
 __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
@@ -390,7 +400,13 @@ __device__ __noinline__ void producer_delay(uint64_t ns) {
 // grid (R(R-1) * 32 bytes per tile group), a few tens of MB, so they live in
 // L2 whatever the message size.  With f.discard, after a warp has read its
 // 32 groups of a round (eight 128-byte lines per source) it drops those
-// lines from L2, so consumed packets are never written back to HBM.
+// lines from L2, so consumed packets are never written back to HBM.  In ring
+// mode (f.ring_rounds = D > 0, for large messages) the packets of round k go
+// instead to slot k mod D of a ring private to the CTA, at the thread's
+// index, and carry the round's own flag (epoch + k; the call moves the epoch
+// on by its rounds); a CTA barrier at the end of every iteration lets a slot
+// be reused only once every warp of the CTA has read it (D = lead + 1), so
+// the lines are overwritten while still in L2 and never written back.
 //
 // Two bodies: iterations whose tiles lie wholly inside every shard (whole
 // 16-byte groups, aligned buffers, offsets within 32 bits: nearly all of
@@ -400,9 +416,10 @@ __device__ __noinline__ void producer_delay(uint64_t ns) {
 // and produce the same bits.
 //
 // Deadlock freedom: iteration i of a warp waits only on scatters of round
-// i - lead by warps of its own CTA, done in their iteration i - lead; by
-// induction on i every wait is eventually satisfied.  The waits are bounded
-// all the same.
+// i - lead by warps of its own CTA, done in their iteration i - lead (and,
+// in ring mode, on the barrier every warp of the CTA reaches at the end of
+// each iteration); by induction on i every wait is eventually satisfied.
+// The waits are bounded all the same.
 template <int R, class E>
 __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, FusedArgs f) {
   constexpr int RO = R > 1 ? R - 1 : 1;  // entries for the other ranks
@@ -476,8 +493,11 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, Fuse
   // itself in, so the last CTA to arrive may install the next epoch (at its
   // end, when the counter's answer has long come back); no CTA waits on
   // another at exit.  The next call, ordered after this kernel, reads it.
+  // The count is a release (the barrier above orders this CTA's read of the
+  // epoch before it); the last CTA takes an acquire fence before its store,
+  // so every CTA's read happens before the new value is written.
   uint32_t arrival = 0;
-  if (threadIdx.x == 0) arrival = atomicAdd(&f.state->done, 1u);
+  if (threadIdx.x == 0) arrival = atom_add_release_u32(&f.state->done, 1u);
   const char* my_in = s_in[r];
   // Slot of (owner r, i-th other source in rank order): r * (R - 1) + i.
   const uint32_t src_row = (uint32_t)(r * (R - 1)) * sstride;
@@ -635,6 +655,7 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, Fuse
     if (R > 1 && f.discard && !ring && rd_round) discard_round<R>(f, r, jtr, t, my_n);
   }
   if (threadIdx.x == 0 && arrival == gridDim.x - 1) {
+    fence_acq_rel_gpu();
     st_relaxed_u32(&f.state->done, 0u);
     st_relaxed_u32(&f.state->epoch, flag_at(epoch, ring ? K_all : 1));
   }
