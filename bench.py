@@ -795,6 +795,7 @@ def run_reference(args):
     lib = oracle.load()
     w = inputs.WORKLOADS[args.workload]
     R, N = w.R, w.count
+    cores, model = host_cpu()
     # calibrate the per-element cost, then size each step's sample so the
     # whole run stays within about a minute
     probe = min(N, 1 << 16)
@@ -825,6 +826,7 @@ def run_reference(args):
         "config": {"workload": args.workload, "R": R, "count": N, "shape": list(w.shape),
                    "fill": w.fill, "variant": "oracle"},
         "cpu_baseline": {"value": round(us_full_call, 3), "unit": "us/call", "cores": 1,
+                         "host_cores": cores, "cpu_model": model,
                          "kind": "oracle", "sample": desc},
         "e2e": {"value": round(us_full_call, 3), "unit": "us/call",
                 "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
