@@ -138,7 +138,11 @@ typedef struct {
  * for fp32 (about 4*(R-1)*max_count bytes for 2-byte types), zeroed here
  * so that no flag matches a live epoch, then written back from L2 to memory
  * (the fused kernel drops consumed packet lines from L2 without writing
- * them back, so they read back as these zeros or as older packets); and
+ * them back, so they read back as these zeros or as older packets; the
+ * write-back writes a temporary buffer of twice the L2 size, about 256 MB,
+ * freed before ar_create returns, unless AR_FUSED_DISCARD=0); the fused
+ * kernel's per-CTA packet rings (3 rounds of (R-1)*32 bytes per co-resident
+ * thread, about 52 MB at R = 8, less for small max_count); and
  * a small state block (epoch, done counter, error word).  Synchronous; not
  * for stream capture.
  * Errors: AR_ERR_INVALID_ARG (R, max_count, out), AR_ERR_UNSUPPORTED (dtype,
