@@ -228,6 +228,12 @@ int occupancy(ar_ctx* h, int variant, int threads) {
 
 constexpr int kMaxRingRounds = 3;  // rings are sized for lead 2 (lead + 1 rounds)
 
+// 32-byte packet groups one CTA's ring needs: `rounds` rounds of R(R-1)
+// slots of Tr groups.
+size_t ring_groups_per_cta(int R, int rounds, int tr) {
+  return (size_t)rounds * (size_t)R * (size_t)(R - 1) * (size_t)tr;
+}
+
 struct FusedMode {
   int lead;         // tiles scattered ahead of the reduce
   int discard;      // drop consumed scratch lines from L2
@@ -235,22 +241,20 @@ struct FusedMode {
 };
 
 // The write-mode fused kernel's packet handling for a call with
-// `shard_groups` groups per shard (the rules at ar_ctx::fused_lead).
-FusedMode fused_mode(const ar_ctx* h, size_t shard_groups) {
+// `shard_groups` groups per shard and warp groups of `tr` threads (the rules
+// at ar_ctx::fused_lead).  Rings only where at least one CTA's ring fits.
+FusedMode fused_mode(const ar_ctx* h, size_t shard_groups, int tr) {
   const double P = 32.0 * h->R * (h->R - 1) * (double)shard_groups;
   const double l2 = h->l2_bytes > 0 ? (double)h->l2_bytes : 128.0 * (1 << 20);
-  const bool ring = h->ring && (h->fused_ring == 1 || (h->fused_ring < 0 && P > 3.0 * l2));
+  const int ring_lead = h->fused_lead > 0 ? h->fused_lead : 1;
+  const bool ring = h->ring &&
+                    h->ring_groups >= ring_groups_per_cta(h->R, ring_lead + 1, tr) &&
+                    (h->fused_ring == 1 || (h->fused_ring < 0 && P > 3.0 * l2));
   FusedMode m;
   m.lead = h->fused_lead > 0 ? h->fused_lead : (ring ? 1 : 2);
   m.ring_rounds = ring ? m.lead + 1 : 0;
   m.discard = ring ? 0 : h->fused_discard >= 0 ? h->fused_discard : (P > 0.5 * l2 ? 1 : 0);
   return m;
-}
-
-// 32-byte packet groups one CTA's ring needs: `rounds` rounds of R(R-1)
-// slots of Tr groups.
-size_t ring_groups_per_cta(int R, int rounds, int tr) {
-  return (size_t)rounds * (size_t)R * (size_t)(R - 1) * (size_t)tr;
 }
 
 // Launch shape of one call.  Threads default to 256.  Fan-out: a persistent
@@ -313,8 +317,8 @@ LaunchCfg shape(ar_ctx* h, int variant, const TuneRow* row, size_t groups, size_
           std::max<size_t>(1, (size_t)occupancy(h, variant, c.threads) * (size_t)h->num_sms);
       size_t ctas = c.ctas > 0 ? (size_t)c.ctas : ceil_div(shard_groups, (size_t)tr);
       c.ctas = (int)std::max<size_t>(1, std::min(ctas, limit));
-      const FusedMode m = fused_mode(h, shard_groups);
-      if (m.ring_rounds) {  // every CTA's ring must fit
+      const FusedMode m = fused_mode(h, shard_groups, tr);
+      if (m.ring_rounds) {  // every CTA's ring must fit (at least one does)
         const size_t per_cta = ring_groups_per_cta(R, m.ring_rounds, tr);
         c.ctas = (int)std::max<size_t>(1, std::min((size_t)c.ctas, h->ring_groups / per_cta));
       }
@@ -405,7 +409,7 @@ ar_status_t launch(ar_ctx* h, int variant, const TuneRow* row, const void* const
       f.state = h->state;
       f.spin_limit_ns = h->spin_limit_ns;
       f.skip_producer = h->skip_producer;
-      const FusedMode m = fused_mode(h, a.shard_groups);
+      const FusedMode m = fused_mode(h, a.shard_groups, cfg.threads / h->R);
       f.lead = m.lead;
       f.discard = m.discard;
       f.ring = h->ring;
