@@ -31,12 +31,13 @@
  *   - AR_ONESHOT_FANOUT_BULK is the same fan-out with every input tile
  *     brought into shared memory, and every result tile sent to the R
  *     outputs, by the bulk-copy (TMA) engine;
- *   - AR_FUSED_LL8_STAGED is that fused kernel without write mode: each
- *     owner sends its reduced shard back as LL8 packets to every rank's
- *     result slot and every rank copies them into its output (the packet
- *     broadcast of the ARK page); AR_PACKET_3OP runs the same three phases
- *     as three launches (that page's send_packet -> recv_reduce_send_packet
- *     -> recv_packet decomposition).  Both exist to measure what write mode
+ *   - AR_FUSED_LL8_STAGED is the fused kernel below without write mode,
+ *     otherwise the same kernel: each owner sends its reduced shard back as
+ *     LL8 packets to every rank's result slot and every rank copies them
+ *     into its output (the packet broadcast of the ARK page);
+ *     AR_PACKET_3OP runs the three phases as three launches over the whole
+ *     message (that page's send_packet -> recv_reduce_send_packet ->
+ *     recv_packet decomposition).  Both exist to measure what write mode
  *     and fusion save;
  *   - AR_FUSED_LL8 is the single fused scatter -> reduce -> broadcast kernel
  *     synchronised by LL packet flags of "Add monolithic fused packet
@@ -61,8 +62,10 @@
  * while the previous kernel in the stream is still running; each waits for that kernel to
  * complete (and its writes to be visible) before touching global memory, so
  * results are those of plain stream order.  The environment variable
- * AR_PDL=0, read by ar_create, turns this off.  The cooperative fused
- * kernels are never launched this way.
+ * AR_PDL=0, read by ar_create, turns this off.  The two pipelined fused
+ * kernels (AR_FUSED_LL8, AR_FUSED_LL8_STAGED) are launched this way at every
+ * size unless AR_PDL=0 or AR_FUSED_PDL=0; the three-launch packet form never
+ * is.
  *
  * Streams are passed as `void*` holding a cudaStream_t (NULL = the legacy
  * default stream), so that this header needs no CUDA header.
@@ -246,12 +249,13 @@ ar_status_t ar_set_variant(ar_handle_t h, int variant);
 ar_status_t ar_select(ar_handle_t h, size_t count, int* variant);
 
 /* ar_set_launch -- override the CTA count and threads per CTA of a variant
- * (0 = automatic).  For AR_FUSED_LL8 ctas is the number of CTAs (each one
- * clique of R warp groups), clamped to the co-resident limit and to the
- * packet rings' room, and threads is rounded to R warp groups of a multiple
- * of 32 threads each (at least 32); for the other variants ctas is the grid
- * (the grid-stride CTA count; a multiple of R for the pull, two-phase and
- * staged packet kernels).  threads must be a multiple of 32 in [64, 512]
+ * (0 = automatic).  For AR_FUSED_LL8 and AR_FUSED_LL8_STAGED ctas is the
+ * number of CTAs (each one clique of R warp groups), clamped to the
+ * co-resident limit (and, in ring mode, to the packet rings' room), and
+ * threads is rounded to R warp groups of a multiple of 32 threads each (at
+ * least 32); for the other variants ctas is the grid (the grid-stride CTA
+ * count; a multiple of R for the pull, two-phase and three-launch packet
+ * kernels).  threads must be a multiple of 32 in [64, 512]
  * (the packet and fan-out kernels accept 128..512). */
 ar_status_t ar_set_launch(ar_handle_t h, int variant, int ctas, int threads);
 

@@ -90,12 +90,15 @@ struct ar_ctx {
   // at 440x5120 with drops); L2/2 < P <= 3 L2: the scratch, with each
   // consumed line dropped from L2 (38.5 vs 45.6 us at 512x8192 without
   // drops); P > 3 L2: per-CTA rings of lead + 1 rounds with lead 1 (138.7 vs
-  // 145.5 us at 16 Mi elements, 269 vs 285 us at 32 Mi).  The AR_FUSED_RING,
-  // AR_FUSED_DISCARD and AR_FUSED_LEAD environment variables force a choice.
+  // 145.5 us at 16 Mi elements, 269 vs 285 us at 32 Mi).  Without write mode
+  // (AR_FUSED_LL8_STAGED) the result packets double P, there are no rings,
+  // and the lead is 1 (69.1 vs 72.5 us at 512x8192, 530 vs 621 us at 32 Mi
+  // elements, 7.0 vs 7.5 us at 4 Ki).  The AR_FUSED_RING, AR_FUSED_DISCARD
+  // and AR_FUSED_LEAD environment variables force a choice.
   int fused_lead = 0;          // tiles scattered ahead of the reduce (0: automatic)
   int fused_discard = -1;      // -1 automatic, 0 never, 1 always (scratch mode)
   int l2_bytes = 0;
-  bool fused_pdl = true;       // programmatic dependent launch for the write-mode fused kernel
+  bool fused_pdl = true;       // programmatic dependent launch for the pipelined fused kernels
   int fused_ring = -1;         // -1 automatic, 0 never, 1 always
   uint64_t* ring = nullptr;    // the rings of all CTAs
   size_t ring_groups = 0;      // its size in 32-byte packet groups
@@ -240,18 +243,21 @@ struct FusedMode {
   int ring_rounds;  // > 0: per-CTA rings of this many rounds instead of the scratch
 };
 
-// The write-mode fused kernel's packet handling for a call with
+// The pipelined fused kernel's packet handling for a call with
 // `shard_groups` groups per shard and warp groups of `tr` threads (the rules
-// at ar_ctx::fused_lead).  Rings only where at least one CTA's ring fits.
-FusedMode fused_mode(const ar_ctx* h, size_t shard_groups, int tr) {
-  const double P = 32.0 * h->R * (h->R - 1) * (double)shard_groups;
+// at ar_ctx::fused_lead).  Rings only in write mode and where at least one
+// CTA's ring fits.  Without write mode the result packets double the
+// footprint that decides on the drops.
+FusedMode fused_mode(const ar_ctx* h, size_t shard_groups, int tr, bool write_mode) {
+  const double P =
+      (write_mode ? 1.0 : 2.0) * 32.0 * h->R * (h->R - 1) * (double)shard_groups;
   const double l2 = h->l2_bytes > 0 ? (double)h->l2_bytes : 128.0 * (1 << 20);
   const int ring_lead = h->fused_lead > 0 ? h->fused_lead : 1;
-  const bool ring = h->ring &&
+  const bool ring = write_mode && h->ring &&
                     h->ring_groups >= ring_groups_per_cta(h->R, ring_lead + 1, tr) &&
                     (h->fused_ring == 1 || (h->fused_ring < 0 && P > 3.0 * l2));
   FusedMode m;
-  m.lead = h->fused_lead > 0 ? h->fused_lead : (ring ? 1 : 2);
+  m.lead = h->fused_lead > 0 ? h->fused_lead : (ring || !write_mode ? 1 : 2);
   m.ring_rounds = ring ? m.lead + 1 : 0;
   m.discard = ring ? 0 : h->fused_discard >= 0 ? h->fused_discard : (P > 0.5 * l2 ? 1 : 0);
   return m;
@@ -308,7 +314,8 @@ LaunchCfg shape(ar_ctx* h, int variant, const TuneRow* row, size_t groups, size_
       c.ctas = (int)(per_rank * (size_t)R);
       break;
     }
-    case AR_FUSED_LL8: {
+    case AR_FUSED_LL8:
+    case AR_FUSED_LL8_STAGED: {
       // One clique per CTA: R warp groups of Tr threads; a persistent grid of
       // at most the co-resident CTAs, at most one per tile of Tr groups.
       const int tr = ar::fused_rank_threads(R, c.threads > 0 ? c.threads : h->fused_threads);
@@ -317,21 +324,11 @@ LaunchCfg shape(ar_ctx* h, int variant, const TuneRow* row, size_t groups, size_
           std::max<size_t>(1, (size_t)occupancy(h, variant, c.threads) * (size_t)h->num_sms);
       size_t ctas = c.ctas > 0 ? (size_t)c.ctas : ceil_div(shard_groups, (size_t)tr);
       c.ctas = (int)std::max<size_t>(1, std::min(ctas, limit));
-      const FusedMode m = fused_mode(h, shard_groups, tr);
+      const FusedMode m = fused_mode(h, shard_groups, tr, variant == AR_FUSED_LL8);
       if (m.ring_rounds) {  // every CTA's ring must fit (at least one does)
         const size_t per_cta = ring_groups_per_cta(R, m.ring_rounds, tr);
         c.ctas = (int)std::max<size_t>(1, std::min((size_t)c.ctas, h->ring_groups / per_cta));
       }
-      break;
-    }
-    case AR_FUSED_LL8_STAGED: {
-      if (c.threads <= 0) c.threads = h->fused_threads;
-      const int per_sm = occupancy(h, variant, c.threads);
-      const size_t limit = (size_t)per_sm * (size_t)h->num_sms / (size_t)R;  // CTAs per rank
-      size_t per_rank = std::max<size_t>(1, ceil_div(shard_groups, (size_t)c.threads));
-      if (c.ctas > 0) per_rank = std::max<size_t>(1, (size_t)c.ctas / (size_t)R);
-      per_rank = std::min(per_rank, limit);
-      c.ctas = (int)(per_rank * (size_t)R);
       break;
     }
     default:
@@ -380,7 +377,7 @@ ar_status_t launch(ar_ctx* h, int variant, const TuneRow* row, const void* const
   LaunchCfg cfg = shape(h, variant, row, a.groups, a.shard_groups);
   cfg.pdl = h->pdl && 2 * (size_t)h->R * count * h->elem_bytes <=
                          (variant == AR_TWOPHASE ? h->pdl_max_bytes_twophase : h->pdl_max_bytes);
-  if (variant == AR_FUSED_LL8) cfg.pdl = h->pdl && h->fused_pdl;
+  if (variant == AR_FUSED_LL8 || variant == AR_FUSED_LL8_STAGED) cfg.pdl = h->pdl && h->fused_pdl;
   if (h->log)
     fprintf(stderr, "[ar] R=%d count=%zu variant=%s ctas=%d threads=%d pdl=%d\n", h->R, count,
             ar_variant_name(variant), cfg.ctas, cfg.threads, (int)cfg.pdl);
@@ -409,7 +406,8 @@ ar_status_t launch(ar_ctx* h, int variant, const TuneRow* row, const void* const
       f.state = h->state;
       f.spin_limit_ns = h->spin_limit_ns;
       f.skip_producer = h->skip_producer;
-      const FusedMode m = fused_mode(h, a.shard_groups, cfg.threads / h->R);
+      const FusedMode m =
+          fused_mode(h, a.shard_groups, cfg.threads / h->R, variant != AR_FUSED_LL8_STAGED);
       f.lead = m.lead;
       f.discard = m.discard;
       f.ring = h->ring;

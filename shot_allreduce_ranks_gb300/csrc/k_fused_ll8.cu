@@ -24,13 +24,13 @@
 //     Motivation); completion is the kernel boundary, so no packets flow
 //     back.
 //
-// k_fused_ll8 (AR_FUSED_LL8) runs the three steps pipelined over rounds,
-// with one clique of R warp groups per CTA (its comment below).  The
-// comparison forms -- k_fused_ll8_staged (the result broadcast as packets,
-// the ARK page's form) and the three-launch decomposition -- run each phase
-// over the whole message with a CTA per virtual rank (b % R), all CTAs
-// co-resident (cooperative launch), every CTA storing all of its packets
-// before it polls.
+// k_fused_ll8 runs the three steps pipelined over rounds, with one clique
+// of R warp groups per CTA (its comment below).  Its write-mode instance is
+// AR_FUSED_LL8; the instance without write mode (AR_FUSED_LL8_STAGED) sends
+// the result back as packets, the ARK page's own form, so the two differ in
+// that step alone.  The three-launch decomposition (AR_PACKET_3OP) runs each
+// phase over the whole message with a CTA per virtual rank (b % R), one
+// kernel per phase.
 //
 // LL8 packet: one 64-bit word, low 32 bits = one 32-bit word of a group (two
 // bf16/fp16, lower-indexed element in the low half, or one fp32), high 32
@@ -138,7 +138,7 @@ __device__ __noinline__ void report_timeout(const FusedArgs& f, int owner, uint3
   st_relaxed_u32(&f.state->abort_epoch, epoch);
 }
 
-// Per-thread view of one launch of a packet kernel.
+// Per-thread view of one launch of a three-launch-form kernel.
 struct Lane {
   int r;              // virtual rank this CTA stands for (blockIdx.x % R)
   size_t t0, tstride; // first group and group stride of this thread within a shard
@@ -179,13 +179,14 @@ __device__ __forceinline__ Lane packet_prologue(const CallArgs& a, const FusedAr
 // advance; every iteration is at least one L2 round trip) it records a
 // timeout and returns false; it also returns false as soon as another
 // waiter of the same call (identified by its base epoch) has given up.
-// With skip >= 0, bit/entry i stands for source i < skip ? i : i + 1 (the
-// array holds only the other ranks' packets); otherwise entry s is source s.
+// Entry i stands for position base + i in the list of sources; with
+// skip >= 0 that list holds only the other ranks (position p is source
+// p < skip ? p : p + 1), otherwise position s is source s.
 template <int N, class Ptr>
 __device__ __forceinline__ bool wait_packets_at(const FusedArgs& f, Packets4 (&pk)[N],
                                                 uint32_t pending, uint32_t flag,
                                                 uint32_t call_epoch, int who, Ptr ptr,
-                                                int skip = -1) {
+                                                int skip = -1, int base = 0) {
 #pragma unroll
   for (int s = 0; s < N; ++s)
     if ((pending & (1u << s)) && pk[s].arrived(flag)) pending &= ~(1u << s);
@@ -205,6 +206,7 @@ __device__ __forceinline__ bool wait_packets_at(const FusedArgs& f, Packets4 (&p
       const uint64_t now = global_timer_ns();
       if (spins == 16u) t_first = now;
       if (spins > kMaxSpins || (spins > 16u && now - t_first > f.spin_limit_ns)) {
+        pending <<= base;
         if (skip >= 0)
           pending = (pending & ((1u << skip) - 1u)) | ((pending >> skip) << (skip + 1));
         report_timeout(f, who, pending, call_epoch);
@@ -303,7 +305,7 @@ __device__ __forceinline__ bool phase_reduce(const CallArgs& a, const FusedArgs&
 }
 
 // ---- receive: rank r copies every other owner's reduced shard out of its
-// result slots into out_r (the staged variants' last step) -------------------
+// result slots into out_r (the three-launch form's last step) ----------------
 template <int R, class E>
 __device__ __forceinline__ bool phase_recv(const CallArgs& a, const FusedArgs& f, const Lane& l,
                                            char* const* s_out) {
@@ -365,13 +367,13 @@ __device__ __forceinline__ void discard_l2_line(const uint64_t* p) {
 // group jt: drop the warp's lines (4 groups of 32 bytes each, 8 lines per
 // source for 32 lanes) that hold some group < n of owner r's slots.
 template <int R>
-__device__ __forceinline__ void discard_round(const FusedArgs& f, int r, size_t jt, size_t t,
-                                              size_t n) {
+__device__ __forceinline__ void discard_round(const uint64_t* region, size_t slot_groups, int r,
+                                              size_t jt, size_t t, size_t n) {
   const size_t wb = jt + (t & ~(size_t)31);  // the warp's first group
   for (int i = (int)(t & 31); i < 8 * (R - 1); i += 32) {
     const size_t line_g = wb + (size_t)(i & 7) * 4;
     if (line_g < n)
-      discard_l2_line(f.scratch + ((size_t)(r * (R - 1) + (i >> 3)) * f.slot_groups + line_g) * 4);
+      discard_l2_line(region + ((size_t)(r * (R - 1) + (i >> 3)) * slot_groups + line_g) * 4);
   }
 }
 
@@ -381,8 +383,13 @@ __device__ __noinline__ void producer_delay(uint64_t ns) {
   for (uint32_t i = 0; i < kMaxSpins && global_timer_ns() - t0 < ns; ++i) __nanosleep(256);
 }
 
-// Write mode: scatter -> reduce -> broadcast straight into all R outputs,
-// pipelined over tiles.
+// Scatter -> reduce -> broadcast, pipelined over tiles.  kWriteMode: the
+// owner stores the sum straight into all R outputs.  Without it (the ARK
+// page's form) the owner stores its own output and sends the sum to every
+// other rank as result packets (a second packet region, same slot layout
+// with a = destination); rank r receives round k - 2 lead in its iteration
+// k, one lead after the owners reduced it, and copies the R - 1 shards into
+// out_r.
 //
 // A CTA is a clique: R warp groups of Tr threads (Tr a multiple of 32), group
 // r standing for virtual rank r, so producers and owners that exchange
@@ -415,12 +422,13 @@ __device__ __noinline__ void producer_delay(uint64_t ns) {
 // first, so each body is a loop of its own.  Both use the same packet layout
 // and produce the same bits.
 //
-// Deadlock freedom: iteration i of a warp waits only on scatters of round
-// i - lead by warps of its own CTA, done in their iteration i - lead (and,
-// in ring mode, on the barrier every warp of the CTA reaches at the end of
-// each iteration); by induction on i every wait is eventually satisfied.
-// The waits are bounded all the same.
-template <int R, class E>
+// Deadlock freedom: iteration i of a warp waits only on warps of its own CTA:
+// on scatters of round i - lead, done in their iteration i - lead; without
+// write mode, on result packets of round i - 2 lead, sent in their iteration
+// i - lead; in ring mode, on the barrier every warp of the CTA reaches at the
+// end of each iteration.  By induction on i every wait is eventually
+// satisfied.  The waits are bounded all the same.
+template <int R, class E, bool kWriteMode = true>
 __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, FusedArgs f) {
   constexpr int RO = R > 1 ? R - 1 : 1;  // entries for the other ranks
   __shared__ const char* s_in[R];
@@ -455,9 +463,13 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, Fuse
   const uint64_t pol_in = l2_policy_evict_first();
   const size_t g0 = (size_t)r * Vs;  // first group of my shard
   const size_t my_n = g0 < a.groups ? min(Vs, a.groups - g0) : 0;
+  const size_t my_n_max = min(Vs, a.groups);  // positions any shard's packets may use
   const size_t tiles = (Vs + Tr - 1) / Tr;
   const size_t K = c < tiles ? (tiles - c + C - 1) / C : 0;  // rounds of this clique
   const size_t L = (size_t)(f.lead > 0 ? f.lead : 1);
+  // Iterations after the last scatter: the reduce trails by L, and without
+  // write mode the receive of the result packets trails the reduce by L.
+  const size_t LL = kWriteMode ? L : 2 * L;
   const bool scatter_on = R > 1 && r != f.skip_producer;
 
   const uint32_t Vs32 = (uint32_t)Vs, SG32 = (uint32_t)f.slot_groups;
@@ -468,7 +480,7 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, Fuse
   // Ring mode: packets of round k live in slot k % D of this CTA's ring,
   // at the thread's index instead of its shard position, and carry the flag
   // of their round (the call moves the epoch on by its rounds).
-  const bool ring = f.ring_rounds > 0;
+  const bool ring = kWriteMode && f.ring_rounds > 0;
   const uint32_t D = ring ? (uint32_t)f.ring_rounds : 1u;
   const uint32_t Tr32 = (uint32_t)Tr, t32 = (uint32_t)t;
   const uint32_t sstride = ring ? Tr32 : SG32;  // groups per (owner, source) slot
@@ -514,7 +526,7 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, Fuse
   // c + kC is whole for k < kf (the same for every warp of the CTA).
   const size_t nf = fast_vs / Tr;
   const size_t kf = nf > c ? (nf - c + C - 1) / C : 0;
-  const size_t k_fast = kf >= K ? K + L : kf;
+  const size_t k_fast = kf >= K ? K + LL : kf;
   // End of an iteration: in ring mode a CTA barrier (a ring slot is reused
   // only after every warp of the CTA has read it; all threads leave the loop
   // together), else a warp vote.
@@ -540,7 +552,7 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, Fuse
   for (; k < k_fast; ++k) {
     // ---------------- whole tiles: 32-bit offsets, no per-group checks
     const size_t jts = (c + k * C) * Tr;                       // scatter tile (round k)
-    const bool rd_round = k >= L;
+    const bool rd_round = k >= L && k < K + L;
     const size_t jtr = rd_round ? (c + (k - L) * C) * Tr : 0;  // reduced tile (round k - L)
     {
       const bool sc = scatter_on && k < K;
@@ -560,7 +572,8 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, Fuse
         for (int q = 0; q < R - 1; ++q)
           st_packets(pkt + (size_t)(s_dst_off[r][q] + ps) * 4, x[q], fl);
       }
-      if (scatter_on && k + 1 < K && k + 1 < k_fast) load_slices(k + 1);
+      const bool preload = scatter_on && k + 1 < K && k + 1 < k_fast;
+      if (kWriteMode && preload) load_slices(k + 1);
       if (rd_round) {
         ok = wait_packets_at<RO>(
             f, pk, R > 1 ? (1u << (R - 1)) - 1u : 0u, flag_of(k - L), epoch, r,
@@ -578,8 +591,51 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, Fuse
           }
           const uint4 y = acc.round();
           const size_t goff = (size_t)(own_off + jr) * kGroupBytes;
+          if (kWriteMode) {
 #pragma unroll
-          for (int q = 0; q < R; ++q) st_v4_stream(s_out[q] + goff, y);
+            for (int q = 0; q < R; ++q) st_v4_stream(s_out[q] + goff, y);
+          } else {
+            // own output, and the sum as result packets to every other rank
+            st_v4_stream(s_out[r] + goff, y);
+#pragma unroll
+            for (int q = 0; q < R - 1; ++q)
+              st_packets(f.rscratch + (size_t)(s_dst_off[r][q] + jr) * 4, y, epoch);
+          }
+        }
+      }
+      // Without write mode: receive the result packets of round k - 2L from
+      // every other owner and copy them into this rank's output, at most four
+      // owners at a time; the next round's slices are loaded once the first
+      // chunk's loads are out (the reduce's registers are free by then).
+      if (!kWriteMode) {
+        constexpr int kChunk = RO < 4 ? RO : 4;
+        const bool rv = R > 1 && k >= 2 * L;
+        const uint32_t jq = rv ? (uint32_t)((c + (k - 2 * L) * C) * Tr + t) : 0u;
+        const uint64_t* const rrow = f.rscratch + (size_t)(src_row + jq) * 4;
+#pragma unroll
+        for (int i0 = 0; i0 < RO; i0 += kChunk) {
+          constexpr int kN = kChunk;
+          const int n = RO - i0 < kN ? RO - i0 : kN;
+          Packets4 rk[kN];
+          if (rv) {
+#pragma unroll
+            for (int i = 0; i < kN; ++i)
+              if (i < n) rk[i].load(rrow + (size_t)(i0 + i) * sstride * 4);
+          }
+          if (i0 == 0 && preload) load_slices(k + 1);
+          if (rv && R > 1) {
+            ok = ok && wait_packets_at<kN>(
+                           f, rk, (1u << n) - 1u, epoch, epoch, r,
+                           [&](int i) { return rrow + (size_t)(i0 + i) * sstride * 4; }, r, i0);
+            if (ok) {
+#pragma unroll
+              for (int i = 0; i < kN; ++i)
+                if (i < n) {
+                  const uint32_t o = (uint32_t)(i0 + i < r ? i0 + i : i0 + i + 1);
+                  st_v4_stream(s_out[r] + (size_t)(o * Vs32 + jq) * kGroupBytes, rk[i].data());
+                }
+            }
+          }
         }
       }
     }
@@ -587,12 +643,16 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, Fuse
       ok = false;
       break;
     }
-    if (R > 1 && f.discard && !ring && rd_round) discard_round<R>(f, r, jtr, t, my_n);
+    if (R > 1 && f.discard && !ring) {
+      if (rd_round) discard_round<R>(f.scratch, f.slot_groups, r, jtr, t, my_n);
+      if (!kWriteMode && k >= 2 * L)
+        discard_round<R>(f.rscratch, f.slot_groups, r, (c + (k - 2 * L) * C) * Tr, t, my_n_max);
+    }
   }
-  for (; ok && k < K + L; ++k) {
+  for (; ok && k < K + LL; ++k) {
     // ---------------- checked body (ragged end, misaligned buffers)
     const size_t jts = (c + k * C) * Tr;
-    const bool rd_round = k >= L;
+    const bool rd_round = k >= L && k < K + L;
     const size_t jtr = rd_round ? (c + (k - L) * C) * Tr : 0;
     {
       const size_t js = jts + t;
@@ -643,8 +703,28 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, Fuse
           const uint4 y = acc.round();
           const size_t g = g0 + jr;
           const int valid = group_valid<E>(g, a.count);
+          if (kWriteMode) {
 #pragma unroll
-          for (int q = 0; q < R; ++q) store_group<E>(s_out[q], g, y, valid, vec);
+            for (int q = 0; q < R; ++q) store_group<E>(s_out[q], g, y, valid, vec);
+          } else {
+            store_group<E>(s_out[r], g, y, valid, vec);
+#pragma unroll
+            for (int q = 1; q < R; ++q)
+              st_packets(slot_ptr<R>(f.rscratch, f.slot_groups, (r + q) % R, r) + jr * 4, y, epoch);
+          }
+        }
+      }
+      // Receive (ragged end): one owner at a time.
+      if (!kWriteMode && R > 1 && k >= 2 * L) {
+        const size_t jq = (c + (k - 2 * L) * C) * Tr + t;
+        for (int o = 0; ok && o < R; ++o) {
+          const size_t g = (size_t)o * Vs + jq;
+          if (o == r || jq >= Vs || g >= a.groups) continue;
+          const uint64_t* const p = slot_ptr<R>(f.rscratch, f.slot_groups, r, o) + jq * 4;
+          Packets4 rk[1];
+          rk[0].load(p);
+          ok = wait_packets_at<1>(f, rk, 1u, epoch, epoch, r, [&](int) { return p; }, -1, o);
+          if (ok) store_group<E>(s_out[r], g, rk[0].data(), group_valid<E>(g, a.count), vec);
         }
       }
     }
@@ -652,25 +732,17 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, Fuse
       ok = false;
       break;
     }
-    if (R > 1 && f.discard && !ring && rd_round) discard_round<R>(f, r, jtr, t, my_n);
+    if (R > 1 && f.discard && !ring) {
+      if (rd_round) discard_round<R>(f.scratch, f.slot_groups, r, jtr, t, my_n);
+      if (!kWriteMode && k >= 2 * L)
+        discard_round<R>(f.rscratch, f.slot_groups, r, (c + (k - 2 * L) * C) * Tr, t, my_n_max);
+    }
   }
   if (threadIdx.x == 0 && arrival == gridDim.x - 1) {
     fence_acq_rel_gpu();
     st_relaxed_u32(&f.state->done, 0u);
     st_relaxed_u32(&f.state->epoch, flag_at(epoch, ring ? K_all : 1));
   }
-}
-
-// Without write mode (the packet broadcast of the ARK page): scatter ->
-// reduce -> result packets to every rank -> every rank copies them out.
-template <int R, class E>
-__global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8_staged(CallArgs a, FusedArgs f) {
-  __shared__ const char* s_in[R];
-  __shared__ char* s_out[R];
-  const Lane l = packet_prologue<R>(a, f, s_in, s_out);
-  phase_scatter<R, E>(a, f, l, s_in[l.r]);
-  if (phase_reduce<R, E, false>(a, f, l, s_in[l.r], s_out)) phase_recv<R, E>(a, f, l, s_out);
-  epoch_advance(f, l.epoch);
 }
 
 // The three-launch decomposition the ARK page replaced (send_packet ->
@@ -705,19 +777,6 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_packet_recv(CallArgs a, Fu
 
 namespace {
 
-cudaLaunchConfig_t cooperative_config(LaunchCfg cfg, cudaStream_t s, cudaLaunchAttribute* attr) {
-  cudaLaunchConfig_t lc = {};
-  lc.gridDim = dim3((unsigned)cfg.ctas);
-  lc.blockDim = dim3((unsigned)cfg.threads);
-  lc.dynamicSmemBytes = 0;
-  lc.stream = s;
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  lc.attrs = attr;
-  lc.numAttrs = 1;
-  return lc;
-}
-
 cudaError_t occ_fused(int R, int dtype, int threads, int* n) {
 #define Q(RR, EE) \
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, k_fused_ll8<RR, EE>, threads, 0)
@@ -728,7 +787,7 @@ cudaError_t occ_fused(int R, int dtype, int threads, int* n) {
 
 cudaError_t occ_staged(int R, int dtype, int threads, int* n) {
 #define Q(RR, EE) \
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, k_fused_ll8_staged<RR, EE>, threads, 0)
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, k_fused_ll8<RR, EE, false>, threads, 0)
   AR_DISPATCH(dtype, R, Q, AR_SWITCH_R8)
 #undef Q
   return cudaErrorInvalidValue;
@@ -761,8 +820,8 @@ cudaError_t launch_fused_ll8(int R, int dtype, const CallArgs& a, const FusedArg
 cudaError_t launch_fused_ll8_staged(int R, int dtype, const CallArgs& a, const FusedArgs& f,
                                     LaunchCfg cfg, cudaStream_t s) {
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t lc = cooperative_config(cfg, s, attr);
-#define L(RR, EE) return cudaLaunchKernelEx(&lc, k_fused_ll8_staged<RR, EE>, a, f)
+  const cudaLaunchConfig_t lc = plain_config(cfg, dim3((unsigned)cfg.ctas), 0, s, attr);
+#define L(RR, EE) return cudaLaunchKernelEx(&lc, k_fused_ll8<RR, EE, false>, a, f)
   AR_DISPATCH(dtype, R, L, AR_SWITCH_R8)
 #undef L
   return cudaErrorInvalidValue;

@@ -319,30 +319,34 @@ def test_ring_mode_missing_producer_times_out_and_recovers(ring_handle, skip):
     h.set_spin_limit_ns(100_000_000)
 
 
-@pytest.mark.parametrize("mode", ["drop", "ring"])
+@pytest.mark.parametrize("mode,variant", [("drop", "fused_ll8"), ("ring", "fused_ll8"),
+                                          ("drop", "fused_ll8_staged"),
+                                          ("drop_lead1", "fused_ll8_staged")])
 @pytest.mark.parametrize("ranks", [3, 8])
-def test_forced_packet_modes_on_ragged_counts(mode, ranks, monkeypatch):
+def test_forced_packet_modes_on_ragged_counts(mode, variant, ranks, monkeypatch):
     """The line drops (their boundary: only lines holding a group below the
-    shard's end are dropped) and the rings, forced on counts that end in a
-    partial tile, a partial group and an odd shard, two calls in a row per
-    count with different inputs: a line dropped from the wrong slot, or a
-    stale packet taken for a new one, would show up as a wrong sum or a
-    timeout."""
+    shard's end are dropped; without write mode, also the result packets'
+    lines) and the rings, forced on counts that end in a partial tile, a
+    partial group and an odd shard, two calls in a row per count with
+    different inputs: a line dropped from the wrong slot, or a stale packet
+    taken for a new one, would show up as a wrong sum or a timeout."""
     from shot_allreduce_ranks_gb300 import AllReduce
-    if mode == "drop":
+    if mode.startswith("drop"):
         monkeypatch.setenv("AR_FUSED_DISCARD", "1")
         monkeypatch.setenv("AR_FUSED_RING", "0")
     else:
         monkeypatch.setenv("AR_FUSED_RING", "1")
+    if mode == "drop_lead1":
+        monkeypatch.setenv("AR_FUSED_LEAD", "1")
     counts = [9, 4097, 65_541, 300_003]
     G.ensure_built()
     with AllReduce(ranks, max(counts)) as h:
-        h.set_variant("fused_ll8")
+        h.set_variant(variant)
         for count in counts:
             for call in range(2):
                 xs = inputs.make_inputs(ranks, count, seed=500 + call + count % 97)
                 outs = h([x.to(G.DEV) for x in xs])
                 torch.cuda.synchronize()
-                G.check_all_outputs(outs, G.oracle_expect(xs),
-                                    "%s R=%d count=%d call %d" % (mode, ranks, count, call))
+                G.check_all_outputs(outs, G.oracle_expect(xs), "%s %s R=%d count=%d call %d"
+                                    % (variant, mode, ranks, count, call))
         assert h.device_status() == AR_OK
