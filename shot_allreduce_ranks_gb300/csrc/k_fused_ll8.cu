@@ -74,20 +74,24 @@ __device__ __forceinline__ void st_relaxed_u32(uint32_t* p, uint32_t v) {
   asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-__device__ __forceinline__ uint32_t atom_add_release_u32(uint32_t* p, uint32_t v) {
-  uint32_t old;
-  asm volatile("atom.release.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+// The pipelined fused kernel treats DevState's epoch (low word) and done
+// (high word) as one 64-bit location.  Every DevState sits at a 256-byte
+// boundary (cudaMalloc, or the allocation-free path's __align__(256) array).
+static_assert(offsetof(DevState, epoch) % 8 == 0 &&
+                  offsetof(DevState, done) == offsetof(DevState, epoch) + 4,
+              "epoch and done must form one aligned 64-bit word, epoch first");
+__device__ __forceinline__ uint64_t* epoch_done(DevState* st) {
+  return reinterpret_cast<uint64_t*>(&st->epoch);
+}
+
+__device__ __forceinline__ uint64_t atom_add_relaxed_u64(uint64_t* p, uint64_t v) {
+  uint64_t old;
+  asm volatile("atom.relaxed.gpu.global.add.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
   return old;
 }
 
-__device__ __forceinline__ void fence_acq_rel_gpu() {
-  asm volatile("fence.acq_rel.gpu;" ::: "memory");
-}
-
-__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
+__device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
 // Four packets of one group in one 32-byte access, flag in the high half of
@@ -439,7 +443,15 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, Fuse
   // kernel in the stream has completed and its writes (the epoch among
   // them) are visible, then let the next one be scheduled.
   pdl_enter();
-  // Pointer tables and the call's epoch, read in one step.
+  // Pointer tables and the call's epoch, read in one step.  Flag rotation at
+  // arrival: thread 2R reads the epoch and counts its CTA in with one 64-bit
+  // atomic on {epoch, done}; the CTA whose count completes the grid writes
+  // {next epoch, 0} in one 64-bit store at its end, so no CTA waits on
+  // another at exit.  Every access this kernel makes to the pair is to that
+  // one location, so coherence alone orders each CTA's read (its atomic, all
+  // of them before the last one) before that store; no fence is needed.  The
+  // next call, ordered after this kernel, reads the new epoch.
+  uint32_t arrival = 0;
   if (threadIdx.x == 0) s_misaligned = 0;
   __syncthreads();
   if (threadIdx.x < R) {
@@ -451,7 +463,9 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, Fuse
     s_out[threadIdx.x - R] = p;
     if (reinterpret_cast<uintptr_t>(p) & 15u) atomicOr(&s_misaligned, 1);
   } else if (threadIdx.x == 2 * R) {
-    s_epoch = ld_acquire_u32(&f.state->epoch);
+    const uint64_t old = atom_add_relaxed_u64(epoch_done(f.state), 1ull << 32);
+    s_epoch = (uint32_t)old;
+    arrival = (uint32_t)(old >> 32);
   }
   // CTA c is clique c; its warp group r (Tr threads, a multiple of 32)
   // stands for virtual rank r.
@@ -501,15 +515,6 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, Fuse
   const size_t fast_vs =
       (vec && f.fast32 && whole > (size_t)(R - 1) * Vs) ? min(Vs, whole - (size_t)(R - 1) * Vs)
                                                         : 0;
-  // Flag rotation at arrival: every CTA has read the epoch before it counts
-  // itself in, so the last CTA to arrive may install the next epoch (at its
-  // end, when the counter's answer has long come back); no CTA waits on
-  // another at exit.  The next call, ordered after this kernel, reads it.
-  // The count is a release (the barrier above orders this CTA's read of the
-  // epoch before it); the last CTA takes an acquire fence before its store,
-  // so every CTA's read happens before the new value is written.
-  uint32_t arrival = 0;
-  if (threadIdx.x == 0) arrival = atom_add_release_u32(&f.state->done, 1u);
   const char* my_in = s_in[r];
   // Slot of (owner r, i-th other source in rank order): r * (R - 1) + i.
   const uint32_t src_row = (uint32_t)(r * (R - 1)) * sstride;
@@ -738,11 +743,8 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, Fuse
         discard_round<R>(f.rscratch, f.slot_groups, r, (c + (k - 2 * L) * C) * Tr, t, my_n_max);
     }
   }
-  if (threadIdx.x == 0 && arrival == gridDim.x - 1) {
-    fence_acq_rel_gpu();
-    st_relaxed_u32(&f.state->done, 0u);
-    st_relaxed_u32(&f.state->epoch, flag_at(epoch, ring ? K_all : 1));
-  }
+  if (threadIdx.x == 2 * R && arrival == gridDim.x - 1)
+    st_relaxed_u64(epoch_done(f.state), (uint64_t)flag_at(epoch, ring ? K_all : 1));
 }
 
 // The three-launch decomposition the ARK page replaced (send_packet ->
