@@ -263,10 +263,10 @@ FusedMode fused_mode(const ar_ctx* h, size_t shard_groups, int tr, bool write_mo
   return m;
 }
 
-// Launch shape of one call.  Threads default to 256.  Fan-out: a persistent
-// grid of co-resident CTAs (two groups per thread per iteration); pull and
-// two-phase: one group per thread, capped at 16 CTAs per SM, a multiple of
-// R; fused: R x min(groups per shard / threads, co-resident CTAs / R).
+// Launch shape of one call.  Fan-out: 128 threads, the co-resident grid,
+// grown for large calls (its comment); pull and two-phase: 256 threads, one
+// group per thread, capped at 16 CTAs per SM, a multiple of R; pipelined
+// fused: cliques of R warp groups, min(tiles per shard, co-resident CTAs).
 LaunchCfg shape(ar_ctx* h, int variant, const TuneRow* row, size_t groups, size_t shard_groups) {
   LaunchCfg c = {0, 0};
   if (row && row->variant == variant) c = {row->ctas, row->threads};
@@ -277,11 +277,23 @@ LaunchCfg shape(ar_ctx* h, int variant, const TuneRow* row, size_t groups, size_
   const size_t cap = (size_t)h->num_sms * 16;
   switch (variant) {
     case AR_ONESHOT_FANOUT: {
+      // The co-resident grid (two groups per thread per pass), replaced for
+      // large calls by a grid that gives a thread at most G groups: 4 (two
+      // 32-byte pairs) for R <= 8, 2 (one pass) above.  A persistent grid
+      // looping over a large message was slower (R = 8, bf16, graph replay:
+      // 22.4 vs 23.3 us at 512x8192, 41.5 vs 45.1 at 8 Mi elements, 79.4 vs
+      // 87.3 at 16 Mi, 155.2 vs 170.9 at 32 Mi; R = 4 at 32 Mi 79.1 vs 88.4;
+      // R = 16 at 4 Mi 42.7 vs 45.6), but a grid of just over one wave of
+      // co-resident CTAs leaves a thin second wave running alone (19.1 vs
+      // 18.3 us at 3.2 Mi), hence the switch at 1.25 waves.
       if (c.threads <= 0) c.threads = 128;
       if (c.ctas <= 0) {
-        const size_t resident = (size_t)occupancy(h, variant, c.threads) * (size_t)h->num_sms;
+        const size_t resident =
+            std::max<size_t>(1, (size_t)occupancy(h, variant, c.threads) * (size_t)h->num_sms);
+        const size_t T = (size_t)c.threads, G = R <= 8 ? 4 : 2;
+        const size_t grown = ceil_div(groups, G * T);
         c.ctas = (int)std::max<size_t>(
-            1, std::min(ceil_div(groups, 2 * (size_t)c.threads), std::max<size_t>(resident, 1)));
+            1, grown >= resident + resident / 4 ? grown : std::min(ceil_div(groups, 2 * T), resident));
       }
       break;
     }

@@ -417,3 +417,21 @@ def test_fanout_wide_requests_edges(count):
     torch.cuda.synchronize()
     G.check_all_outputs(vout, want, "fanout 16B-aligned count=%d" % count)
     ar.set_variant("auto")
+
+
+@pytest.mark.parametrize("R,count", [(8, (1 << 22) + 8 + 3), (8, 3 * (1 << 22) - 5),
+                                     (16, (1 << 22) + 1), (3, (1 << 23) + 13)])
+def test_fanout_large_call_grid(R, count):
+    """Large calls run the fan-out on a grid of several waves (a thread takes
+    at most two 32-byte pairs, or one pass of two groups above eight ranks)
+    instead of the co-resident grid: ragged ends (odd whole groups, a partial
+    group) at sizes above the switch, bit-exact against the oracle."""
+    ar = G.handle(R, count)
+    xs = inputs.make_inputs(R, count, seed=count % 13)
+    want = G.oracle_expect(xs)
+    ar.set_variant("oneshot_fanout")
+    outs = ar(G.to_device(xs))
+    torch.cuda.synchronize()
+    G.check_all_outputs(outs, want, "fanout R=%d count=%d" % (R, count))
+    assert ar.device_status() == 0
+    ar.set_variant("auto")
