@@ -541,6 +541,54 @@ def sets_for(per_set_bytes: int) -> int:
     return min(64, max(2, math.ceil(3 * L2_BYTES / per_set_bytes)))
 
 
+def time_copy_same_bytes(R, N, steps, stream, device, per_graph=50):
+    """Size-matched bandwidth reference: a plain device copy (PyTorch's
+    elementwise kernel, not this library's) that reads 2RN bytes and writes
+    2RN bytes per call, one buffer of R*N bf16 elements, graph-replayed with
+    buffers rotating over more than L2 like the allreduce.  Returns us/call."""
+    import torch
+    elems = R * N
+    nsets = sets_for(4 * elems)
+    src = [torch.ones(elems, dtype=torch.bfloat16, device=device) for _ in range(nsets)]
+    dst = [torch.empty_like(x) for x in src]
+    g_n = max(1, min(per_graph, steps))
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            torch.mul(src[i % nsets], 1, out=dst[i % nsets])
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(g_n):
+            torch.mul(src[i % nsets], 1, out=dst[i % nsets])
+    reps = max(1, steps // g_n)
+    with torch.cuda.stream(stream):
+        g.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / (reps * g_n)
+    del g, src, dst
+    torch.cuda.empty_cache()
+    return us
+
+
+def copy_entry(R, N, steps, stream, device, peak, fanout_us=None):
+    us = time_copy_same_bytes(R, N, steps, stream, device)
+    e = {"us_per_call": round(us, 3),
+         "frac_of_measured": round(4 * R * N / us / 1e3 / peak, 4),
+         "what": "plain device copy of the same 4RN bytes (torch elementwise kernel), "
+                 "graph-replayed, rotating over more than L2"}
+    if fanout_us:
+        e["fanout_over_copy"] = round(fanout_us / us, 3)
+    return e
+
+
 EXTRA_WORKLOADS = ("r8_440x5120", "r8_512x8192", "r8_64mib", "r4_64mib")
 ALL_VARIANTS = ("oneshot_fanout", "oneshot_fanout_bulk", "oneshot_pull", "twophase",
                 "fused_ll8", "fused_ll8_staged", "packet_3op")
@@ -598,6 +646,9 @@ def run_ours(args):
         extra["%s_per_call_l2_flushed_us" % args.variant] = spread(
             time_flushed(ar, sets, N, args.variant, 200, stream, flush))
         del flush
+        extra["copy_same_bytes"] = copy_entry(
+            R, N, min(args.steps, 2000), stream, dev, peak,
+            extra.get("oneshot_fanout", {}).get("us_per_call"))
 
     # ---- the headline: W warm-up steps, then exactly K timed steps
     nvml = NvmlClocks(uuid) if not args.no_clocks else None
@@ -750,6 +801,9 @@ def run_ours(args):
             art.close()
             del tsets
             torch.cuda.empty_cache()
+            extra["%s_copy_same_bytes" % name] = copy_entry(
+                wl.R, wl.count, min(args.steps, 2000 if wl.count < (1 << 24) else 400), stream,
+                dev, peak, extra["%s_oneshot_fanout" % name]["us_per_call"])
         if "%s_fused_ll8" % "r8_64mib" in extra and "r8_64mib_oneshot_fanout" in extra:
             extra["r8_64mib_fused_over_fanout"] = round(
                 extra["r8_64mib_fused_ll8"]["us_per_call"] /

@@ -283,9 +283,10 @@ LaunchCfg shape(ar_ctx* h, int variant, const TuneRow* row, size_t groups, size_
       // looping over a large message was slower (R = 8, bf16, graph replay:
       // 22.4 vs 23.3 us at 512x8192, 41.5 vs 45.1 at 8 Mi elements, 79.4 vs
       // 87.3 at 16 Mi, 155.2 vs 170.9 at 32 Mi; R = 4 at 32 Mi 79.1 vs 88.4;
-      // R = 16 at 4 Mi 42.7 vs 45.6), but a grid of just over one wave of
+      // R = 16 at 4 Mi 42.7 vs 45.6), but a grid of up to about 1.5 waves of
       // co-resident CTAs leaves a thin second wave running alone (19.1 vs
-      // 18.3 us at 3.2 Mi), hence the switch at 1.25 waves.
+      // 18.3 us at 3.2 Mi, 20.0 vs 19.3 at 3.4 Mi), hence the switch at 1.5
+      // waves (512x8192 is 1.7).
       if (c.threads <= 0) c.threads = 128;
       if (c.ctas <= 0) {
         const size_t resident =
@@ -293,7 +294,7 @@ LaunchCfg shape(ar_ctx* h, int variant, const TuneRow* row, size_t groups, size_
         const size_t T = (size_t)c.threads, G = R <= 8 ? 4 : 2;
         const size_t grown = ceil_div(groups, G * T);
         c.ctas = (int)std::max<size_t>(
-            1, grown >= resident + resident / 4 ? grown : std::min(ceil_div(groups, 2 * T), resident));
+            1, grown >= resident + resident / 2 ? grown : std::min(ceil_div(groups, 2 * T), resident));
       }
       break;
     }
