@@ -109,8 +109,9 @@ struct ar_ctx {
   int occ_staged[33] = {};
   int occ_fanout[33] = {};
   int bulk_ctas_per_sm = 0;    // bulk fan-out (fixed 256 threads)
-  // Programmatic dependent launch for the plain (non-cooperative) kernels of
-  // calls that move at most pdl_max_bytes (AR_PDL=0: never).  Measured at
+  // Programmatic dependent launch for the one-shot, two-phase, reduce-scatter
+  // and all-gather kernels of calls that move at most pdl_max_bytes (the
+  // pipelined fused kernels: every call; AR_PDL=0: never).  Measured at
   // R = 8, bf16, back-to-back graph-replayed calls: pull 2.34 vs 2.52 us at
   // 4 Ki elements, 2.78 vs 3.15 at 64 Ki; fan-out 3.39 vs 3.77 at 256 Ki;
   // but two-phase 11.2 vs 9.7 us at 1 Mi (32 MiB moved), hence 16 MiB; and
