@@ -274,6 +274,19 @@ ar_status_t ar_set_spin_limit_ns(ar_handle_t h, uint64_t ns);
  * meta-pytorch/torchcomms #3850. */
 ar_status_t ar_get_device_status(ar_handle_t h, void* stream);
 
+/* ar_last_timeout -- details of the last AR_ERR_TIMEOUT that
+ * ar_get_device_status returned on this handle (host-only, no device work):
+ * *waiting_rank = the virtual rank whose packet wait gave up first,
+ * *missing_rank = the lowest-numbered rank whose packets (scatter packets,
+ * or result packets without write mode) it was still missing, *waits = how
+ * many waits gave up before the others saw the call abandoned.  All -1 / 0
+ * if no timeout has been reported.  AR_ERR_INVALID_ARG for a NULL argument.
+ * Source: no counterpart on the pages; it names the peer that a bounded poll
+ * (the summary of meta-pytorch/torchcomms #3850) gave up on, which a
+ * multi-GPU caller would use to tell a dead peer from a slow one. */
+ar_status_t ar_last_timeout(ar_handle_t h, int* waiting_rank, int* missing_rank,
+                            uint32_t* waits);
+
 /* ar_query -- fill *info. */
 ar_status_t ar_query(ar_handle_t h, ar_info_t* info);
 

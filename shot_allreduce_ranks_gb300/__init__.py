@@ -202,6 +202,14 @@ class AllReduce:
         """AR_OK, or AR_ERR_TIMEOUT if a fused call gave up waiting (clears it)."""
         return self._lib.ar_get_device_status(self._h, _stream_handle(stream))
 
+    def last_timeout(self):
+        """(waiting rank, lowest missing rank, waits that gave up) of the last
+        timeout device_status() reported; (-1, -1, 0) if none."""
+        w, m, n = ctypes.c_int(), ctypes.c_int(), ctypes.c_uint32()
+        check(self._lib.ar_last_timeout(self._h, ctypes.byref(w), ctypes.byref(m),
+                                        ctypes.byref(n)), "ar_last_timeout")
+        return w.value, m.value, n.value
+
     # -- test hooks ----------------------------------------------------------
     def debug_skip_producer(self, rank: int) -> None:
         check(self._lib.ar_debug_skip_producer(self._h, int(rank)), "ar_debug_skip_producer")

@@ -60,6 +60,8 @@ PROTOTYPES = {
     "ar_set_launch": (_ST, [_H, _I, _I, _I]),
     "ar_set_spin_limit_ns": (_ST, [_H, ctypes.c_uint64]),
     "ar_get_device_status": (_ST, [_H, _VP]),
+    "ar_last_timeout": (_ST, [_H, ctypes.POINTER(_I), ctypes.POINTER(_I),
+                              ctypes.POINTER(ctypes.c_uint32)]),
     "ar_query": (_ST, [_H, ctypes.POINTER(ArInfo)]),
     "ar_status_string": (ctypes.c_char_p, [_I]),
     "ar_variant_name": (ctypes.c_char_p, [_I]),

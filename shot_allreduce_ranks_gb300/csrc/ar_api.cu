@@ -81,6 +81,9 @@ struct ar_ctx {
   size_t slot_groups = 0;
   uint64_t spin_limit_ns = 100ull * 1000ull * 1000ull;
   int skip_producer = -1;
+  // The device error block as ar_get_device_status last found it set (it
+  // clears the device copy), for ar_last_timeout.
+  uint32_t last_error = 0, last_error_info = 0, last_timeouts = 0;
   int delay_rank = -1;         // skewed-producer test hook (persists until cleared)
   uint64_t delay_ns = 0;
   // Packet handling of the write-mode fused kernel, chosen per call from the
@@ -718,10 +721,29 @@ ar_status_t ar_get_device_status(ar_handle_t h, void* stream) {
   if (cudaMemcpy(&host, h->state, sizeof host, cudaMemcpyDeviceToHost) != cudaSuccess)
     return AR_ERR_CUDA;
   if (host.error == ar::kDevErrNone) return AR_OK;
+  h->last_error = host.error;
+  h->last_error_info = host.error_info;
+  h->last_timeouts = host.timeouts;
   const uint32_t zero[3] = {0, 0, 0};  // error, error_info, timeouts
   if (cudaMemcpy(&h->state->error, zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
     return AR_ERR_CUDA;
   return host.error == ar::kDevErrTimeout ? AR_ERR_TIMEOUT : AR_ERR_CUDA;
+}
+
+ar_status_t ar_last_timeout(ar_handle_t h, int* waiting_rank, int* missing_rank,
+                            uint32_t* waits) {
+  if (!h || !waiting_rank || !missing_rank || !waits) return AR_ERR_INVALID_ARG;
+  if (h->last_error != ar::kDevErrTimeout) {
+    *waiting_rank = -1;
+    *missing_rank = -1;
+    *waits = 0;
+    return AR_OK;
+  }
+  *waiting_rank = (int)(h->last_error_info >> 16);
+  const uint32_t m = h->last_error_info & 0xFFFFu;
+  *missing_rank = m == 0xFFFFu ? -1 : (int)m;
+  *waits = h->last_timeouts;
+  return AR_OK;
 }
 
 ar_status_t ar_reserve_host_staging(ar_handle_t h) {

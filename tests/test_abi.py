@@ -63,6 +63,7 @@ def test_null_handle_calls(lib):
     assert lib.ar_set_launch(None, 1, 0, 0) == _lib.AR_ERR_INVALID_ARG
     assert lib.ar_set_spin_limit_ns(None, 10 ** 6) == _lib.AR_ERR_INVALID_ARG
     assert lib.ar_get_device_status(None, None) == _lib.AR_ERR_INVALID_ARG
+    assert lib.ar_last_timeout(None, None, None, None) == _lib.AR_ERR_INVALID_ARG
     assert lib.ar_query(None, None) == _lib.AR_ERR_INVALID_ARG
     assert lib.ar_reserve_host_staging(None) == _lib.AR_ERR_INVALID_ARG
     assert lib.ar_debug_skip_producer(None, 0) == _lib.AR_ERR_INVALID_ARG
@@ -101,7 +102,7 @@ def test_core_entry_points_cite_their_source_passage():
     cites = ("#1910", "#245", "#3850", "#254", "no counterpart", "define no such")
     for name in ("ar_create", "ar_allreduce", "ar_destroy", "ar_set_variant",
                  "ar_get_device_status", "ar_status_string",
-                 "ar_allreduce_fused_noalloc"):
+                 "ar_allreduce_fused_noalloc", "ar_last_timeout"):
         comment = _prototype_comment(text, name)
         assert comment, name
         assert "Source:" in comment or "no counterpart" in comment, name

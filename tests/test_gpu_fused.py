@@ -103,7 +103,11 @@ def test_missing_producer_times_out_and_next_call_recovers(ar, variant, skip):
     ar.debug_skip_producer(skip)
     ar(bufs, outs)
     assert ar.device_status() == AR_ERR_TIMEOUT
+    waiting, missing, waits = ar.last_timeout()
+    assert missing == skip, (waiting, missing, waits)
+    assert 0 <= waiting < R and waiting != skip and waits >= 1
     assert ar.device_status() == AR_OK  # reading clears it
+    assert ar.last_timeout() == (waiting, missing, waits)  # the last one reported stays
     ar(bufs, outs)
     assert ar.device_status() == AR_OK
     G.check_all_outputs(outs, want, "call after a timeout")
@@ -313,6 +317,8 @@ def test_ring_mode_missing_producer_times_out_and_recovers(ring_handle, skip):
     h.debug_skip_producer(skip)
     h(bufs, outs)
     assert h.device_status() == AR_ERR_TIMEOUT
+    waiting, missing, _ = h.last_timeout()
+    assert missing == skip and waiting != skip, (waiting, missing)
     h(bufs, outs)
     assert h.device_status() == AR_OK
     G.check_all_outputs(outs, want, "ring call after a timeout")
