@@ -26,7 +26,7 @@ def _cleanup():
 
 
 @pytest.mark.parametrize("variant", G.PARITY_VARIANTS)
-@pytest.mark.parametrize("R", [1, 2, 3, 5, 8])
+@pytest.mark.parametrize("R", [1, 2, 3, 4, 5, 6, 7, 8])
 def test_ragged_counts(variant, R):
     ar = G.handle(R, max(RAGGED))
     for count in RAGGED:
