@@ -99,10 +99,13 @@ __device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
 // the owner); loads mark it evict-first once read.  As a vector access, the
 // memory model treats it as four 64-bit accesses, each single-copy atomic.
 // kCta: strong at CTA scope only, which suffices when the producer and the
-// owner are threads of one CTA (the pipelined kernel's cliques; measured
-// 38.35 vs 38.62 us at 512x8192 and 261.9 vs 268.7 us at 64 MiB per rank
-// against GPU scope); the three-launch form, whose producers and owners are
-// in different CTAs, keeps GPU scope.
+// owner are threads of one CTA (the pipelined kernel's cliques).  The
+// write-mode instance uses it (R = 8, bf16, same-call A/B against GPU scope:
+// 38.2 vs 38.4 us at 512x8192, 135.0 vs 137.8 at 16 Mi elements, 261.2 vs
+// 268.3 at 32 Mi; R = 6: 233.0 vs 236.2 at 32 Mi); the instance without
+// write mode keeps GPU scope, which was faster for it (R = 6: 337 vs 366 us,
+// R = 4: 215 vs 222 at 32 Mi), as does the three-launch form, whose
+// producers and owners are in different CTAs.
 template <bool kCta = false>
 __device__ __forceinline__ void st_packets(uint64_t* p, uint4 x, uint32_t epoch) {
   const uint64_t hi = (uint64_t)epoch << 32;
@@ -586,18 +589,18 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, Fuse
         own = ld_v4_stream<true>(my_in + (size_t)(own_off + jr) * kGroupBytes, pol_in);
 #pragma unroll
         for (int i = 0; i < R - 1; ++i)
-          pk[i].load<true>(pkt + (size_t)(src_row + (uint32_t)i * sstride + pr) * 4);
+          pk[i].load<kWriteMode>(pkt + (size_t)(src_row + (uint32_t)i * sstride + pr) * 4);
       }
       if (sc) {
         const uint32_t ps = ppos(k, js), fl = flag_of(k);
 #pragma unroll
         for (int q = 0; q < R - 1; ++q)
-          st_packets<true>(pkt + (size_t)(s_dst_off[r][q] + ps) * 4, x[q], fl);
+          st_packets<kWriteMode>(pkt + (size_t)(s_dst_off[r][q] + ps) * 4, x[q], fl);
       }
       const bool preload = scatter_on && k + 1 < K && k + 1 < k_fast;
       if (kWriteMode && preload) load_slices(k + 1);
       if (rd_round) {
-        ok = wait_packets_at<RO, true>(
+        ok = wait_packets_at<RO, kWriteMode>(
             f, pk, R > 1 ? (1u << (R - 1)) - 1u : 0u, flag_of(k - L), epoch, r,
             [&](int i) { return pkt + (size_t)(src_row + (uint32_t)i * sstride + pr) * 4; }, r);
         if (ok) {
@@ -621,7 +624,7 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, Fuse
             st_v4_stream(s_out[r] + goff, y);
 #pragma unroll
             for (int q = 0; q < R - 1; ++q)
-              st_packets<true>(f.rscratch + (size_t)(s_dst_off[r][q] + jr) * 4, y, epoch);
+              st_packets<kWriteMode>(f.rscratch + (size_t)(s_dst_off[r][q] + jr) * 4, y, epoch);
           }
         }
       }
@@ -642,11 +645,11 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, Fuse
           if (rv) {
 #pragma unroll
             for (int i = 0; i < kN; ++i)
-              if (i < n) rk[i].load<true>(rrow + (size_t)(i0 + i) * sstride * 4);
+              if (i < n) rk[i].load<kWriteMode>(rrow + (size_t)(i0 + i) * sstride * 4);
           }
           if (i0 == 0 && preload) load_slices(k + 1);
           if (rv && R > 1) {
-            ok = ok && wait_packets_at<kN, true>(
+            ok = ok && wait_packets_at<kN, kWriteMode>(
                            f, rk, (1u << n) - 1u, epoch, epoch, r,
                            [&](int i) { return rrow + (size_t)(i0 + i) * sstride * 4; }, r, i0);
             if (ok) {
@@ -699,7 +702,7 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, Fuse
 #pragma unroll
         for (int s = 0; s < R; ++s)
           if (s != r) {
-            pk[s].load<true>(slot_ptr<R>(pkt, sstride, r, s) + (size_t)ppos(k - L, (uint32_t)jr) * 4);
+            pk[s].load<kWriteMode>(slot_ptr<R>(pkt, sstride, r, s) + (size_t)ppos(k - L, (uint32_t)jr) * 4);
             pending |= 1u << s;
           }
       }
@@ -708,13 +711,13 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, Fuse
         for (int q = 1; q < R; ++q) {
           const int o = (r + q) % R;
           if ((size_t)o * Vs + js < a.groups)
-            st_packets<true>(slot_ptr<R>(pkt, sstride, o, r) + (size_t)ppos(k, (uint32_t)js) * 4,
+            st_packets<kWriteMode>(slot_ptr<R>(pkt, sstride, o, r) + (size_t)ppos(k, (uint32_t)js) * 4,
                        x[q - 1], flag_of(k));
         }
       }
       if (rd) {
         const size_t pr = ppos(k - L, (uint32_t)jr);
-        ok = wait_packets_at<R, true>(f, pk, pending, flag_of(k - L), epoch, r, [&](int s) {
+        ok = wait_packets_at<R, kWriteMode>(f, pk, pending, flag_of(k - L), epoch, r, [&](int s) {
           return slot_ptr<R>(pkt, sstride, r, s) + pr * 4;
         });
         if (ok) {
@@ -732,7 +735,7 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, Fuse
             store_group<E>(s_out[r], g, y, valid, vec);
 #pragma unroll
             for (int q = 1; q < R; ++q)
-              st_packets<true>(slot_ptr<R>(f.rscratch, f.slot_groups, (r + q) % R, r) + jr * 4, y, epoch);
+              st_packets<kWriteMode>(slot_ptr<R>(f.rscratch, f.slot_groups, (r + q) % R, r) + jr * 4, y, epoch);
           }
         }
       }
@@ -744,8 +747,8 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, Fuse
           if (o == r || jq >= Vs || g >= a.groups) continue;
           const uint64_t* const p = slot_ptr<R>(f.rscratch, f.slot_groups, r, o) + jq * 4;
           Packets4 rk[1];
-          rk[0].load<true>(p);
-          ok = wait_packets_at<1, true>(f, rk, 1u, epoch, epoch, r, [&](int) { return p; }, -1, o);
+          rk[0].load<kWriteMode>(p);
+          ok = wait_packets_at<1, kWriteMode>(f, rk, 1u, epoch, epoch, r, [&](int) { return p; }, -1, o);
           if (ok) store_group<E>(s_out[r], g, rk[0].data(), group_valid<E>(g, a.count), vec);
         }
       }
