@@ -271,7 +271,8 @@ FusedMode fused_mode(const ar_ctx* h, size_t shard_groups, int tr, bool write_mo
 // grown for large calls (its comment); pull and two-phase: 256 threads, one
 // group per thread, capped at 16 CTAs per SM, a multiple of R; pipelined
 // fused: cliques of R warp groups, min(tiles per shard, co-resident CTAs).
-LaunchCfg shape(ar_ctx* h, int variant, const TuneRow* row, size_t groups, size_t shard_groups) {
+LaunchCfg shape(ar_ctx* h, int variant, const TuneRow* row, size_t groups, size_t shard_groups,
+                bool host_memory = false) {
   LaunchCfg c = {0, 0};
   if (row && row->variant == variant) c = {row->ctas, row->threads};
   const LaunchCfg& o = h->override_cfg[variant];
@@ -290,15 +291,19 @@ LaunchCfg shape(ar_ctx* h, int variant, const TuneRow* row, size_t groups, size_
       // R = 16 at 4 Mi 42.7 vs 45.6), but a grid of up to about 1.5 waves of
       // co-resident CTAs leaves a thin second wave running alone (19.1 vs
       // 18.3 us at 3.2 Mi, 20.0 vs 19.3 at 3.4 Mi), hence the switch at 1.5
-      // waves (512x8192 is 1.7).
+      // waves (512x8192 is 1.7).  On page-locked host buffers (the host
+      // path) the co-resident grid stays: more CTAs in flight over the host
+      // link were slower (553 vs 492 us with 2048 CTAs at 512x8192, 325 vs
+      // 290 with 1024 at 440x5120).
       if (c.threads <= 0) c.threads = 128;
       if (c.ctas <= 0) {
         const size_t resident =
             std::max<size_t>(1, (size_t)occupancy(h, variant, c.threads) * (size_t)h->num_sms);
         const size_t T = (size_t)c.threads, G = R <= 8 ? 4 : 2;
         const size_t grown = ceil_div(groups, G * T);
+        const bool waves = !host_memory && grown >= resident + resident / 2;
         c.ctas = (int)std::max<size_t>(
-            1, grown >= resident + resident / 2 ? grown : std::min(ceil_div(groups, 2 * T), resident));
+            1, waves ? grown : std::min(ceil_div(groups, 2 * T), resident));
       }
       break;
     }
@@ -380,7 +385,7 @@ ar_status_t check_device(const ar_ctx* h) {
 }
 
 ar_status_t launch(ar_ctx* h, int variant, const TuneRow* row, const void* const* d_in,
-                   void* const* d_out, size_t count, cudaStream_t s) {
+                   void* const* d_out, size_t count, cudaStream_t s, bool host_memory = false) {
   NvtxRange range(range_name(variant));
   CallArgs a;
   if (is_packet_variant(variant) && h->R > AR_MAX_PACKET_RANKS) return AR_ERR_UNSUPPORTED;
@@ -391,7 +396,7 @@ ar_status_t launch(ar_ctx* h, int variant, const TuneRow* row, const void* const
   a.shard_groups = ceil_div(a.groups, (size_t)h->R);
   a.state = h->state;
   a.spin_limit_ns = h->spin_limit_ns;
-  LaunchCfg cfg = shape(h, variant, row, a.groups, a.shard_groups);
+  LaunchCfg cfg = shape(h, variant, row, a.groups, a.shard_groups, host_memory);
   cfg.pdl = h->pdl && 2 * (size_t)h->R * count * h->elem_bytes <=
                          (variant == AR_TWOPHASE ? h->pdl_max_bytes_twophase : h->pdl_max_bytes);
   if (variant == AR_FUSED_LL8 || variant == AR_FUSED_LL8_STAGED) cfg.pdl = h->pdl && h->fused_pdl;
@@ -826,7 +831,8 @@ ar_status_t ar_allreduce_host(ar_handle_t h, const void* const* h_in, void* cons
     // choice for host memory unless a variant is forced.
     const int v = h->variant != AR_AUTO ? h->variant : AR_ONESHOT_FANOUT;
     return launch(h, v, nullptr, reinterpret_cast<const void* const*>(h->direct_tables),
-                  reinterpret_cast<void* const*>(h->direct_tables + h->R), count, s);
+                  reinterpret_cast<void* const*>(h->direct_tables + h->R), count, s,
+                  /*host_memory=*/true);
   }
 
   // Staging path (pageable host memory): one copy per rank each way.
