@@ -332,9 +332,11 @@ ar_status_t ar_allreduce_host(ar_handle_t h, const void* const* h_in,
 
 /* ---- test hooks (faults made on the host side) --------------------------
  *
- * ar_debug_skip_producer -- for the NEXT AR_FUSED_LL8 call only, virtual
- * rank `rank` stores none of its packets, so every owner's wait for that
- * rank runs out after the spin limit and the error word is set.  -1 clears.
+ * ar_debug_skip_producer -- for the NEXT call of a packet variant only
+ * (AR_FUSED_LL8, AR_FUSED_LL8_STAGED, AR_PACKET_3OP), virtual rank `rank`
+ * stores none of its scatter packets, so every owner's wait for that rank
+ * runs out after the spin limit, the error word is set and ar_last_timeout
+ * names `rank` as the missing one.  -1 clears.
  * No memory is touched out of bounds and no wait is unbounded.
  *
  * ar_debug_set_epoch / ar_debug_get_epoch -- synchronous write / read of
@@ -346,9 +348,10 @@ ar_status_t ar_allreduce_host(ar_handle_t h, const void* const* h_in,
  */
 ar_status_t ar_debug_skip_producer(ar_handle_t h, int rank);
 
-/* ar_debug_delay_producer -- for every later AR_FUSED_LL8 call (until
- * cleared with rank -1 or ns 0), the CTAs of virtual rank `rank` wait `ns`
- * nanoseconds of the device's global timer before their first packet store,
+/* ar_debug_delay_producer -- for every later AR_FUSED_LL8 or
+ * AR_FUSED_LL8_STAGED call (until cleared with rank -1 or ns 0), the warps of
+ * virtual rank `rank` wait `ns` nanoseconds of the device's global timer
+ * before their first packet store,
  * so every owner polls for that rank's packets longer than the others'.
  * This is the skewed producer of "Add HIP-graph capture coverage for the
  * sharded-relay collectives" (meta-pytorch/torchcomms #3850, summary:
