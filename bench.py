@@ -902,6 +902,46 @@ def sweep_counts():
     return sorted(counts)
 
 
+# Variants the selector may choose (the staged and three-launch packet forms
+# are comparisons, not candidates).
+SELECTABLE = ("oneshot_pull", "oneshot_fanout", "oneshot_fanout_bulk", "twophase", "fused_ll8")
+MAX_TUNED_COUNT = 1 << 40
+
+
+def tuning_rows(R, timings):
+    """Selector rows (R, max_count, variant) from measured us/call.
+
+    `timings` maps count -> {variant: us}.  The fastest selectable variant at
+    each measured count wins; consecutive counts with the same winner merge
+    into one row; a row ends at the geometric mean of the last count its
+    variant won and the first count the next one won (where the two curves
+    cross, to the resolution of the sweep); the last row is open-ended."""
+    winners = []
+    for c in sorted(timings):
+        cand = {v: t for v, t in timings[c].items() if v in SELECTABLE}
+        if cand:
+            winners.append((c, min(sorted(cand), key=cand.get)))
+    rows = []
+    for i, (c, v) in enumerate(winners):
+        if i + 1 < len(winners) and winners[i + 1][1] == v:
+            continue
+        if i + 1 < len(winners):
+            nxt = winners[i + 1][0]
+            bound = max(c, min(math.isqrt(c * nxt), nxt - 1))
+        else:
+            bound = MAX_TUNED_COUNT
+        rows.append((R, bound, v))
+    return rows
+
+
+def write_tuning(path, rows, header):
+    """The AR_TUNING_FILE format: one "R max_count variant" row per line."""
+    with open(path, "w") as f:
+        f.write("# %s\n" % header)
+        for R, max_count, v in rows:
+            f.write("%d %d %s\n" % (R, max_count, v))
+
+
 def run_sweep(args):
     """One JSON line per (count, variant): graph-replay us/call and
     algorithmic GB/s, inputs rotating over more than L2."""
@@ -920,6 +960,7 @@ def run_sweep(args):
                                         "packet_3op"))]
     ar = AllReduce(R, max(counts), device=dev, dtype=dtype)
     peak, _ = measured_peaks()
+    timings = {}
     for N in counts:
         per = 2 * ebytes * R * N
         nsets = min(16, max(2, math.ceil(3 * L2_BYTES / per)))
@@ -933,6 +974,7 @@ def run_sweep(args):
         for v in variants:
             t, _, _, _ = time_variant(ar, sets, N, v, steps, 20, stream, "graph")
             us = t * 1e6 / steps
+            timings.setdefault(N, {})[v] = us
             alg = alg_bytes(v, R, N) * ebytes // 2
             print(json.dumps({"R": R, "count": N, "dtype": args.dtype, "variant": v,
                               "us_per_call": round(us, 3),
@@ -944,6 +986,13 @@ def run_sweep(args):
     if ar.device_status() != 0:
         raise RuntimeError("device error word set during the sweep")
     ar.close()
+    if args.write_tuning:
+        rows = tuning_rows(R, timings)
+        write_tuning(args.write_tuning, rows,
+                     "selector table from bench.py --sweep (R=%d, %s, graph replay); "
+                     "load with AR_TUNING_FILE" % (R, args.dtype))
+        print(json.dumps({"tuning_file": args.write_tuning,
+                          "rows": [list(r) for r in rows]}), flush=True)
 
 
 def run_collective(args):
@@ -1030,6 +1079,9 @@ def parse_args(argv=None):
     p.add_argument("--sweep", action="store_true",
                    help="time every variant over the benchmark message sizes (JSON lines)")
     p.add_argument("--sweep-r", type=int, default=8)
+    p.add_argument("--write-tuning", default=None, metavar="FILE",
+                   help="with --sweep: write the fastest variant per size as an "
+                        "AR_TUNING_FILE selector table")
     p.add_argument("--dtype", choices=["bf16", "fp16", "fp32"], default="bf16",
                    help="element type of --sweep and --collective")
     p.add_argument("--collective", choices=["reduce_scatter", "all_gather"], default=None,

@@ -125,3 +125,44 @@ def test_reference_arm_prints_one_contract_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     assert d["config"]["workload"] == "r8_4096"
+
+
+def _timings(rows):
+    """{count: {variant: us}} from (count, {variant: us}) pairs."""
+    return {c: dict(t) for c, t in rows}
+
+
+def test_tuning_rows_merge_runs_and_split_where_the_curves_cross():
+    t = _timings([
+        (4096, {"oneshot_pull": 2.1, "oneshot_fanout": 2.5, "fused_ll8": 4.9}),
+        (65536, {"oneshot_pull": 2.4, "oneshot_fanout": 2.7}),
+        (131072, {"oneshot_pull": 3.1, "oneshot_fanout": 3.0}),
+        (1048576, {"oneshot_pull": 15.0, "oneshot_fanout": 7.9, "twophase": 9.9}),
+    ])
+    rows = bench.tuning_rows(8, t)
+    # pull up to the geometric mean of 65536 and 131072, fan-out beyond
+    assert rows == [(8, 92681, "oneshot_pull"), (8, bench.MAX_TUNED_COUNT, "oneshot_fanout")]
+    # every measured count lands in the row of its own winner
+    for c, v in ((4096, "oneshot_pull"), (65536, "oneshot_pull"), (131072, "oneshot_fanout"),
+                 (1048576, "oneshot_fanout")):
+        assert next(r[2] for r in rows if c <= r[1]) == v
+
+
+def test_tuning_rows_skip_the_comparison_forms_and_handle_one_size():
+    t = _timings([(8, {"fused_ll8_staged": 0.1, "packet_3op": 0.1, "twophase": 3.0,
+                       "oneshot_fanout_bulk": 2.0})])
+    assert bench.tuning_rows(16, t) == [(16, bench.MAX_TUNED_COUNT, "oneshot_fanout_bulk")]
+    # a boundary never falls below the last count the earlier variant won
+    t = _timings([(7, {"oneshot_pull": 1.0, "oneshot_fanout": 2.0}),
+                  (8, {"oneshot_pull": 2.0, "oneshot_fanout": 1.0})])
+    assert bench.tuning_rows(2, t) == [(2, 7, "oneshot_pull"),
+                                       (2, bench.MAX_TUNED_COUNT, "oneshot_fanout")]
+
+
+def test_write_tuning_writes_the_library_format(tmp_path):
+    path = tmp_path / "table.txt"
+    bench.write_tuning(str(path), [(8, 92681, "oneshot_pull"), (8, 1 << 40, "oneshot_fanout")],
+                       "test")
+    lines = path.read_text().splitlines()
+    assert lines[0].startswith("#")
+    assert lines[1:] == ["8 92681 oneshot_pull", "8 1099511627776 oneshot_fanout"]

@@ -308,6 +308,22 @@ def test_tuning_file_and_forced_variant_env(tmp_path, monkeypatch):
         outs = G.run_variant(ar, G.to_device(xs), "auto")
         G.check_all_outputs(outs, G.oracle_expect(xs), "tuning-file auto")
     monkeypatch.delenv("AR_TUNING_FILE")
+    # a table written from sweep timings (bench.py --sweep --write-tuning)
+    import bench
+    rows = bench.tuning_rows(8, {4096: {"oneshot_pull": 2.0, "oneshot_fanout": 2.5},
+                                 16384: {"oneshot_pull": 3.0, "oneshot_fanout": 2.6},
+                                 65536: {"twophase": 1.0, "oneshot_fanout": 2.6}})
+    written = tmp_path / "written.txt"
+    bench.write_tuning(str(written), rows, "test")
+    monkeypatch.setenv("AR_TUNING_FILE", str(written))
+    with AllReduce(8, 100000) as ar:
+        assert ar.select(4096) == "oneshot_pull"
+        assert ar.select(8192) == "oneshot_pull"       # up to sqrt(4096 * 16384)
+        assert ar.select(8193) == "oneshot_fanout"
+        assert ar.select(16384) == "oneshot_fanout"
+        assert ar.select(65536) == "twophase"
+        assert ar.select(100000) == "twophase"
+    monkeypatch.delenv("AR_TUNING_FILE")
     monkeypatch.setenv("AR_VARIANT", "twophase")
     with AllReduce(4, 100) as ar:
         assert ar.select(10) == "twophase"
