@@ -348,6 +348,16 @@ ar_status_t ar_allreduce_host(ar_handle_t h, const void* const* h_in,
  */
 ar_status_t ar_debug_skip_producer(ar_handle_t h, int rank);
 
+/* ar_debug_check_guards -- synchronise the device, then check the guard
+ * zones (4 KiB of a fixed byte value before and after each packet region the
+ * handle owns: the scatter scratch, the result scratch and the rings), which
+ * nothing in the library writes.  *intact = 1 if every guard byte still holds
+ * its value, 0 if some kernel wrote outside a packet region.  AR_ERR_CUDA if
+ * a copy fails, AR_ERR_INVALID_ARG for a NULL argument.  A stand-in for a
+ * memory checker on the library's own buffers (output buffers belong to the
+ * caller, who can surround them with guards of its own). */
+ar_status_t ar_debug_check_guards(ar_handle_t h, int* intact);
+
 /* ar_debug_delay_producer -- for every later AR_FUSED_LL8 or
  * AR_FUSED_LL8_STAGED call (until cleared with rank -1 or ns 0), the warps of
  * virtual rank `rank` wait `ns` nanoseconds of the device's global timer

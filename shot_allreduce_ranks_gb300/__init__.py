@@ -214,6 +214,12 @@ class AllReduce:
     def debug_skip_producer(self, rank: int) -> None:
         check(self._lib.ar_debug_skip_producer(self._h, int(rank)), "ar_debug_skip_producer")
 
+    def debug_guards_intact(self) -> bool:
+        """True if nothing wrote outside the handle's packet regions."""
+        ok = ctypes.c_int()
+        check(self._lib.ar_debug_check_guards(self._h, ctypes.byref(ok)), "ar_debug_check_guards")
+        return bool(ok.value)
+
     def debug_delay_producer(self, rank: int, ns: int) -> None:
         check(self._lib.ar_debug_delay_producer(self._h, int(rank), int(ns)),
               "ar_debug_delay_producer")

@@ -68,6 +68,7 @@ PROTOTYPES = {
     "ar_reserve_host_staging": (_ST, [_H]),
     "ar_allreduce_host": (_ST, [_H, _VP, _VP, _SZ, _VP]),
     "ar_debug_skip_producer": (_ST, [_H, _I]),
+    "ar_debug_check_guards": (_ST, [_H, ctypes.POINTER(_I)]),
     "ar_debug_delay_producer": (_ST, [_H, _I, ctypes.c_uint64]),
     "ar_debug_set_epoch": (_ST, [_H, ctypes.c_uint32]),
     "ar_debug_get_epoch": (_ST, [_H, ctypes.POINTER(ctypes.c_uint32)]),

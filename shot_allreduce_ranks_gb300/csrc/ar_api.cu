@@ -77,6 +77,10 @@ struct ar_ctx {
   DevState* state = nullptr;
   uint64_t* scratch = nullptr;   // scatter packets
   uint64_t* rscratch = nullptr;  // result packets (staged variants)
+  // Allocations behind the packet regions (scratch, rscratch, ring), each
+  // with a guard zone before and after the region (guarded_alloc).
+  void* region_base[3] = {nullptr, nullptr, nullptr};
+  size_t region_bytes[3] = {0, 0, 0};
   size_t scratch_bytes = 0;      // bytes of each region
   size_t slot_groups = 0;
   uint64_t spin_limit_ns = 100ull * 1000ull * 1000ull;
@@ -359,6 +363,23 @@ LaunchCfg shape(ar_ctx* h, int variant, const TuneRow* row, size_t groups, size_
   return c;
 }
 
+// Guard zones around every packet region: kGuardBytes of kGuardByte before
+// and after it, never touched by the library, checked by
+// ar_debug_check_guards (writes outside a region would change them).
+constexpr size_t kGuardBytes = 4096;
+constexpr unsigned char kGuardByte = 0x5A;
+
+cudaError_t guarded_alloc(size_t bytes, void** region, void** base) {
+  char* p = nullptr;
+  cudaError_t e = cudaMalloc(&p, bytes + 2 * kGuardBytes);
+  if (e != cudaSuccess) return e;
+  *base = p;
+  if ((e = cudaMemset(p, kGuardByte, kGuardBytes)) != cudaSuccess) return e;
+  if ((e = cudaMemset(p + kGuardBytes + bytes, kGuardByte, kGuardBytes)) != cudaSuccess) return e;
+  *region = p + kGuardBytes;  // 256-byte aligned like the allocation
+  return cudaSuccess;
+}
+
 // Writes a temporary buffer of twice the L2 size on the current device and
 // waits, so that every dirty line L2 held before (the packet scratch just
 // zeroed) has been written back to memory.  The fused kernel drops consumed
@@ -553,10 +574,16 @@ ar_status_t ar_create(int R, size_t max_count, int dtype, ar_handle_t* out) {
 
   ar_status_t st = AR_OK;
   if (cudaMalloc(&h->state, sizeof(DevState)) != cudaSuccess) st = AR_ERR_OOM;
-  if (st == AR_OK && h->scratch_bytes &&
-      (cudaMalloc(&h->scratch, h->scratch_bytes) != cudaSuccess ||
-       cudaMalloc(&h->rscratch, h->scratch_bytes) != cudaSuccess))
-    st = AR_ERR_OOM;
+  if (st == AR_OK && h->scratch_bytes) {
+    void* r0 = nullptr;
+    void* r1 = nullptr;
+    if (guarded_alloc(h->scratch_bytes, &r0, &h->region_base[0]) != cudaSuccess ||
+        guarded_alloc(h->scratch_bytes, &r1, &h->region_base[1]) != cudaSuccess)
+      st = AR_ERR_OOM;
+    h->scratch = static_cast<uint64_t*>(r0);
+    h->rscratch = static_cast<uint64_t*>(r1);
+    h->region_bytes[0] = h->region_bytes[1] = h->scratch_bytes;
+  }
   if (st == AR_OK) {
     DevState init;
     memset(&init, 0, sizeof init);
@@ -579,9 +606,12 @@ ar_status_t ar_create(int R, size_t max_count, int dtype, ar_handle_t* out) {
       cap = std::max(cap, ctas * ring_groups_per_cta(R, kMaxRingRounds, tr));
     }
     h->ring_groups = cap;
-    if (cap && (cudaMalloc(&h->ring, cap * 32) != cudaSuccess ||
-                cudaMemset(h->ring, 0, cap * 32) != cudaSuccess))
+    void* r2 = nullptr;
+    if (cap && (guarded_alloc(cap * 32, &r2, &h->region_base[2]) != cudaSuccess ||
+                cudaMemset(r2, 0, cap * 32) != cudaSuccess))
       st = AR_ERR_OOM;
+    h->ring = static_cast<uint64_t*>(r2);
+    h->region_bytes[2] = cap * 32;
   }
   if (st == AR_OK && cudaDeviceSynchronize() != cudaSuccess) st = AR_ERR_CUDA;
   if (st == AR_OK && h->scratch_bytes && h->fused_discard != 0 && write_back_l2(dev) != cudaSuccess)
@@ -602,9 +632,8 @@ ar_status_t ar_destroy(ar_handle_t h) {
   cudaGetDevice(&prev);
   if (prev != h->device) cudaSetDevice(h->device);
   if (cudaDeviceSynchronize() != cudaSuccess) st = AR_ERR_CUDA;
-  if (h->scratch && cudaFree(h->scratch) != cudaSuccess) st = AR_ERR_CUDA;
-  if (h->ring && cudaFree(h->ring) != cudaSuccess) st = AR_ERR_CUDA;
-  if (h->rscratch && cudaFree(h->rscratch) != cudaSuccess) st = AR_ERR_CUDA;
+  for (void* b : h->region_base)
+    if (b && cudaFree(b) != cudaSuccess) st = AR_ERR_CUDA;
   if (h->state && cudaFree(h->state) != cudaSuccess) st = AR_ERR_CUDA;
   if (h->staging && cudaFree(h->staging) != cudaSuccess) st = AR_ERR_CUDA;
   if (h->staging_tables && cudaFree(h->staging_tables) != cudaSuccess) st = AR_ERR_CUDA;
@@ -733,6 +762,25 @@ ar_status_t ar_get_device_status(ar_handle_t h, void* stream) {
   if (cudaMemcpy(&h->state->error, zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
     return AR_ERR_CUDA;
   return host.error == ar::kDevErrTimeout ? AR_ERR_TIMEOUT : AR_ERR_CUDA;
+}
+
+ar_status_t ar_debug_check_guards(ar_handle_t h, int* intact) {
+  if (!h || !intact) return AR_ERR_INVALID_ARG;
+  *intact = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) return AR_ERR_CUDA;
+  std::vector<unsigned char> buf(kGuardBytes);
+  for (int i = 0; i < 3; ++i) {
+    if (!h->region_base[i]) continue;
+    const char* base = static_cast<const char*>(h->region_base[i]);
+    for (const char* g : {base, base + kGuardBytes + h->region_bytes[i]}) {
+      if (cudaMemcpy(buf.data(), g, kGuardBytes, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return AR_ERR_CUDA;
+      for (unsigned char c : buf)
+        if (c != kGuardByte) return AR_OK;
+    }
+  }
+  *intact = 1;
+  return AR_OK;
 }
 
 ar_status_t ar_last_timeout(ar_handle_t h, int* waiting_rank, int* missing_rank,

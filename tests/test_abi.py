@@ -64,6 +64,7 @@ def test_null_handle_calls(lib):
     assert lib.ar_set_spin_limit_ns(None, 10 ** 6) == _lib.AR_ERR_INVALID_ARG
     assert lib.ar_get_device_status(None, None) == _lib.AR_ERR_INVALID_ARG
     assert lib.ar_last_timeout(None, None, None, None) == _lib.AR_ERR_INVALID_ARG
+    assert lib.ar_debug_check_guards(None, None) == _lib.AR_ERR_INVALID_ARG
     assert lib.ar_query(None, None) == _lib.AR_ERR_INVALID_ARG
     assert lib.ar_reserve_host_staging(None) == _lib.AR_ERR_INVALID_ARG
     assert lib.ar_debug_skip_producer(None, 0) == _lib.AR_ERR_INVALID_ARG

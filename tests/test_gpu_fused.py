@@ -355,4 +355,5 @@ def test_forced_packet_modes_on_ragged_counts(mode, variant, ranks, monkeypatch)
                 torch.cuda.synchronize()
                 G.check_all_outputs(outs, G.oracle_expect(xs), "%s %s R=%d count=%d call %d"
                                     % (variant, mode, ranks, count, call))
+        assert h.debug_guards_intact(), "a packet store landed outside its region"
         assert h.device_status() == AR_OK

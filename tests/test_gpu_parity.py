@@ -34,6 +34,7 @@ def test_ragged_counts(variant, R):
         want = G.oracle_expect(xs)
         outs = G.run_variant(ar, G.to_device(xs), variant)
         G.check_all_outputs(outs, want, "%s R=%d count=%d" % (variant, R, count))
+    assert ar.debug_guards_intact(), "%s R=%d wrote outside a packet region" % (variant, R)
 
 
 FULL = ["r8_4096", "r8_440x5120", "r8_512x5120", "r8_512x7168", "r8_512x8192",
@@ -60,6 +61,7 @@ def test_full_size_configs(name):
             G.run_variant(ar, xd, variant, outs)
             G.check_all_outputs(outs, want, "%s %s seed=%d" % (name, variant, seed))
         del xd, outs
+    assert ar.debug_guards_intact(), "%s: a write outside a packet region" % name
     torch.cuda.empty_cache()
 
 
@@ -144,7 +146,8 @@ def test_in_place(variant):
 
 @pytest.mark.parametrize("variant", G.PARITY_VARIANTS)
 def test_guard_canaries(variant):
-    """Nothing is written outside [0, count) of any output."""
+    """Nothing is written outside [0, count) of any output, nor outside the
+    handle's packet regions."""
     R, count, pad = 8, 1000 * 8 + 5, 64
     ar = G.handle(R, count)
     xs = inputs.make_inputs(R, count, seed=2, fill="normal")
@@ -158,6 +161,7 @@ def test_guard_canaries(variant):
     for b in bases:
         bits = G.device_bits(b)
         assert (bits[:pad] == canary).all() and (bits[pad + count:] == canary).all()
+    assert ar.debug_guards_intact()
 
 
 def test_back_to_back_calls_with_changing_inputs():
