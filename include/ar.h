@@ -65,7 +65,14 @@
  * AR_PDL=0, read by ar_create, turns this off.  The two pipelined fused
  * kernels (AR_FUSED_LL8, AR_FUSED_LL8_STAGED) are launched this way at every
  * size unless AR_PDL=0 or AR_FUSED_PDL=0; the three-launch packet form never
- * is.
+ * is.  Such a kernel reads the two pointer tables (not the buffers they
+ * point to) before that wait, so the table round trip overlaps the previous
+ * kernel's tail.  Hence a precondition: the tables must not be written by
+ * the kernel just before the call in the same stream if that kernel lets
+ * its dependents start early (griddepcontrol.launch_dependents) before it
+ * writes them.  Tables written by a copy, a memset, any kernel without such
+ * a trigger, or an earlier call of this library (which never writes them)
+ * are safe.
  *
  * Streams are passed as `void*` holding a cudaStream_t (NULL = the legacy
  * default stream), so that this header needs no CUDA header.

@@ -459,11 +459,11 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, Fuse
   __shared__ char* s_out[R];
   __shared__ uint32_t s_epoch;
   __shared__ int s_misaligned;
-  // Launched with programmatic dependent launch: wait until the previous
-  // kernel in the stream has completed and its writes (the epoch among
-  // them) are visible, then let the next one be scheduled.
-  pdl_enter();
-  // Pointer tables and the call's epoch, read in one step.  Flag rotation at
+  // Launched with programmatic dependent launch.  The caller's pointer
+  // tables are read first, overlapping the previous kernel's tail; then the
+  // kernel waits until that kernel has completed and its writes (the epoch
+  // among them) are visible, and lets the next one be scheduled, before it
+  // reads the epoch or touches any input, output or packet.  Flag rotation at
   // arrival: thread 2R reads the epoch and counts its CTA in with one 64-bit
   // atomic on {epoch, done}; the CTA whose count completes the grid writes
   // {next epoch, 0} in one 64-bit store at its end, so no CTA waits on
@@ -482,7 +482,9 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, Fuse
     char* p = a.out_tbl[threadIdx.x - R];
     s_out[threadIdx.x - R] = p;
     if (reinterpret_cast<uintptr_t>(p) & 15u) atomicOr(&s_misaligned, 1);
-  } else if (threadIdx.x == 2 * R) {
+  }
+  pdl_enter();
+  if (threadIdx.x == 2 * R) {
     const uint64_t old = atom_add_relaxed_u64(epoch_done(f.state), 1ull << 32);
     s_epoch = (uint32_t)old;
     arrival = (uint32_t)(old >> 32);

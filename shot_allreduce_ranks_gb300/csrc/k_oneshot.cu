@@ -78,10 +78,13 @@ __device__ __forceinline__ void fanout_wide(const CallArgs& a, const char* const
 
 template <int R, class E>
 __global__ void __launch_bounds__(512) k_oneshot_fanout(CallArgs a) {
-  pdl_enter();
   __shared__ const char* s_in[R];
   __shared__ char* s_out[R];
+  // The caller's pointer tables are read before waiting for the previous
+  // kernel in the stream (programmatic dependent launch), so that round trip
+  // overlaps its tail; inputs and outputs are touched only after the wait.
   const bool vec = load_tables<R>(a, s_in, s_out);
+  pdl_enter();
   if constexpr (R <= 8) {
     if (vec && a.groups >= kWideMinGroups) {
       bool all32 = true;
@@ -136,11 +139,14 @@ __global__ void __launch_bounds__(512) k_oneshot_fanout(CallArgs a) {
 // chunk write every output instead (the fan-out order, alias-safe).
 template <int R, class E>
 __global__ void __launch_bounds__(512) k_oneshot_pull(CallArgs a) {
-  pdl_enter();
   __shared__ const char* s_in[R];
   __shared__ char* s_out[R];
   __shared__ int s_alias;
+  // The caller's pointer tables are read before waiting for the previous
+  // kernel in the stream (programmatic dependent launch), so that round trip
+  // overlaps its tail; inputs and outputs are touched only after the wait.
   const bool vec = load_tables<R>(a, s_in, s_out);
+  pdl_enter();
   if (threadIdx.x == 0) {
     int alias = 0;
     for (int r = 0; r < R; ++r)

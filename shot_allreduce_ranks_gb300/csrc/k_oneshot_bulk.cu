@@ -154,13 +154,16 @@ __device__ __forceinline__ void bulk_issue(uint8_t* in_tiles, const char* const*
 
 template <int R, class E>
 __global__ void __launch_bounds__(kBulkThreads) k_oneshot_fanout_bulk(CallArgs a) {
-  pdl_enter();
   constexpr int S = bulk_stages<R>();
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full[S];
   __shared__ const char* s_in[R];
   __shared__ char* s_out[R];
+  // The caller's pointer tables are read before waiting for the previous
+  // kernel in the stream (programmatic dependent launch), so that round trip
+  // overlaps its tail; inputs and outputs are touched only after the wait.
   const bool vec = load_tables<R>(a, s_in, s_out);
+  pdl_enter();
   const int tid = threadIdx.x;
 
   if (!vec) {  // element path: some pointer is not 16-byte aligned

@@ -25,10 +25,13 @@ namespace {
 
 template <int R, class E>
 __global__ void __launch_bounds__(512) k_reduce_scatter(CallArgs a) {
-  pdl_enter();
   __shared__ const char* s_in[R];
   __shared__ char* s_out[R];
+  // The caller's pointer tables are read before waiting for the previous
+  // kernel in the stream (programmatic dependent launch), so that round trip
+  // overlaps its tail; inputs and outputs are touched only after the wait.
   const bool vec = load_tables<R>(a, s_in, s_out) && (a.count % E::kGroup == 0);
+  pdl_enter();
   const int r = blockIdx.y;
   const size_t base = (size_t)r * a.count * E::kBytes;  // byte offset of block r
   const size_t stride = (size_t)gridDim.x * blockDim.x;
@@ -47,10 +50,13 @@ __global__ void __launch_bounds__(512) k_reduce_scatter(CallArgs a) {
 
 template <int R, class E>
 __global__ void __launch_bounds__(512) k_all_gather(CallArgs a) {
-  pdl_enter();
   __shared__ const char* s_in[R];
   __shared__ char* s_out[R];
+  // The caller's pointer tables are read before waiting for the previous
+  // kernel in the stream (programmatic dependent launch), so that round trip
+  // overlaps its tail; inputs and outputs are touched only after the wait.
   const bool vec = load_tables<R>(a, s_in, s_out) && (a.count % E::kGroup == 0);
+  pdl_enter();
   const int s = blockIdx.y;
   const size_t base = (size_t)s * a.count * E::kBytes;  // byte offset of block s in every output
   const size_t stride = (size_t)gridDim.x * blockDim.x;

@@ -21,10 +21,13 @@ namespace {
 // CTA b works for owner b % R on chunk b / R (gridDim.x is a multiple of R).
 template <int R, class E>
 __global__ void __launch_bounds__(512) k_twophase_reduce(CallArgs a) {
-  pdl_enter();
   __shared__ const char* s_in[R];
   __shared__ char* s_out[R];
+  // The caller's pointer tables are read before waiting for the previous
+  // kernel in the stream (programmatic dependent launch), so that round trip
+  // overlaps its tail; inputs and outputs are touched only after the wait.
   const bool vec = load_tables<R>(a, s_in, s_out);
+  pdl_enter();
   const int o = (int)(blockIdx.x % R);
   const size_t g0 = (size_t)o * a.shard_groups;
   if (g0 >= a.groups) return;
@@ -46,10 +49,13 @@ __global__ void __launch_bounds__(512) k_twophase_reduce(CallArgs a) {
 
 template <int R, class E>
 __global__ void __launch_bounds__(512) k_twophase_broadcast(CallArgs a) {
-  pdl_enter();
   __shared__ const char* s_in[R];
   __shared__ char* s_out[R];
+  // The caller's pointer tables are read before waiting for the previous
+  // kernel in the stream (programmatic dependent launch), so that round trip
+  // overlaps its tail; inputs and outputs are touched only after the wait.
   const bool vec = load_tables<R>(a, s_in, s_out);
+  pdl_enter();
   const int o = (int)(blockIdx.x % R);
   const size_t g0 = (size_t)o * a.shard_groups;
   if (g0 >= a.groups) return;

@@ -455,3 +455,37 @@ def test_fanout_large_call_grid(R, count):
     G.check_all_outputs(outs, want, "fanout R=%d count=%d" % (R, count))
     assert ar.device_status() == 0
     ar.set_variant("auto")
+
+
+@pytest.mark.parametrize("variant", ["oneshot_pull", "oneshot_fanout", "twophase", "fused_ll8",
+                                     "fused_ll8_staged", "oneshot_fanout_bulk"])
+def test_tables_rewritten_by_copies_between_back_to_back_calls(variant):
+    """One pair of device pointer tables, rewritten by a host-to-device copy
+    on the call's stream before each of six back-to-back calls (no
+    synchronisation in between; small calls, so launched with programmatic
+    dependent launch, whose kernels read the tables before waiting for the
+    previous kernel): each call must use its own tables."""
+    R, count, calls = 8, 4096 * 3 + 5, 6
+    ar = G.handle(R, count)
+    ar.set_variant(variant)
+    xs = [inputs.make_inputs(R, count, seed=900 + c) for c in range(calls)]
+    ins = [G.to_device(x) for x in xs]
+    outs = [[torch.empty(count, dtype=torch.bfloat16, device=G.DEV) for _ in range(R)]
+            for _ in range(calls)]
+    tin = torch.empty(R, dtype=torch.int64, device=G.DEV)
+    tout = torch.empty(R, dtype=torch.int64, device=G.DEV)
+    hosts = [(torch.tensor([t.data_ptr() for t in ins[c]], dtype=torch.int64).pin_memory(),
+              torch.tensor([t.data_ptr() for t in outs[c]], dtype=torch.int64).pin_memory())
+             for c in range(calls)]
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        for c in range(calls):
+            tin.copy_(hosts[c][0], non_blocking=True)
+            tout.copy_(hosts[c][1], non_blocking=True)
+            ar.allreduce_tables(tin, tout, count, s)
+    s.synchronize()
+    for c in range(calls):
+        G.check_all_outputs(outs[c], G.oracle_expect(xs[c]), "%s call %d" % (variant, c))
+    assert ar.device_status() == 0
+    ar.set_variant("auto")
