@@ -48,11 +48,13 @@ struct TuneRow {
 // a number of bytes per rank: fp16 crosses where bf16 does, fp32 at half
 // the element count (R = 8: pull 2.91 vs 2.99 us at 32 Ki; 3.36 vs 3.10 at
 // 64 Ki), about 1.75 MiB / R per rank.  At R = 16 (bf16) the bulk-copy
-// fan-out beats the register fan-out from 64 Ki to 128 Ki elements (4.63 vs
-// 5.27 us, 5.18 vs 5.72) and not above (6.46 vs 6.40 at 256 Ki, 14.79 vs
-// 13.37 at 1 Mi).  Rows are generated per (R, element size) from these rules.
+// fan-out beats the register fan-out from 64 Ki to 256 Ki elements (3.75 vs
+// 4.32 us, 4.16 vs 4.84, 5.11 vs 5.56) and not above (9.26 vs 8.52 at
+// 512 Ki, 14.81 vs 13.41 at 1 Mi), hence its end near the geometric mean of
+// 256 Ki and 512 Ki (360 Ki elements).  Rows are generated per (R, element
+// size) from these rules.
 constexpr size_t kPullCrossoverBytesTimesR = 917504 * 2;
-constexpr size_t kBulkMaxBytesR16 = 131072 * 2;
+constexpr size_t kBulkMaxBytesR16 = 368640 * 2;
 
 std::vector<TuneRow> builtin_table(int R, size_t elem_bytes) {
   const size_t pull_max = kPullCrossoverBytesTimesR / elem_bytes / (size_t)R / 64 * 64;

@@ -282,12 +282,12 @@ def test_host_buffer_path():
 @pytest.mark.parametrize("R", [2, 4, 8, 16])
 def test_selector_boundaries_bracket_the_measured_crossover(R, dtype):
     """Pull up to about 1.75 MiB / R per rank (fp32: half the elements of
-    bf16/fp16), then fan-out; at R = 16 the bulk-copy fan-out up to 256 KiB
+    bf16/fp16), then fan-out; at R = 16 the bulk-copy fan-out up to 720 KiB
     per rank first."""
     from shot_allreduce_ranks_gb300 import AllReduce
     eb = 4 if dtype == torch.float32 else 2
     edge = 917504 * 2 // eb // R // 64 * 64
-    bulk_edge = 262144 // eb if R >= 16 else edge
+    bulk_edge = 368640 * 2 // eb if R >= 16 else edge
     with AllReduce(R, max(edge, bulk_edge) + 4096, dtype=dtype) as ar:
         assert ar.select(1) == "oneshot_pull"
         assert ar.select(edge) == "oneshot_pull"
