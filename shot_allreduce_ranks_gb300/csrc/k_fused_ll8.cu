@@ -483,12 +483,6 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, Fuse
     s_out[threadIdx.x - R] = p;
     if (reinterpret_cast<uintptr_t>(p) & 15u) atomicOr(&s_misaligned, 1);
   }
-  pdl_enter();
-  if (threadIdx.x == 2 * R) {
-    const uint64_t old = atom_add_relaxed_u64(epoch_done(f.state), 1ull << 32);
-    s_epoch = (uint32_t)old;
-    arrival = (uint32_t)(old >> 32);
-  }
   // CTA c is clique c; its warp group r (Tr threads, a multiple of 32)
   // stands for virtual rank r.
   const size_t Tr = blockDim.x / R;
@@ -528,9 +522,14 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, Fuse
     s_in_off[r][q - 1] = (uint32_t)o * Vs32;
     s_dst_off[r][q - 1] = (uint32_t)(o * (R - 1) + (r < o ? r : r - 1)) * sstride;
   }
-  __syncthreads();
+  __syncthreads();  // tables and offsets visible; all of this overlapped the previous kernel
+  pdl_enter();
+  if (threadIdx.x == 2 * R) {
+    const uint64_t old = atom_add_relaxed_u64(epoch_done(f.state), 1ull << 32);
+    s_epoch = (uint32_t)old;
+    arrival = (uint32_t)(old >> 32);
+  }
   const bool vec = s_misaligned == 0;
-  const uint32_t epoch = s_epoch;
   // Fast body: tiles [jt, jt + Tr) with jt + Tr <= fast_vs are whole groups
   // in every shard (the last shard is the shortest).
   const size_t whole = a.count / E::kGroup;
@@ -538,6 +537,24 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, Fuse
       (vec && f.fast32 && whole > (size_t)(R - 1) * Vs) ? min(Vs, whole - (size_t)(R - 1) * Vs)
                                                         : 0;
   const char* my_in = s_in[r];
+  // The input slices of round k are loaded during iteration k - 1, right
+  // after that iteration's packet stores (when their registers are free), so
+  // their HBM latency overlaps the reduce of iteration k - 1.  Round 0's are
+  // issued here, before the epoch's round trip completes.
+  uint4 x[RO];
+  auto load_slices = [&](size_t kk) {
+    const uint32_t js = (uint32_t)((c + kk * C) * Tr + t);
+#pragma unroll
+    for (int q = 0; q < R - 1; ++q)
+      x[q] = ld_v4_stream<true>(my_in + (size_t)(s_in_off[r][q] + js) * kGroupBytes, pol_in);
+  };
+  {
+    const size_t nf0 = fast_vs / Tr;
+    const bool whole0 = nf0 > c;  // round 0 of this clique is a whole tile
+    if (scatter_on && whole0 && K > 0) load_slices(0);
+  }
+  __syncthreads();  // the epoch
+  const uint32_t epoch = s_epoch;
   // Slot of (owner r, i-th other source in rank order): r * (R - 1) + i.
   const uint32_t src_row = (uint32_t)(r * (R - 1)) * sstride;
   const uint32_t own_off = (uint32_t)r * Vs32;
@@ -565,17 +582,6 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, Fuse
 
   bool ok = true;
   size_t k = 0;
-  // The input slices of round k are loaded during iteration k - 1, right
-  // after that iteration's packet stores (when their registers are free), so
-  // their HBM latency overlaps the reduce of iteration k - 1.
-  uint4 x[RO];
-  auto load_slices = [&](size_t kk) {
-    const uint32_t js = (uint32_t)((c + kk * C) * Tr + t);
-#pragma unroll
-    for (int q = 0; q < R - 1; ++q)
-      x[q] = ld_v4_stream<true>(my_in + (size_t)(s_in_off[r][q] + js) * kGroupBytes, pol_in);
-  };
-  if (scatter_on && k_fast > 0 && K > 0) load_slices(0);
   for (; k < k_fast; ++k) {
     // ---------------- whole tiles: 32-bit offsets, no per-group checks
     const size_t jts = (c + k * C) * Tr;                       // scatter tile (round k)
