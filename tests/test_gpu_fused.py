@@ -357,3 +357,41 @@ def test_forced_packet_modes_on_ragged_counts(mode, variant, ranks, monkeypatch)
                                     % (variant, mode, ranks, count, call))
         assert h.debug_guards_intact(), "a packet store landed outside its region"
         assert h.device_status() == AR_OK
+
+
+@pytest.mark.parametrize("variant,count,calls", [("fused_ll8", 4096 * 3 + 5, 200_000),
+                                                 ("fused_ll8", 65_536 * 8 + 11, 20_000),
+                                                 ("fused_ll8_staged", 4096 * 3 + 5, 50_000)])
+def test_soak_many_graph_replayed_calls(variant, count, calls):
+    """Many back-to-back calls replayed from one CUDA graph of 1000 calls (the
+    epoch advancing on every one): no packet wait may run out, the epoch must
+    have moved by the number of calls, and the last call's outputs are
+    bit-exact."""
+    R = 8
+    ar = G.handle(R, count)
+    ar.set_variant(variant)
+    xs = inputs.make_inputs(R, count, seed=77)
+    bufs = G.to_device(xs)
+    outs = [torch.empty_like(b) for b in bufs]
+    in_tbl, out_tbl = ar.tables(bufs, outs)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        ar.allreduce_tables(in_tbl, out_tbl, count)
+    torch.cuda.synchronize()
+    per_graph = 1000
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(per_graph):
+            ar.allreduce_tables(in_tbl, out_tbl, count)
+    torch.cuda.synchronize()
+    e0 = ar.debug_get_epoch()
+    for o in outs:
+        o.zero_()
+    for _ in range(calls // per_graph):
+        g.replay()
+    torch.cuda.synchronize()
+    assert ar.device_status() == AR_OK
+    assert ar.debug_get_epoch() == _flag_after(e0, (calls // per_graph) * per_graph)
+    G.check_all_outputs(outs, G.oracle_expect(xs), "%s after %d calls" % (variant, calls))
+    ar.set_variant("fused_ll8")
