@@ -245,7 +245,7 @@ class ClockSampler:
 
 
 class NvmlClocks:
-    """SM clock and clock-event reasons read through NVML (the driver's
+    """SM clock and clock-event reasons read through NVML (NVIDIA's
     libnvidia-ml, plain ctypes) by a background thread every ~0.2 ms, so that
     even a timed region of a millisecond holds samples.  Read-only queries."""
 
