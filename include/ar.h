@@ -286,7 +286,10 @@ ar_status_t ar_get_device_status(ar_handle_t h, void* stream);
  * *waiting_rank = the virtual rank whose packet wait gave up first,
  * *missing_rank = the lowest-numbered rank whose packets (scatter packets,
  * or result packets without write mode) it was still missing, *waits = how
- * many waits gave up before the others saw the call abandoned.  All -1 / 0
+ * many waits gave up before the others saw the call abandoned.  Waits for
+ * result packets run twice the spin limit, so when a producer stores nothing
+ * it is a wait for that producer's scatter packets that runs out first and
+ * the producer that is named.  All -1 / 0
  * if no timeout has been reported.  AR_ERR_INVALID_ARG for a NULL argument.
  * Source: no counterpart on the pages; it names the peer that a bounded poll
  * (the summary of meta-pytorch/torchcomms #3850) gave up on, which a

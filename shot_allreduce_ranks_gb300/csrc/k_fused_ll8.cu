@@ -205,12 +205,16 @@ __device__ __forceinline__ Lane packet_prologue(const CallArgs& a, const FusedAr
 // waiter of the same call (identified by its base epoch) has given up.
 // Entry i stands for position base + i in the list of sources; with
 // skip >= 0 that list holds only the other ranks (position p is source
-// p < skip ? p : p + 1), otherwise position s is source s.
+// p < skip ? p : p + 1), otherwise position s is source s.  limit_mul
+// stretches the limits for waits on packets that are sent only after their
+// sender's own wait succeeded (result packets), so that when a producer is
+// missing, a wait on its own packets runs out first and is the one reported.
 template <int N, bool kCta = false, class Ptr>
 __device__ __forceinline__ bool wait_packets_at(const FusedArgs& f, Packets4 (&pk)[N],
                                                 uint32_t pending, uint32_t flag,
                                                 uint32_t call_epoch, int who, Ptr ptr,
-                                                int skip = -1, int base = 0) {
+                                                int skip = -1, int base = 0,
+                                                uint32_t limit_mul = 1) {
 #pragma unroll
   for (int s = 0; s < N; ++s)
     if ((pending & (1u << s)) && pk[s].arrived(flag)) pending &= ~(1u << s);
@@ -229,7 +233,8 @@ __device__ __forceinline__ bool wait_packets_at(const FusedArgs& f, Packets4 (&p
     if (pending && (++spins & 15u) == 0) {
       const uint64_t now = global_timer_ns();
       if (spins == 16u) t_first = now;
-      if (spins > kMaxSpins || (spins > 16u && now - t_first > f.spin_limit_ns)) {
+      if (spins / limit_mul > kMaxSpins ||
+          (spins > 16u && now - t_first > f.spin_limit_ns * limit_mul)) {
         pending <<= base;
         if (skip >= 0)
           pending = (pending & ((1u << skip) - 1u)) | ((pending >> skip) << (skip + 1));
@@ -659,7 +664,8 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, Fuse
           if (rv && R > 1) {
             ok = ok && wait_packets_at<kN, kWriteMode>(
                            f, rk, (1u << n) - 1u, epoch, epoch, r,
-                           [&](int i) { return rrow + (size_t)(i0 + i) * sstride * 4; }, r, i0);
+                           [&](int i) { return rrow + (size_t)(i0 + i) * sstride * 4; }, r, i0,
+                           2u);
             if (ok) {
 #pragma unroll
               for (int i = 0; i < kN; ++i)
@@ -756,7 +762,8 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, Fuse
           const uint64_t* const p = slot_ptr<R>(f.rscratch, f.slot_groups, r, o) + jq * 4;
           Packets4 rk[1];
           rk[0].load<kWriteMode>(p);
-          ok = wait_packets_at<1, kWriteMode>(f, rk, 1u, epoch, epoch, r, [&](int) { return p; }, -1, o);
+          ok = wait_packets_at<1, kWriteMode>(f, rk, 1u, epoch, epoch, r, [&](int) { return p; }, -1, o,
+                                              2u);
           if (ok) store_group<E>(s_out[r], g, rk[0].data(), group_valid<E>(g, a.count), vec);
         }
       }
