@@ -149,15 +149,42 @@ KERNEL_SOURCES = {
 }
 
 
+def strip_comments(src: str) -> str:
+    """C/C++/CUDA source without its comments, trailing blanks and empty
+    lines (string and character literals are kept whole)."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            out.append(" ")
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    lines = (l.rstrip() for l in "".join(out).split("\n"))
+    return "\n".join(l for l in lines if l)
+
+
 def kernel_source_digest(kernel: str) -> str:
-    """Digest of the sources a kernel is compiled from (its file and the
-    shared device header)."""
+    """Digest of the code a kernel is compiled from (its file and the shared
+    device header), comments left out: a profile stays valid across edits
+    of comments only."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "shot_allreduce_ranks_gb300", "csrc")
     for name in ("ar_internal.cuh", KERNEL_SOURCES[kernel]):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + b"\0" + f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            h.update(name.encode() + b"\0" + strip_comments(f.read()).encode())
     return h.hexdigest()[:16]
 
 

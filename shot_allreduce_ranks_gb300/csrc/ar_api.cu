@@ -239,6 +239,15 @@ int occupancy(ar_ctx* h, int variant, int threads) {
   return cache[k] > 0 ? cache[k] : 0;
 }
 
+// Threads per rank of a fused launch: the request split over R warp groups,
+// narrowed while the kernel cannot start a CTA of that size (the write-mode
+// kernel for R <= 4 is compiled for at most 256 threads).
+int fused_tr(ar_ctx* h, int variant, int threads) {
+  int tr = ar::fused_rank_threads(h->R, threads);
+  while (tr > 32 && occupancy(h, variant, h->R * tr) == 0) tr -= 32;
+  return tr;
+}
+
 constexpr int kMaxRingRounds = 3;  // rings are sized for lead 2 (lead + 1 rounds)
 
 // 32-byte packet groups one CTA's ring needs: `rounds` rounds of R(R-1)
@@ -346,7 +355,7 @@ LaunchCfg shape(ar_ctx* h, int variant, const TuneRow* row, size_t groups, size_
     case AR_FUSED_LL8_STAGED: {
       // One clique per CTA: R warp groups of Tr threads; a persistent grid of
       // at most the co-resident CTAs, at most one per tile of Tr groups.
-      const int tr = ar::fused_rank_threads(R, c.threads > 0 ? c.threads : h->fused_threads);
+      const int tr = fused_tr(h, variant, c.threads > 0 ? c.threads : h->fused_threads);
       c.threads = R * tr;
       const size_t limit =
           std::max<size_t>(1, (size_t)occupancy(h, variant, c.threads) * (size_t)h->num_sms);
@@ -570,7 +579,7 @@ ar_status_t ar_create(int R, size_t max_count, int dtype, ar_handle_t* out) {
   h->scratch_bytes =
       packets ? (size_t)R * (size_t)(R - 1) * h->slot_groups * 4 * sizeof(uint64_t) : 0;
   h->fused_ctas_per_sm =
-      packets ? occupancy(h, AR_FUSED_LL8, R * ar::fused_rank_threads(R, h->fused_threads)) : 0;
+      packets ? occupancy(h, AR_FUSED_LL8, R * fused_tr(h, AR_FUSED_LL8, h->fused_threads)) : 0;
   if (ar::bulk_prepare(R, dtype) == cudaSuccess) h->bulk_ctas_per_sm = ar::bulk_ctas_per_sm(R, dtype);
   cudaGetLastError();
 
@@ -602,7 +611,7 @@ ar_status_t ar_create(int R, size_t max_count, int dtype, ar_handle_t* out) {
   if (st == AR_OK && packets && R > 1) {
     size_t cap = 0;
     for (int threads : {h->fused_threads, 512}) {
-      const int tr = ar::fused_rank_threads(R, threads);
+      const int tr = fused_tr(h, AR_FUSED_LL8, threads);
       const size_t ctas = std::min((size_t)occupancy(h, AR_FUSED_LL8, R * tr) * (size_t)sms,
                                    ceil_div(h->slot_groups, (size_t)tr));
       cap = std::max(cap, ctas * ring_groups_per_cta(R, kMaxRingRounds, tr));
@@ -683,7 +692,7 @@ ar_status_t ar_query(ar_handle_t h, ar_info_t* info) {
   info->scratch_bytes = 2 * h->scratch_bytes + h->ring_groups * 32;
   info->num_sms = h->num_sms;
   info->fused_max_ctas = h->fused_ctas_per_sm * h->num_sms;
-  info->fused_threads = h->R * ar::fused_rank_threads(h->R, h->fused_threads);
+  info->fused_threads = h->R * fused_tr(h, AR_FUSED_LL8, h->fused_threads);
   info->device = h->device;
   return AR_OK;
 }

@@ -62,6 +62,21 @@ namespace ar {
 namespace {
 
 constexpr int kFusedMaxThreads = 512;
+// The write-mode kernel for R <= 4 is compiled for at most 256 threads and
+// three CTAs per SM (80 registers instead of 128, a third clique per SM).
+// Against the 128-register build (R = 4, bf16, graph replay) it is faster
+// from about 2 Mi elements per rank up (10.7 vs 11.3 us at 2.2 Mi, 18.3 vs
+// 19.7 at 4 Mi, 63.3 vs 68.5 at 16 Mi, 133.7 vs 138.5 at 32 Mi; R = 3 at
+// 4 Mi 14.3 vs 19.2) and slower below, where a CTA has one or two tiles
+// (4.8 vs 4.2 us at 512 Ki, 7.4 vs 6.7 at 1 Mi, with any grid; the one-shot
+// kernels serve those sizes).  The form without write mode keeps the wider
+// bound: at 80 registers its receive spills and it was 9-20% slower.  Host
+// code finds the limit through fused_ctas_per_sm (zero CTAs per SM above
+// it).
+template <int R, bool kWriteMode>
+constexpr int fused_bound_threads() { return kWriteMode && R <= 4 ? 256 : kFusedMaxThreads; }
+template <int R, bool kWriteMode>
+constexpr int fused_bound_ctas() { return kWriteMode && R <= 4 ? 3 : 1; }
 constexpr uint32_t kMaxSpins = 1u << 24;
 
 __device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {
@@ -458,7 +473,8 @@ __device__ __noinline__ void producer_delay(uint64_t ns) {
 // end of each iteration.  By induction on i every wait is eventually
 // satisfied.  The waits are bounded all the same.
 template <int R, class E, bool kWriteMode = true>
-__global__ void __launch_bounds__(kFusedMaxThreads) k_fused_ll8(CallArgs a, FusedArgs f) {
+__global__ void __launch_bounds__(fused_bound_threads<R, kWriteMode>(),
+                                  fused_bound_ctas<R, kWriteMode>()) k_fused_ll8(CallArgs a, FusedArgs f) {
   constexpr int RO = R > 1 ? R - 1 : 1;  // entries for the other ranks
   __shared__ const char* s_in[R];
   __shared__ char* s_out[R];
@@ -814,17 +830,29 @@ __global__ void __launch_bounds__(kFusedMaxThreads) k_packet_recv(CallArgs a, Fu
 
 namespace {
 
+// CTAs per SM of `threads` threads; zero above the kernel's launch bound,
+// which the occupancy query alone does not report.
+template <class Kernel>
+cudaError_t occ_within_bound(Kernel kernel, int threads, int* n) {
+  cudaFuncAttributes fa;
+  const cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
+  if (e != cudaSuccess) return e;
+  if (threads > fa.maxThreadsPerBlock) {
+    *n = 0;
+    return cudaSuccess;
+  }
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, kernel, threads, 0);
+}
+
 cudaError_t occ_fused(int R, int dtype, int threads, int* n) {
-#define Q(RR, EE) \
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, k_fused_ll8<RR, EE>, threads, 0)
+#define Q(RR, EE) return occ_within_bound(k_fused_ll8<RR, EE>, threads, n)
   AR_DISPATCH(dtype, R, Q, AR_SWITCH_R8)
 #undef Q
   return cudaErrorInvalidValue;
 }
 
 cudaError_t occ_staged(int R, int dtype, int threads, int* n) {
-#define Q(RR, EE) \
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, k_fused_ll8<RR, EE, false>, threads, 0)
+#define Q(RR, EE) return occ_within_bound(k_fused_ll8<RR, EE, false>, threads, n)
   AR_DISPATCH(dtype, R, Q, AR_SWITCH_R8)
 #undef Q
   return cudaErrorInvalidValue;

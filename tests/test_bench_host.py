@@ -166,3 +166,18 @@ def test_write_tuning_writes_the_library_format(tmp_path):
     lines = path.read_text().splitlines()
     assert lines[0].startswith("#")
     assert lines[1:] == ["8 92681 oneshot_pull", "8 1099511627776 oneshot_fanout"]
+
+
+def test_strip_comments_keeps_code_and_literals():
+    src = ('int a = 1;  // one\n'
+           '/* a block\n   over lines */ const char* s = "x // y /* z */";\n'
+           "char q = '\"';  /* inline */ int b;\n"
+           '\n'
+           '   // alone\n')
+    out = bench.strip_comments(src)
+    assert out == ('int a = 1;\n  const char* s = "x // y /* z */";\n'
+                   "char q = '\"';    int b;")
+    # a code change shows, a comment change does not
+    assert bench.strip_comments(src.replace("one", "uno")) == out
+    assert bench.strip_comments(src.replace("b;", "c;")) != out
+

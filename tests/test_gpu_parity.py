@@ -187,11 +187,15 @@ def test_back_to_back_calls_with_changing_inputs():
         G.check_all_outputs(snap, want, "call %d" % call)
 
 
-def test_fused_launch_shapes():
+@pytest.mark.parametrize("R", [8, 4, 3])
+def test_fused_launch_shapes(R):
     """The fused kernel is correct for every CTA count it can be given,
-    down to one CTA per rank, and for 128/256/512 threads."""
-    R, count = 8, 200_003
+    down to one CTA per rank, and for 128/256/512 threads (narrowed to 256
+    for R <= 4, the bound that kernel is compiled for)."""
+    count = 200_003
     ar = G.handle(R, count)
+    if R <= 4:
+        assert ar.query().fused_threads <= 256
     xs = inputs.make_inputs(R, count, seed=9, fill="normal")
     want = G.oracle_expect(xs)
     xd = G.to_device(xs)
