@@ -260,7 +260,9 @@ ar_status_t ar_select(ar_handle_t h, size_t count, int* variant);
  * number of CTAs (each one clique of R warp groups), clamped to the
  * co-resident limit (and, in ring mode, to the packet rings' room), and
  * threads is rounded to R warp groups of a multiple of 32 threads each (at
- * least 32); for the other variants ctas is the grid (the grid-stride CTA
+ * least 32), narrowed where the kernel is compiled for fewer (AR_FUSED_LL8
+ * for R <= 4 launches at most 256 threads); for the other variants ctas is
+ * the grid (the grid-stride CTA
  * count; a multiple of R for the pull, two-phase and three-launch packet
  * kernels).  threads must be a multiple of 32 in [64, 512]
  * (the packet and fan-out kernels accept 128..512). */
