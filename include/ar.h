@@ -193,7 +193,7 @@ ar_status_t ar_create(int R, size_t max_count, int dtype, ar_handle_t* out);
  * Allocates nothing, synchronises nothing, so it can be captured into a CUDA
  * graph; the fused kernel's epoch lives on the device and rotates on every
  * execution, including graph replays (by one per call, or, when the kernel
- * keeps its packets in per-CTA rings -- messages of several L2 sizes -- by
+ * keeps its packets in per-CTA rings -- more than two L2 sizes of packets -- by
  * its number of rounds, one flag per round).
  * Errors: AR_ERR_INVALID_ARG (NULL handle or table, count > max_count),
  * AR_ERR_UNSUPPORTED (a packet variant forced with R > 8), AR_ERR_CUDA

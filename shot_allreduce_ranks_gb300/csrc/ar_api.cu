@@ -93,13 +93,16 @@ struct ar_ctx {
   int delay_rank = -1;         // skewed-producer test hook (persists until cleared)
   uint64_t delay_ns = 0;
   // Packet handling of the write-mode fused kernel, chosen per call from the
-  // bytes of packets P = 32 R (R-1) groups-per-shard (measured at R = 8 on
-  // GB300, graph replay): P <= L2/2: packets written into the message-sized
-  // scratch stay in L2 between calls, so they are left there (22.8 vs 23.5 us
-  // at 440x5120 with drops); L2/2 < P <= 3 L2: the scratch, with each
-  // consumed line dropped from L2 (38.5 vs 45.6 us at 512x8192 without
-  // drops); P > 3 L2: per-CTA rings of lead + 1 rounds with lead 1 (138.7 vs
-  // 145.5 us at 16 Mi elements, 269 vs 285 us at 32 Mi).  Without write mode
+  // bytes of packets P = 32 R (R-1) groups-per-shard (measured on GB300,
+  // graph replay): P <= L2/2: packets written into the message-sized
+  // scratch stay in L2 between calls, so they are left there (R = 8: 22.8 vs
+  // 23.5 us at 440x5120 with drops); L2/2 < P <= 2 L2: the scratch, with
+  // each consumed line dropped from L2 (R = 8: 38.5 vs 45.6 us at 512x8192
+  // without drops); P > 2 L2: per-CTA rings of lead + 1 rounds with lead 1
+  // (R = 8: 86.8 vs 88.2 us at 10 Mi elements, 103.1 vs 105.4 at 12 Mi,
+  // 138.7 vs 145.5 at 16 Mi; R = 4: 90.9 vs 97.9 at 24 Mi, 119.9 vs 134.2 at
+  // 32 Mi; below 2 L2 the two were within 3% either way at R = 3 and 4, and
+  // the scratch won by 8% at R = 2, 32-48 Mi).  Without write mode
   // (AR_FUSED_LL8_STAGED) the result packets double P, there are no rings,
   // and the lead is 1 (69.1 vs 72.5 us at 512x8192, 530 vs 621 us at 32 Mi
   // elements, 7.0 vs 7.5 us at 4 Ki).  The AR_FUSED_RING, AR_FUSED_DISCARD
@@ -274,7 +277,7 @@ FusedMode fused_mode(const ar_ctx* h, size_t shard_groups, int tr, bool write_mo
   const int ring_lead = h->fused_lead > 0 ? h->fused_lead : 1;
   const bool ring = write_mode && h->ring &&
                     h->ring_groups >= ring_groups_per_cta(h->R, ring_lead + 1, tr) &&
-                    (h->fused_ring == 1 || (h->fused_ring < 0 && P > 3.0 * l2));
+                    (h->fused_ring == 1 || (h->fused_ring < 0 && P > 2.0 * l2));
   FusedMode m;
   m.lead = h->fused_lead > 0 ? h->fused_lead : (ring || !write_mode ? 1 : 2);
   m.ring_rounds = ring ? m.lead + 1 : 0;
@@ -470,6 +473,9 @@ ar_status_t launch(ar_ctx* h, int variant, const TuneRow* row, const void* const
       f.delay_rank = h->delay_rank;
       f.delay_ns = h->delay_ns;
       h->skip_producer = -1;
+      if (h->log)
+        fprintf(stderr, "[ar]   packets: lead=%d discard=%d ring_rounds=%d\n", f.lead, f.discard,
+                f.ring_rounds);
       const int dt = h->dtype;
       e = variant == AR_FUSED_LL8          ? ar::launch_fused_ll8(h->R, dt, a, f, cfg, s)
           : variant == AR_FUSED_LL8_STAGED ? ar::launch_fused_ll8_staged(h->R, dt, a, f, cfg, s)
