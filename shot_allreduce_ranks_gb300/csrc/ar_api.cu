@@ -96,10 +96,14 @@ struct ar_ctx {
   // bytes of packets P = 32 R (R-1) groups-per-shard (measured on GB300,
   // graph replay): P <= L2/2: packets written into the message-sized
   // scratch stay in L2 between calls, so they are left there (R = 8: 22.8 vs
-  // 23.5 us at 440x5120 with drops); L2/2 < P <= 2 L2: the scratch, with
-  // each consumed line dropped from L2 (R = 8: 38.5 vs 45.6 us at 512x8192
-  // without drops); P > 2 L2: per-CTA rings of lead + 1 rounds with lead 1
-  // (R = 8: 86.8 vs 88.2 us at 10 Mi elements, 103.1 vs 105.4 at 12 Mi,
+  // 23.5 us at 440x5120 with drops, where packets, inputs and outputs come
+  // to 135 MB); L2/2 < P <= 2 L2, or P plus the 4RN bytes of inputs and
+  // outputs above 1.1 L2: the scratch, with each consumed line dropped from
+  // L2 (R = 8: 38.5 vs 45.6 us at 512x8192 without drops; 67 MB of packets
+  // at R = 3, 8 Mi elements: 25.3 vs 30.7 us, and at R = 2, 16 Mi: 35.7 vs
+  // 39.9, with 168 and 201 MB in all); P > 2 L2: per-CTA rings of lead + 1
+  // rounds with lead 1 (R = 8: 86.8 vs 88.2 us at 10 Mi elements, 103.1 vs
+  // 105.4 at 12 Mi,
   // 138.7 vs 145.5 at 16 Mi; R = 4: 90.9 vs 97.9 at 24 Mi, 119.9 vs 134.2 at
   // 32 Mi; below 2 L2 the two were within 3% either way at R = 3 and 4, and
   // the scratch won by 8% at R = 2, 32-48 Mi).  Without write mode
@@ -281,7 +285,12 @@ FusedMode fused_mode(const ar_ctx* h, size_t shard_groups, int tr, bool write_mo
   FusedMode m;
   m.lead = h->fused_lead > 0 ? h->fused_lead : (ring || !write_mode ? 1 : 2);
   m.ring_rounds = ring ? m.lead + 1 : 0;
-  m.discard = ring ? 0 : h->fused_discard >= 0 ? h->fused_discard : (P > 0.5 * l2 ? 1 : 0);
+  // Write mode also drops the lines when packets, inputs and outputs
+  // together (P + 4RN bytes; 32 R^2 bytes per shard group for the last two)
+  // overflow L2.
+  const double io = 32.0 * h->R * h->R * (double)shard_groups;
+  const bool drop = P > 0.5 * l2 || (write_mode && P + io > 1.1 * l2);
+  m.discard = ring ? 0 : h->fused_discard >= 0 ? h->fused_discard : (drop ? 1 : 0);
   return m;
 }
 
