@@ -103,14 +103,13 @@ struct ar_ctx {
   // at R = 3, 8 Mi elements: 25.3 vs 30.7 us, and at R = 2, 16 Mi: 35.7 vs
   // 39.9, with 168 and 201 MB in all); P > 2 L2: per-CTA rings of lead + 1
   // rounds with lead 1 (R = 8: 86.8 vs 88.2 us at 10 Mi elements, 103.1 vs
-  // 105.4 at 12 Mi,
-  // 138.7 vs 145.5 at 16 Mi; R = 4: 90.9 vs 97.9 at 24 Mi, 119.9 vs 134.2 at
-  // 32 Mi; below 2 L2 the two were within 3% either way at R = 3 and 4, and
-  // the scratch won by 8% at R = 2, 32-48 Mi).  Without write mode
-  // (AR_FUSED_LL8_STAGED) the result packets double P, there are no rings,
-  // and the lead is 1 (69.1 vs 72.5 us at 512x8192, 530 vs 621 us at 32 Mi
-  // elements, 7.0 vs 7.5 us at 4 Ki).  The AR_FUSED_RING, AR_FUSED_DISCARD
-  // and AR_FUSED_LEAD environment variables force a choice.
+  // 105.4 at 12 Mi, 138.7 vs 145.5 at 16 Mi; R = 4: 90.9 vs 97.9 at 24 Mi,
+  // 119.9 vs 134.2 at 32 Mi; below 2 L2 the two were within 3% either way at
+  // R = 3 and 4, and the scratch won by 8% at R = 2, 32-48 Mi).  Without
+  // write mode (AR_FUSED_LL8_STAGED) the result packets double P, there are
+  // no rings, and the lead is 1 (69.1 vs 72.5 us at 512x8192, 530 vs 621 us
+  // at 32 Mi elements, 7.0 vs 7.5 us at 4 Ki).  The AR_FUSED_RING,
+  // AR_FUSED_DISCARD and AR_FUSED_LEAD environment variables force a choice.
   int fused_lead = 0;          // tiles scattered ahead of the reduce (0: automatic)
   int fused_discard = -1;      // -1 automatic, 0 never, 1 always (scratch mode)
   int l2_bytes = 0;
