@@ -395,3 +395,49 @@ def test_soak_many_graph_replayed_calls(variant, count, calls):
     assert ar.debug_get_epoch() == _flag_after(e0, (calls // per_graph) * per_graph)
     G.check_all_outputs(outs, G.oracle_expect(xs), "%s after %d calls" % (variant, calls))
     ar.set_variant("fused_ll8")
+
+
+# Packet handling the handle picks per call on a GB300 (its L2 size decides):
+# (R, elements per rank) -> (lead, line drops, ring rounds).  The benchmark
+# sizes, and the measured crossovers of the rules (scratch left alone while
+# packets, inputs and outputs fit L2; drops above; rings above 2 L2 of
+# packets).
+AUTO_MODES = [
+    (8, 2_252_800, (2, 0, 0)),    # 440x5120: 63 MB of packets, 135 MB in all
+    (8, 4_194_304, (2, 1, 0)),    # 512x8192: 117 MB of packets
+    (8, 10_485_760, (1, 0, 2)),   # 294 MB of packets, above 2 L2
+    (8, 33_554_432, (1, 0, 2)),   # 64 MiB per rank
+    (4, 4_194_304, (2, 0, 0)),    # 50 MB of packets, 117 MB in all
+    (4, 33_554_432, (1, 0, 2)),   # 64 MiB per rank: 403 MB of packets
+    (3, 8_388_608, (2, 1, 0)),    # 67 MB of packets, 168 MB in all
+]
+
+
+@pytest.mark.parametrize("R_, count, want", AUTO_MODES)
+def test_automatic_packet_mode(R_, count, want, monkeypatch, capfd):
+    """The call's packet handling, as AR_LOG reports it, is the one the
+    measured rules give for this size; the call is still correct."""
+    import re
+
+    from shot_allreduce_ranks_gb300 import AllReduce
+    for k in ("AR_FUSED_RING", "AR_FUSED_DISCARD", "AR_FUSED_LEAD"):
+        monkeypatch.delenv(k, raising=False)
+    monkeypatch.setenv("AR_LOG", "1")
+    bufs = [torch.full((count,), float(r + 1), dtype=torch.bfloat16, device=G.DEV)
+            for r in range(R_)]
+    outs = [torch.empty_like(b) for b in bufs]
+    with AllReduce(R_, count) as h:
+        h.set_variant("fused_ll8")
+        capfd.readouterr()
+        h(bufs, outs)
+        torch.cuda.synchronize()
+        assert h.device_status() == AR_OK
+    err = capfd.readouterr().err
+    m = re.search(r"packets: lead=(\d+) discard=(\d+) ring_rounds=(\d+)", err)
+    assert m, err
+    assert tuple(int(x) for x in m.groups()) == want
+    total = float(R_ * (R_ + 1) // 2)  # exact in bf16 for R <= 8
+    for o in outs:
+        assert bool((o == total).all())
+    del bufs, outs
+    torch.cuda.empty_cache()
