@@ -328,7 +328,7 @@ def test_ring_mode_missing_producer_times_out_and_recovers(ring_handle, skip):
 @pytest.mark.parametrize("mode,variant", [("drop", "fused_ll8"), ("ring", "fused_ll8"),
                                           ("drop", "fused_ll8_staged"),
                                           ("drop_lead1", "fused_ll8_staged")])
-@pytest.mark.parametrize("ranks", [3, 8])
+@pytest.mark.parametrize("ranks", [3, 4, 8])
 def test_forced_packet_modes_on_ragged_counts(mode, variant, ranks, monkeypatch):
     """The line drops (their boundary: only lines holding a group below the
     shard's end are dropped; without write mode, also the result packets'
